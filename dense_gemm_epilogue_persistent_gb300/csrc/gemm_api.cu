@@ -1,0 +1,531 @@
+// Host side of the C ABI declared in include/gemm_gb300.h: argument
+// validation, kernel-configuration planning, TMA tensor-map encoding and the
+// cluster launch of the persistent kernel.
+//
+// Validation follows the "Constraints" list of "custom_epilogue_dense_gemm.py"
+// (A and B share one type; the contiguous dimension of every tensor is 16-byte
+// aligned) and the cuBLASDx Blackwell card's "alignment_unfulfilled" error;
+// the shared-memory ring accounting follows that card's "Depth and shared
+// memory" bullets (stage = (M*K + N*K) * sizeof(input); 8 bytes per barrier,
+// two per stage and two per tensor-memory stage; a 4-byte tensor-memory
+// handle) and its opt-in limit check against
+// cudaDevAttrMaxSharedMemoryPerBlockOptin before launching.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "gemm_gb300.h"
+#include "gemm_kernel.cuh"
+#include "kernels.h"
+
+#define GEMM_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+using gb300::KernelParams;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+constexpr uint64_t kDefaultTimeoutNs = 4000000000ull;
+constexpr int kMaxStages = 12;
+constexpr int kSmemSlack = 1024 + 16;   // base alignment + abort flag
+
+struct VariantState {
+  int smem_set = 0;          // dynamic smem attribute last set
+  int max_clusters = 0;      // occupancy for that smem size
+};
+
+}  // namespace
+
+struct gemm_handle {
+  int device = 0;
+  int sm_count = 0;
+  int smem_optin = 0;
+  EncodeTiledFn encode = nullptr;
+  uint32_t* d_status = nullptr;
+  bool forced = false;
+  gemm_config_t forced_cfg{};
+  gemm_config_t last{};
+  uint64_t timeout_ns = kDefaultTimeoutNs;
+  VariantState variants[2][2][2];   // [ab 16/8][cta_group 1/2][tile_n 128/256]
+  std::mutex mu;
+};
+
+namespace {
+
+int dtype_bytes(int dt) {
+  switch (dt) {
+    case GEMM_F32: return 4;
+    case GEMM_F16: return 2;
+    case GEMM_BF16: return 2;
+    case GEMM_E4M3: return 1;
+  }
+  return 0;
+}
+
+bool is_epi_type(int dt) { return dt == GEMM_F32 || dt == GEMM_F16 || dt == GEMM_BF16; }
+bool is_ab_type(int dt) { return dt == GEMM_F16 || dt == GEMM_BF16 || dt == GEMM_E4M3; }
+bool is_layout(int v) { return v == GEMM_K_MAJOR || v == GEMM_MN_MAJOR; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool reads_c(const gemm_problem_t& p) { return p.beta != 0.0f; }
+bool reads_x(const gemm_problem_t& p) { return p.X != nullptr && p.x_factor != 0.0f; }
+
+gemm_status_t validate(const gemm_problem_t* pp) {
+  if (!pp) return GEMM_ERR_INVALID_ARG;
+  const gemm_problem_t& p = *pp;
+  const gemm_dtypes_t& t = p.dtypes;
+  if (p.M < 0 || p.N < 0 || p.K < 0 || p.L < 0) return GEMM_ERR_INVALID_ARG;
+  const int64_t kMax = INT32_MAX;
+  if (p.M > kMax || p.N > kMax || p.K > kMax || p.L > kMax) return GEMM_ERR_INVALID_ARG;
+  if (!is_layout(p.layoutA) || !is_layout(p.layoutB) || !is_layout(t.cdxy_major))
+    return GEMM_ERR_INVALID_ARG;
+  if (!is_ab_type(t.ab) || !is_epi_type(t.c) || !is_epi_type(t.d) || !is_epi_type(t.x) ||
+      !is_epi_type(t.y))
+    return GEMM_ERR_UNSUPPORTED_DTYPE;
+  if (p.M == 0 || p.N == 0 || p.L == 0) return GEMM_OK;   // nothing to compute
+
+  // Sizes the kernel indexes with 32-bit tile ids and 64-bit element offsets.
+  if (cdiv(p.M, 128) * cdiv(p.N, 128) * p.L > kMax) return GEMM_ERR_INVALID_ARG;
+  if ((double)p.M * (double)p.N * (double)p.L > 9.0e15) return GEMM_ERR_INVALID_ARG;
+
+  // Outputs and epilogue inputs: packed, one major order.
+  const bool m_major = t.cdxy_major == GEMM_MN_MAJOR;
+  const int64_t ld = m_major ? p.M : p.N;
+  if (!p.D) return GEMM_ERR_INVALID_ARG;
+  if (reads_c(p) && !p.C) return GEMM_ERR_INVALID_ARG;
+  auto cd_ok = [&](const void* ptr, int dt) {
+    return aligned16(ptr) && (ld * dtype_bytes(dt)) % 16 == 0;
+  };
+  if (!cd_ok(p.D, t.d)) return GEMM_ERR_MISALIGNED;
+  if (p.Y && !cd_ok(p.Y, t.y)) return GEMM_ERR_MISALIGNED;
+  if (reads_c(p) && !cd_ok(p.C, t.c)) return GEMM_ERR_MISALIGNED;
+  if (reads_x(p) && !cd_ok(p.X, t.x)) return GEMM_ERR_MISALIGNED;
+  if (p.C && p.C == p.D && reads_c(p) && t.c != t.d) return GEMM_ERR_INVALID_ARG;
+
+  if (p.K > 0) {
+    if (!p.A || !p.B) return GEMM_ERR_INVALID_ARG;
+    const int64_t es = dtype_bytes(t.ab);
+    const int64_t a_min = p.layoutA == GEMM_K_MAJOR ? p.K : p.M;
+    const int64_t b_min = p.layoutB == GEMM_K_MAJOR ? p.K : p.N;
+    if (p.lda < a_min || p.ldb < b_min) return GEMM_ERR_INVALID_ARG;
+    if (!aligned16(p.A) || !aligned16(p.B)) return GEMM_ERR_MISALIGNED;
+    if ((p.lda * es) % 16 != 0 || (p.ldb * es) % 16 != 0) return GEMM_ERR_MISALIGNED;
+    // Tensor-map limits: strides below 2^40 bytes.
+    const int64_t a_rows = p.layoutA == GEMM_K_MAJOR ? p.M : p.K;
+    const int64_t b_rows = p.layoutB == GEMM_K_MAJOR ? p.N : p.K;
+    const double lim = 1099511627776.0;   // 2^40
+    if ((double)p.lda * es * a_rows >= lim || (double)p.ldb * es * b_rows >= lim)
+      return GEMM_ERR_INVALID_ARG;
+  }
+  return GEMM_OK;
+}
+
+int ring_bytes(int cta_group, int tile_n, int ab_bytes, int stages) {
+  const int stage = 128 * 128 + (tile_n / cta_group) * 128;   // A + B, 128-byte rows
+  return stages * stage + 8 * (2 * stages + 2 * gb300::kAccStages) + 4;
+}
+
+bool variant_supports(const gemm_problem_t& p, int cg, int bn) {
+  if (cg != 1 && cg != 2) return false;
+  if (bn != 128 && bn != 256) return false;
+  const int ab_bytes = dtype_bytes(p.dtypes.ab);
+  const int atom = 128 / ab_bytes;
+  // MN-major B is staged in swizzle atoms of `atom` rows per CTA.
+  if (p.layoutB == GEMM_MN_MAJOR && (bn / cg) % atom != 0) return false;
+  if (p.layoutA == GEMM_MN_MAJOR && 128 % atom != 0) return false;
+  return true;
+}
+
+// Relative cost of running `tiles` tiles of one variant: full waves of
+// 128 x tile_n work per SM, weighted by how close the variant's shared-memory
+// operand traffic comes to the SM's read bandwidth.
+double plan_cost(int64_t tiles, int cg, int bn, int sm_count) {
+  const int64_t units = std::max(1, sm_count / cg);
+  const double waves = (double)cdiv(tiles, units);
+  double eff = 1.0;
+  if (cg == 1 && bn == 256) eff = 1.06;
+  if (cg == 2 && bn == 128) eff = 1.12;
+  if (cg == 1 && bn == 128) eff = 1.25;
+  return waves * bn * eff;
+}
+
+gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
+                   const gemm_config_t* forced, gemm_config_t* out) {
+  gemm_status_t st = validate(pp);
+  if (st != GEMM_OK) return st;
+  if (!out || sm_count <= 0 || smem_optin <= 0) return GEMM_ERR_INVALID_ARG;
+  const gemm_problem_t& p = *pp;
+  const int ab_bytes = dtype_bytes(p.dtypes.ab);
+
+  int cg = forced ? forced->cta_group : 0;
+  int bn = forced ? forced->tile_n : 0;
+  if (cg || bn) {
+    const int cgs[2] = {1, 2}, bns[2] = {128, 256};
+    double best = 1e300;
+    int bcg = 0, bbn = 0;
+    for (int a : cgs)
+      for (int b : bns) {
+        if ((cg && a != cg) || (bn && b != bn)) continue;
+        if (!variant_supports(p, a, b)) continue;
+        const int64_t tiles = cdiv(std::max<int64_t>(p.M, 1), 128 * a) *
+                              cdiv(std::max<int64_t>(p.N, 1), b) * std::max<int64_t>(p.L, 1);
+        const double c = plan_cost(tiles, a, b, sm_count);
+        if (c < best) { best = c; bcg = a; bbn = b; }
+      }
+    if (!bcg) return GEMM_ERR_UNSUPPORTED_CONFIG;
+    cg = bcg;
+    bn = bbn;
+  } else {
+    double best = 1e300;
+    for (int a : {2, 1})
+      for (int b : {256, 128}) {
+        if (!variant_supports(p, a, b)) continue;
+        const int64_t tiles = cdiv(std::max<int64_t>(p.M, 1), 128 * a) *
+                              cdiv(std::max<int64_t>(p.N, 1), b) * std::max<int64_t>(p.L, 1);
+        const double c = plan_cost(tiles, a, b, sm_count);
+        if (c < best - 1e-9) { best = c; cg = a; bn = b; }
+      }
+    if (!cg) return GEMM_ERR_UNSUPPORTED_CONFIG;
+  }
+  if (gemm_tmem_columns(128, bn) * gb300::kAccStages > (int)gb300::kTmemCols)
+    return GEMM_ERR_UNSUPPORTED_CONFIG;
+
+  const int budget = smem_optin - kSmemSlack;
+  int max_stages = 0;
+  while (max_stages < kMaxStages && ring_bytes(cg, bn, ab_bytes, max_stages + 1) <= budget)
+    ++max_stages;
+  int stages = forced && forced->stages ? forced->stages : max_stages;
+  if (stages < 2 || stages > max_stages) return GEMM_ERR_UNSUPPORTED_CONFIG;
+
+  const int64_t tiles_m = cdiv(std::max<int64_t>(p.M, 1), 128 * cg);
+  const int64_t tiles_n = cdiv(std::max<int64_t>(p.N, 1), bn);
+  const int64_t tiles = tiles_m * tiles_n * std::max<int64_t>(p.L, 1);
+  int group_m = forced && forced->group_m ? forced->group_m : 8;
+  group_m = (int)std::max<int64_t>(1, std::min<int64_t>(group_m, tiles_m));
+
+  gemm_config_t c{};
+  c.cta_group = cg;
+  c.tile_n = bn;
+  c.stages = stages;
+  c.group_m = group_m;
+  c.tile_m = 128 * cg;
+  c.tile_k = 128 / ab_bytes;
+  c.acc_stages = gb300::kAccStages;
+  c.ring_bytes = ring_bytes(cg, bn, ab_bytes, stages);
+  // At least half the opt-in limit: one CTA per SM, so no two CTAs ever
+  // contend for the 512 tensor-memory columns each allocates.
+  c.smem_bytes = std::max(c.ring_bytes + kSmemSlack, smem_optin / 2 + 1024);
+  c.tiles = tiles;
+  const int64_t units = std::max(1, sm_count / cg);
+  c.grid_ctas = (int)(std::min<int64_t>(tiles, units) * cg);
+  *out = c;
+  return GEMM_OK;
+}
+
+CUtensorMapDataType tma_type(int dt) {
+  switch (dt) {
+    case GEMM_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    case GEMM_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    default: return CU_TENSOR_MAP_DATA_TYPE_UINT8;   // fp8: bytes, never converted
+  }
+}
+
+// Operand tensor map.  K-major: dims {K, rows, L}, box {tile_k, box_rows}.
+// MN-major: dims {rows, K, L}, box {128 bytes of rows, tile_k}.
+// Out-of-range elements of a box are filled with zeros.
+bool encode_operand(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int dt, int64_t rows,
+                    int64_t K, int64_t L, int64_t ld, bool mn_major, int box_rows, int tile_k) {
+  const int64_t es = dtype_bytes(dt);
+  cuuint64_t dims[3], strides[2];
+  cuuint32_t box[3], estr[3] = {1, 1, 1};
+  if (!mn_major) {
+    dims[0] = (cuuint64_t)K; dims[1] = (cuuint64_t)rows; dims[2] = (cuuint64_t)L;
+    strides[0] = (cuuint64_t)(ld * es);
+    strides[1] = (cuuint64_t)(ld * es * rows);
+    box[0] = (cuuint32_t)tile_k; box[1] = (cuuint32_t)box_rows; box[2] = 1;
+  } else {
+    dims[0] = (cuuint64_t)rows; dims[1] = (cuuint64_t)K; dims[2] = (cuuint64_t)L;
+    strides[0] = (cuuint64_t)(ld * es);
+    strides[1] = (cuuint64_t)(ld * es * K);
+    box[0] = (cuuint32_t)(128 / es); box[1] = (cuuint32_t)tile_k; box[2] = 1;
+  }
+  CUresult r = enc(map, tma_type(dt), 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+uint32_t make_idesc(int ab, int cg, int bn, bool a_mn, bool b_mn) {
+  // kind::f16: A/B format 0 = fp16, 1 = bf16.  kind::f8f6f4: 0 = e4m3.
+  const uint32_t fmt = (ab == GEMM_BF16) ? 1u : 0u;
+  uint32_t d = 0;
+  d |= 1u << 4;                                   // accumulator (D) format: fp32
+  d |= fmt << 7;                                  // A format
+  d |= fmt << 10;                                 // B format
+  d |= (a_mn ? 1u : 0u) << 15;                    // A MN-major
+  d |= (b_mn ? 1u : 0u) << 16;                    // B MN-major
+  d |= (uint32_t)(bn >> 3) << 17;                 // N >> 3
+  d |= (uint32_t)((128 * cg) >> 4) << 24;         // M >> 4
+  return d;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+
+GEMM_API const char* gemm_status_string(gemm_status_t s) {
+  switch (s) {
+    case GEMM_OK: return "GEMM_OK";
+    case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG";
+    case GEMM_ERR_UNSUPPORTED_DTYPE: return "GEMM_ERR_UNSUPPORTED_DTYPE";
+    case GEMM_ERR_MISALIGNED: return "GEMM_ERR_MISALIGNED";
+    case GEMM_ERR_UNSUPPORTED_ARCH: return "GEMM_ERR_UNSUPPORTED_ARCH";
+    case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA";
+    case GEMM_ERR_DEVICE_TIMEOUT: return "GEMM_ERR_DEVICE_TIMEOUT";
+    case GEMM_ERR_UNSUPPORTED_CONFIG: return "GEMM_ERR_UNSUPPORTED_CONFIG";
+  }
+  return "GEMM_ERR_UNKNOWN";
+}
+
+GEMM_API int gemm_tmem_columns(int tile_m, int tile_n) {
+  if (tile_m <= 0 || tile_n <= 0 || tile_m > 256 || tile_n > 256) return 0;
+  if (tile_m % 64 != 0 || tile_n % 8 != 0) return 0;
+  const int blocks = (tile_m % 128 == 0) ? tile_m / 128 : tile_m / 64;
+  return blocks * tile_n;
+}
+
+GEMM_API gemm_status_t gemm_check(const gemm_problem_t* p) { return validate(p); }
+
+GEMM_API gemm_status_t gemm_plan(const gemm_problem_t* p, int sm_count, int smem_optin,
+                                 const gemm_config_t* forced, gemm_config_t* out) {
+  return plan(p, sm_count, smem_optin, forced, out);
+}
+
+GEMM_API gemm_status_t gemm_create(gemm_handle_t* out, int device) {
+  if (!out) return GEMM_ERR_INVALID_ARG;
+  *out = nullptr;
+  int count = 0;
+  if (cudaGetDeviceCount(&count) != cudaSuccess) { cudaGetLastError(); return GEMM_ERR_CUDA; }
+  if (device < 0 || device >= count) return GEMM_ERR_INVALID_ARG;
+  int major = 0, minor = 0, sms = 0, optin = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) !=
+          cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  if (major != 10 || minor != 3) return GEMM_ERR_UNSUPPORTED_ARCH;
+
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+
+  int prev = 0;
+  cudaGetDevice(&prev);
+  if (cudaSetDevice(device) != cudaSuccess) { cudaGetLastError(); return GEMM_ERR_CUDA; }
+  uint32_t* status = nullptr;
+  cudaError_t e = cudaMalloc(&status, sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaMemset(status, 0, sizeof(uint32_t));
+  cudaSetDevice(prev);
+  if (e != cudaSuccess) {
+    if (status) cudaFree(status);
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  gemm_handle* h = new gemm_handle();
+  h->device = device;
+  h->sm_count = sms;
+  h->smem_optin = optin;
+  h->encode = reinterpret_cast<EncodeTiledFn>(fn);
+  h->d_status = status;
+  *out = h;
+  return GEMM_OK;
+}
+
+GEMM_API gemm_status_t gemm_destroy(gemm_handle_t h) {
+  if (!h) return GEMM_OK;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(h->device);
+  cudaFree(h->d_status);
+  cudaSetDevice(prev);
+  delete h;
+  return GEMM_OK;
+}
+
+GEMM_API gemm_status_t gemm_set_config(gemm_handle_t h, const gemm_config_t* cfg) {
+  if (!h) return GEMM_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> g(h->mu);
+  if (!cfg) {
+    h->forced = false;
+    return GEMM_OK;
+  }
+  if ((cfg->cta_group && cfg->cta_group != 1 && cfg->cta_group != 2) ||
+      (cfg->tile_n && cfg->tile_n != 128 && cfg->tile_n != 256) || cfg->stages < 0 ||
+      cfg->stages > kMaxStages || cfg->group_m < 0)
+    return GEMM_ERR_INVALID_ARG;
+  h->forced = true;
+  h->forced_cfg = *cfg;
+  return GEMM_OK;
+}
+
+GEMM_API gemm_status_t gemm_last_config(gemm_handle_t h, gemm_config_t* out) {
+  if (!h || !out) return GEMM_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> g(h->mu);
+  *out = h->last;
+  return GEMM_OK;
+}
+
+GEMM_API gemm_status_t gemm_set_timeout_ns(gemm_handle_t h, uint64_t ns) {
+  if (!h) return GEMM_ERR_INVALID_ARG;
+  h->timeout_ns = ns ? ns : kDefaultTimeoutNs;
+  return GEMM_OK;
+}
+
+GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, int64_t L,
+                                const void* A, int64_t lda, gemm_layout_t layoutA, const void* B,
+                                int64_t ldb, gemm_layout_t layoutB, const void* C, const void* X,
+                                void* D, void* Y, float alpha, float beta, float x_factor,
+                                const gemm_dtypes_t* dtypes, struct CUstream_st* stream) {
+  if (!h || !dtypes) return GEMM_ERR_INVALID_ARG;
+  gemm_problem_t p{M, N, K, L, A, lda, layoutA, B, ldb, layoutB, C, X, D, Y,
+                   alpha, beta, x_factor, *dtypes};
+  gemm_status_t st = validate(&p);
+  if (st != GEMM_OK) return st;
+  if (M == 0 || N == 0 || L == 0) return GEMM_OK;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device) {
+    cudaGetLastError();
+    return GEMM_ERR_INVALID_ARG;
+  }
+
+  std::lock_guard<std::mutex> guard(h->mu);
+  gemm_config_t cfg{};
+  st = plan(&p, h->sm_count, h->smem_optin, h->forced ? &h->forced_cfg : nullptr, &cfg);
+  if (st != GEMM_OK) return st;
+
+  const int ab_bytes = dtype_bytes(dtypes->ab);
+  const void* kern = ab_bytes == 2 ? gb300::kernel_ab16(cfg.cta_group, cfg.tile_n)
+                                   : gb300::kernel_ab8(cfg.cta_group, cfg.tile_n);
+  if (!kern) return GEMM_ERR_UNSUPPORTED_CONFIG;
+  VariantState& vs =
+      h->variants[ab_bytes == 2 ? 0 : 1][cfg.cta_group - 1][cfg.tile_n == 256 ? 1 : 0];
+
+  cudaLaunchConfig_t lc{};
+  cudaLaunchAttribute attr[1];
+  lc.blockDim = dim3(gb300::kThreads);
+  lc.dynamicSmemBytes = (size_t)cfg.smem_bytes;
+  lc.stream = reinterpret_cast<cudaStream_t>(stream);
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cfg.cta_group;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+
+  if (vs.smem_set != cfg.smem_bytes) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             cfg.smem_bytes) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_CUDA;
+    }
+    int nclusters = 0;
+    lc.gridDim = dim3((unsigned)(cfg.cta_group * h->sm_count));
+    if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &lc) != cudaSuccess || nclusters <= 0) {
+      cudaGetLastError();
+      return GEMM_ERR_CUDA;
+    }
+    vs.smem_set = cfg.smem_bytes;
+    vs.max_clusters = nclusters;
+  }
+  const int64_t clusters = std::min<int64_t>(cfg.tiles, vs.max_clusters);
+  cfg.grid_ctas = (int)(clusters * cfg.cta_group);
+  lc.gridDim = dim3((unsigned)cfg.grid_ctas);
+
+  const bool a_mn = layoutA == GEMM_MN_MAJOR, b_mn = layoutB == GEMM_MN_MAJOR;
+  CUtensorMap tmA, tmB;
+  std::memset(&tmA, 0, sizeof(tmA));
+  std::memset(&tmB, 0, sizeof(tmB));
+  if (K > 0) {
+    if (!encode_operand(h->encode, &tmA, A, dtypes->ab, M, K, L, lda, a_mn, 128, cfg.tile_k) ||
+        !encode_operand(h->encode, &tmB, B, dtypes->ab, N, K, L, ldb, b_mn,
+                        cfg.tile_n / cfg.cta_group, cfg.tile_k))
+      return GEMM_ERR_CUDA;
+  }
+
+  KernelParams kp{};
+  kp.M = (int)M; kp.N = (int)N; kp.K = (int)K; kp.L = (int)L;
+  kp.tiles_m = (int)cdiv(M, cfg.tile_m);
+  kp.tiles_n = (int)cdiv(N, cfg.tile_n);
+  kp.num_tiles = (int)cfg.tiles;
+  kp.k_blocks = (int)cdiv(K, cfg.tile_k);
+  kp.group_m = cfg.group_m;
+  kp.stages = cfg.stages;
+  kp.a_mn_major = a_mn;
+  kp.b_mn_major = b_mn;
+  kp.idesc = make_idesc(dtypes->ab, cfg.cta_group, cfg.tile_n, a_mn, b_mn);
+  kp.status = h->d_status;
+  kp.timeout_ns = h->timeout_ns;
+  kp.epi.C = C;
+  kp.epi.X = X;
+  kp.epi.D = D;
+  kp.epi.Y = Y;
+  kp.epi.c_dt = dtypes->c;
+  kp.epi.d_dt = dtypes->d;
+  kp.epi.x_dt = dtypes->x;
+  kp.epi.y_dt = dtypes->y;
+  kp.epi.cd_m_major = dtypes->cdxy_major == GEMM_MN_MAJOR;
+  kp.epi.read_c = reads_c(p);
+  kp.epi.read_x = reads_x(p);
+  kp.epi.write_y = Y != nullptr;
+  kp.epi.alpha = alpha;
+  kp.epi.beta = beta;
+  kp.epi.x_factor = x_factor;
+
+  void* args[3] = {&tmA, &tmB, &kp};
+  if (cudaLaunchKernelExC(&lc, kern, args) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  h->last = cfg;
+  return GEMM_OK;
+}
+
+GEMM_API gemm_status_t gemm_sync_status(gemm_handle_t h, struct CUstream_st* stream,
+                                        uint32_t* detail) {
+  if (!h) return GEMM_ERR_INVALID_ARG;
+  if (detail) *detail = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) { cudaGetLastError(); return GEMM_ERR_CUDA; }
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, h->d_status, sizeof(word), cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  if (detail) *detail = word;
+  if (word != 0) {
+    cudaMemsetAsync(h->d_status, 0, sizeof(uint32_t), s);
+    cudaStreamSynchronize(s);
+    return GEMM_ERR_DEVICE_TIMEOUT;
+  }
+  return GEMM_OK;
+}

@@ -1,0 +1,184 @@
+/*
+ * gemm_gb300.h -- C ABI of the GB300 (sm_103a) persistent batched GEMM with a
+ * fused custom epilogue.
+ *
+ * Operation (for every batch l < L, row m < M, column n < N):
+ *
+ *     acc       = sum_k A(m,k,l) * B(n,k,l)        fp32 accumulation
+ *     Y(m,n,l)  = acc                              (optional output)
+ *     D(m,n,l)  = alpha*acc + beta*C(m,n,l) + x_factor*X(m,n,l)   (fp32 epilogue)
+ *
+ * Sources: "custom_epilogue_dense_gemm.py" (CuTeDSL Blackwell example), module
+ * docstring "Y = A * B", "D = (A * B) * alpha + C * beta + X * x_factor", its
+ * "Tensor dimensions" list (A is MxKxL, B is NxKxL, C/D/X/Y are MxNxL and share
+ * one major order) and its "Constraints" list (A and B share one type; the
+ * contiguous dimension of every tensor is 16-byte aligned);
+ * "04_mma_tma_2sm_sm100.cu" (CuTe Blackwell tutorial 04), header comment
+ * "D (f32) = beta * C (F32) + alpha * A (F16) * B (F16)".
+ *
+ * Memory: every tensor pointer is a DEVICE pointer on the handle's device,
+ * owned by the caller; the library never allocates, frees or retains them.
+ *
+ * Layouts (element strides; ld = leading dimension in elements):
+ *   A, GEMM_K_MAJOR : A(m,k,l) at (l*M + m)*lda + k      (lda >= K)
+ *   A, GEMM_MN_MAJOR: A(m,k,l) at (l*K + k)*lda + m      (lda >= M)
+ *   B, GEMM_K_MAJOR : B(n,k,l) at (l*N + n)*ldb + k      (ldb >= K)
+ *   B, GEMM_MN_MAJOR: B(n,k,l) at (l*K + k)*ldb + n      (ldb >= N)
+ *   C/D/X/Y are packed; dtypes->cdxy_major selects
+ *     GEMM_K_MAJOR (row-major, "N-major"): (l*M + m)*N + n
+ *     GEMM_MN_MAJOR (column-major, "M-major"): (l*N + n)*M + m
+ *
+ * Errors: validation happens on the host before anything is enqueued and is
+ * reported synchronously by the return code.  gemm_run never synchronises;
+ * a device-side watchdog (a bounded wait on every pipeline barrier) records a
+ * timeout in a status word that gemm_sync_status reads.
+ */
+#ifndef GEMM_GB300_H
+#define GEMM_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* the CUDA runtime's cudaStream_t is `struct CUstream_st*` */
+
+typedef struct gemm_handle* gemm_handle_t;
+
+typedef enum {
+  GEMM_OK = 0,
+  GEMM_ERR_INVALID_ARG = 1,        /* bad shape, NULL where required, bad enum, bad ld */
+  GEMM_ERR_UNSUPPORTED_DTYPE = 2,  /* type combination not implemented */
+  GEMM_ERR_MISALIGNED = 3,         /* pointer or leading dimension not 16-byte aligned */
+  GEMM_ERR_UNSUPPORTED_ARCH = 4,   /* device is not compute capability 10.3 */
+  GEMM_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed */
+  GEMM_ERR_DEVICE_TIMEOUT = 6,     /* a kernel pipeline wait exceeded its limit */
+  GEMM_ERR_UNSUPPORTED_CONFIG = 7  /* a forced kernel configuration cannot run this problem */
+} gemm_status_t;
+
+typedef enum { GEMM_F32 = 0, GEMM_F16 = 1, GEMM_BF16 = 2, GEMM_E4M3 = 3 } gemm_dtype_t;
+
+typedef enum { GEMM_K_MAJOR = 0, GEMM_MN_MAJOR = 1 } gemm_layout_t;
+
+/* Element types.  ab: F16, BF16 or E4M3 (A and B share it).  c, x: F32, F16
+ * or BF16 (inputs).  d, y: F32, F16 or BF16 (outputs).  cdxy_major: the one
+ * major order of C, D, X and Y. */
+typedef struct {
+  gemm_dtype_t ab, c, d, x, y;
+  gemm_layout_t cdxy_major;
+} gemm_dtypes_t;
+
+/* Kernel configuration.  Chosen automatically per problem shape unless the
+ * handle has one forced (gemm_set_config).
+ *   cta_group   1: each CTA owns a 128 x tile_n output tile (tcgen05 cta_group::1)
+ *               2: a CTA pair owns a 256 x tile_n tile (tcgen05 cta_group::2);
+ *                  each CTA stages 128 rows of A and tile_n/2 rows of B.
+ *   tile_n      output tile width: 128 or 256.
+ *   stages      depth of the shared-memory A/B ring (0 = as deep as fits).
+ *   group_m     tile rasterisation: tiles are walked in column strips
+ *               group_m tiles high (0 = automatic).
+ * Filled in by gemm_plan / reported by gemm_last_config:
+ *   tile_m      128 * cta_group.
+ *   tile_k      K elements per ring stage (64 for 16-bit, 128 for 8-bit inputs).
+ *   acc_stages  tensor-memory accumulator stages (2: double buffered).
+ *   ring_bytes  ring bytes per CTA: stages*(A stage + B stage) + 8 bytes per
+ *               mbarrier (2 per stage, 2 per accumulator stage) + 4 bytes of
+ *               tensor-memory address.
+ *   smem_bytes  dynamic shared memory per CTA (ring + alignment slack).
+ *   tiles       number of output tiles; grid_ctas: CTAs launched. */
+typedef struct {
+  int cta_group, tile_n, stages, group_m;
+  int tile_m, tile_k, acc_stages;
+  int ring_bytes, smem_bytes;
+  int64_t tiles;
+  int grid_ctas;
+} gemm_config_t;
+
+/* Every argument of one gemm_run call, for the host-only planning calls. */
+typedef struct {
+  int64_t M, N, K, L;
+  const void* A; int64_t lda; gemm_layout_t layoutA;
+  const void* B; int64_t ldb; gemm_layout_t layoutB;
+  const void* C; const void* X; void* D; void* Y;
+  float alpha, beta, x_factor;
+  gemm_dtypes_t dtypes;
+} gemm_problem_t;
+
+/* Create a handle for CUDA device `device`.  Checks the device is compute
+ * capability 10.3 (GEMM_ERR_UNSUPPORTED_ARCH otherwise), caches its SM count
+ * and shared-memory limit, resolves cuTensorMapEncodeTiled through the runtime
+ * and allocates a 4-byte device status word.  *out is NULL on failure. */
+gemm_status_t gemm_create(gemm_handle_t* out, int device);
+
+/* Release the handle and its status word.  NULL is accepted (no-op).  Work
+ * already enqueued with this handle must be complete. */
+gemm_status_t gemm_destroy(gemm_handle_t h);
+
+/* Enqueue D = alpha*(A*B) + beta*C + x_factor*X (and Y = A*B) on `stream`.
+ *
+ * M, N, K, L >= 0.  M, N or L == 0: nothing to do, returns GEMM_OK.
+ * K == 0: acc = 0, so D = beta*C + x_factor*X and Y = 0.
+ * A, B: required when K > 0.  lda/ldb as in the layout table above, and
+ *   lda*sizeof(ab), ldb*sizeof(ab) multiples of 16 bytes.
+ * C: read only when beta != 0 (then required); otherwise may be NULL.
+ * X: read only when X != NULL and x_factor != 0.
+ * D: required.  Y: written when non-NULL.
+ * Every non-NULL pointer 16-byte aligned; the packed leading dimension of
+ *   C/D/X/Y (N for row-major, M for column-major) times the element size a
+ *   multiple of 16 bytes.
+ * Aliasing: D may equal C when they have the same type (each element of C is
+ *   read before the same element of D is written); any other overlap between
+ *   an output and any tensor is undefined.
+ * Asynchronous: returns once the kernel is enqueued; never synchronises.
+ * The calling thread's current device must be the handle's device. */
+gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, int64_t L,
+                       const void* A, int64_t lda, gemm_layout_t layoutA,
+                       const void* B, int64_t ldb, gemm_layout_t layoutB,
+                       const void* C, const void* X, void* D, void* Y,
+                       float alpha, float beta, float x_factor,
+                       const gemm_dtypes_t* dtypes, struct CUstream_st* stream);
+
+/* Synchronise `stream`, then read and clear the handle's device status word.
+ * Returns GEMM_ERR_DEVICE_TIMEOUT if any kernel since the last call hit its
+ * watchdog, GEMM_ERR_CUDA if the stream reported an error, else GEMM_OK.
+ * *detail (optional) receives the raw status word (0 when clean). */
+gemm_status_t gemm_sync_status(gemm_handle_t h, struct CUstream_st* stream, uint32_t* detail);
+
+/* Human-readable name of a status code (static storage). */
+const char* gemm_status_string(gemm_status_t s);
+
+/* Host-only validation of one call's arguments, exactly as gemm_run performs
+ * it (no device access; pointers are checked for NULL and alignment only). */
+gemm_status_t gemm_check(const gemm_problem_t* p);
+
+/* Host-only kernel configuration for problem `p` on a device with `sm_count`
+ * SMs and `smem_optin` bytes of opt-in shared memory per block.  `forced`
+ * (may be NULL) fixes cta_group/tile_n/stages/group_m; zero fields are
+ * chosen automatically.  Returns GEMM_ERR_UNSUPPORTED_CONFIG when a forced
+ * configuration cannot run the problem. */
+gemm_status_t gemm_plan(const gemm_problem_t* p, int sm_count, int smem_optin,
+                        const gemm_config_t* forced, gemm_config_t* out);
+
+/* Force a kernel configuration for later gemm_run calls on this handle
+ * (NULL restores automatic selection).  Used by tests and tuning sweeps. */
+gemm_status_t gemm_set_config(gemm_handle_t h, const gemm_config_t* cfg);
+
+/* The configuration chosen by the most recent successful gemm_run. */
+gemm_status_t gemm_last_config(gemm_handle_t h, gemm_config_t* out);
+
+/* Tensor-memory columns one fp32 accumulator of tile_m x tile_n occupies:
+ * tile_m/128 blocks when tile_m is a multiple of 128, else tile_m/64 blocks,
+ * times tile_n columns (the fit rule of the cuBLASDx Blackwell pipeline card,
+ * "Size" bullet: 512 columns per SM).  0 for an invalid tile. */
+int gemm_tmem_columns(int tile_m, int tile_n);
+
+/* Watchdog limit for every pipeline wait of later launches, in nanoseconds
+ * (0 restores the default of 4 seconds). */
+gemm_status_t gemm_set_timeout_ns(gemm_handle_t h, uint64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_GB300_H */

@@ -1,0 +1,191 @@
+"""CPU tests of the C-ABI library: it loads without a GPU, exports every entry
+point the header declares, validates arguments, and plans configurations
+(including the cuBLASDx Blackwell card's printed shared-memory and
+tensor-memory figures).  No compute call is made here."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import dense_gemm_epilogue_persistent_gb300 as G
+from dense_gemm_epilogue_persistent_gb300 import build as B
+import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden", "cublasdx_blackwell_card.txt")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return G.library()
+
+
+def _header_symbols():
+    syms = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            text = open(os.path.join(inc, f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            syms |= set(re.findall(r"\b(gemm_[a-z_0-9]+)\s*\(", text))
+    return syms
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _header_symbols()
+    assert {"gemm_create", "gemm_run", "gemm_destroy", "gemm_sync_status"} <= declared
+    out = subprocess.run(["nm", "-D", "--defined-only", G.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (gemm_\w+)", out))
+    assert declared <= exported, declared - exported
+    for s in declared:
+        assert hasattr(lib, s)
+
+
+def test_library_links_no_driver_library():
+    out = subprocess.run(["ldd", G.LIB_PATH], capture_output=True, text=True).stdout
+    assert "libcuda.so" not in out and "libcudart.so" not in out
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        assert G.gemm_status_string(code).startswith("GEMM_")
+    assert G.gemm_status_string(99) == "GEMM_ERR_UNKNOWN"
+
+
+def test_create_without_gpu_fails_cleanly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = ctypes.c_void_p(123)
+    st = lib.gemm_create(ctypes.byref(h), 0)
+    assert st in (G.GEMM_ERR_CUDA, G.GEMM_ERR_INVALID_ARG) and h.value is None
+    assert lib.gemm_destroy(None) == G.GEMM_OK
+
+
+# ---------------------------------------------------------------- validation
+
+A16 = 1 << 20           # fake, 16-byte-aligned device addresses (never dereferenced)
+B16 = 2 << 20
+C16 = 3 << 20
+D16 = 4 << 20
+
+
+def _p(**kw):
+    base = dict(M=256, N=256, K=256, L=1, A=A16, lda=256, B=B16, ldb=256, C=C16, D=D16,
+                alpha=1.0, beta=1.0, dtypes=G.make_dtypes("f16", "f32", "f32"))
+    base.update(kw)
+    return G.make_problem(**base)
+
+
+def test_check_accepts_valid(lib):
+    assert G.gemm_check(_p()) == G.GEMM_OK
+    assert G.gemm_check(_p(layoutA=G.GEMM_MN_MAJOR, lda=256, layoutB=G.GEMM_MN_MAJOR)) == 0
+    assert G.gemm_check(_p(C=None, beta=0.0)) == G.GEMM_OK          # C unread
+    assert G.gemm_check(_p(M=0, A=None, B=None, D=None)) == G.GEMM_OK
+    assert G.gemm_check(_p(K=0, A=None, B=None, lda=0, ldb=0)) == G.GEMM_OK
+    assert G.gemm_check(_p(C=D16)) == G.GEMM_OK                      # D aliases C, same type
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(M=-1), G.GEMM_ERR_INVALID_ARG),
+    (dict(K=1 << 31), G.GEMM_ERR_INVALID_ARG),
+    (dict(D=None), G.GEMM_ERR_INVALID_ARG),
+    (dict(C=None), G.GEMM_ERR_INVALID_ARG),                          # beta != 0 needs C
+    (dict(A=None), G.GEMM_ERR_INVALID_ARG),
+    (dict(lda=128), G.GEMM_ERR_INVALID_ARG),                         # lda < K
+    (dict(layoutA=7), G.GEMM_ERR_INVALID_ARG),
+    (dict(A=A16 + 8), G.GEMM_ERR_MISALIGNED),
+    (dict(lda=260), G.GEMM_ERR_MISALIGNED),                          # 520 B rows
+    (dict(N=250, ldb=256), G.GEMM_ERR_MISALIGNED),                   # f32 C/D rows of 1000 B
+    (dict(D=D16 + 4), G.GEMM_ERR_MISALIGNED),
+    (dict(dtypes=G.make_dtypes("f32")), G.GEMM_ERR_UNSUPPORTED_DTYPE),
+    (dict(dtypes=G.make_dtypes("f16", d="e4m3")), G.GEMM_ERR_UNSUPPORTED_DTYPE),
+    (dict(C=D16, dtypes=G.make_dtypes("f16", c="f16", d="f32")), G.GEMM_ERR_INVALID_ARG),
+])
+def test_check_rejects(lib, kw, code):
+    assert G.gemm_check(_p(**kw)) == code
+
+
+def test_check_e4m3_alignment(lib):
+    dt = G.make_dtypes("e4m3", "f16", "f16")
+    assert G.gemm_check(_p(K=4096, lda=4096, ldb=4096, N=5000, M=3000, dtypes=dt)) == 0
+    assert G.gemm_check(_p(K=4104, lda=4104, ldb=4104, dtypes=dt)) == G.GEMM_ERR_MISALIGNED
+
+
+# ---------------------------------------------------------------- planning
+
+def _golden():
+    rows = []
+    for line in open(GOLDEN):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            rows.append(line.split())
+    return rows
+
+
+def test_golden_ring_bytes_from_the_card(lib):
+    """The ring accounting reproduces the card's printed 48 KiB stage and
+    196,708-byte depth-4 buffer for a 128x256x64 bf16 tile."""
+    g = {r[0]: r for r in _golden()}
+    assert int(g["optin_limit"][1]) == 232448
+    p = _p(M=4096, N=4096, K=4096, lda=4096, ldb=4096, dtypes=G.make_dtypes("bf16", "f32", "f32"))
+    st, cfg = G.gemm_plan(p, 148, 232448, G.gemm_config_t(cta_group=1, tile_n=256, stages=4))
+    assert st == G.GEMM_OK
+    assert (cfg.tile_m, cfg.tile_n, cfg.tile_k, cfg.acc_stages) == (128, 256, 64, 2)
+    assert cfg.ring_bytes == int(g["buffer_bytes"][-1])
+    st, cfg3 = G.gemm_plan(p, 148, 232448, G.gemm_config_t(cta_group=1, tile_n=256, stages=3))
+    assert cfg.ring_bytes - cfg3.ring_bytes == int(g["stage_bytes"][-1]) + 16
+    assert cfg.smem_bytes <= 232448
+
+
+def test_golden_tmem_fit_rule(lib):
+    cap = 512
+    for r in _golden():
+        if r[0] == "tmem_fit":
+            m = int(r[1].split("=")[1])
+            n = int(r[2].split("=")[1])
+            assert (0 < G.gemm_tmem_columns(m, n) <= cap) == (r[3] == "yes"), r
+        if r[0] == "tmem_capacity_columns":
+            assert int(r[1]) == cap
+
+
+@pytest.mark.parametrize("name", list(W.WORKLOADS))
+def test_plan_every_workload(lib, name):
+    w = W.WORKLOADS[name]
+    lda = w.M if w.a_mn_major else w.K
+    ldb = w.N if w.b_mn_major else w.K
+    dt = G.make_dtypes(w.ab, w.c or "f32", w.d, w.x or "f32", w.y or "f32",
+                       G.GEMM_MN_MAJOR if w.cd_m_major else G.GEMM_K_MAJOR)
+    p = _p(M=w.M, N=w.N, K=w.K, L=w.L, lda=lda, ldb=ldb, layoutA=int(w.a_mn_major),
+           layoutB=int(w.b_mn_major), alpha=w.alpha, beta=w.beta, x_factor=w.x_factor,
+           dtypes=dt, C=C16 if w.c else None)
+    assert G.gemm_check(p) == G.GEMM_OK
+    st, cfg = G.gemm_plan(p, 152, 232448)
+    assert st == G.GEMM_OK
+    assert cfg.cta_group in (1, 2) and cfg.tile_n in (128, 256)
+    assert cfg.tile_k == (128 if w.ab == "e4m3" else 64)
+    assert 2 <= cfg.stages and cfg.smem_bytes <= 232448
+    assert cfg.tiles == (-(-w.M // cfg.tile_m)) * (-(-w.N // cfg.tile_n)) * w.L
+    assert cfg.grid_ctas % cfg.cta_group == 0 and cfg.grid_ctas <= 152
+    assert 2 * G.gemm_tmem_columns(128, cfg.tile_n) <= 512
+
+
+def test_plan_forced_and_rejected(lib):
+    p = _p(M=1024, N=1024, K=512, lda=512, ldb=512)
+    for cg in (1, 2):
+        for bn in (128, 256):
+            st, cfg = G.gemm_plan(p, 152, 232448, G.gemm_config_t(cta_group=cg, tile_n=bn))
+            assert st == 0 and (cfg.cta_group, cfg.tile_n) == (cg, bn)
+    st, _ = G.gemm_plan(p, 152, 232448, G.gemm_config_t(cta_group=1, tile_n=256, stages=9))
+    assert st == G.GEMM_ERR_UNSUPPORTED_CONFIG                 # 9 x 48 KiB does not fit
+    # fp8 with N-major B needs 128 B rows per CTA: not with tile_n/cta_group = 64
+    dt8 = G.make_dtypes("e4m3", "f16", "f16")
+    p8 = _p(M=1024, N=1024, K=512, lda=512, ldb=1024, layoutB=G.GEMM_MN_MAJOR, dtypes=dt8)
+    st, _ = G.gemm_plan(p8, 152, 232448, G.gemm_config_t(cta_group=2, tile_n=128))
+    assert st == G.GEMM_ERR_UNSUPPORTED_CONFIG
+    st, cfg = G.gemm_plan(p8, 152, 232448)
+    assert st == 0 and (cfg.tile_n // cfg.cta_group) % 128 == 0

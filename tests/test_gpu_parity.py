@@ -1,0 +1,265 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Small problems (spanning several tiles and ragged tails) are compared element
+by element; the full-size workloads are compared on 4096 seeded entries plus
+whole rows and columns at tile boundaries, in the same launch configuration
+the benchmark uses.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+import dense_gemm_epilogue_persistent_gb300 as G
+from gemm_cases import (Case, compare_full, compare_sampled, logical, prepare, run_gpu,
+                        to_f64)
+
+pytestmark = pytest.mark.gpu
+
+VARIANTS = [(1, 128), (1, 256), (2, 128), (2, 256)]
+
+
+@pytest.fixture(scope="module")
+def gemm():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    g = G.Gemm(0)
+    yield g
+    g.close()
+
+
+def _force(gemm, cg, bn, stages=0):
+    gemm.set_config(cta_group=cg, tile_n=bn, stages=stages)
+
+
+def _finish(gemm):
+    st, detail = gemm.sync_status()
+    assert st == G.GEMM_OK, f"device status {G.gemm_status_string(st)} detail={detail:#x}"
+
+
+# ------------------------------------------------------------ bit-exact workload
+
+@pytest.mark.parametrize("variant", VARIANTS + [None])
+def test_int256_bit_exact(gemm, variant):
+    """256^3, integers in [-2,2], alpha=1.5, beta=-0.5: every intermediate is
+    exact in fp32, so D must equal the once-rounded oracle bit for bit."""
+    w = W.WORKLOADS["int256_f16_f32"]
+    if variant:
+        _force(gemm, *variant)
+    else:
+        gemm.set_config(None)
+    prep = prepare(Case.from_workload(w))
+    D, Y = run_gpu(gemm, prep)
+    _finish(gemm)
+    compare_full(prep, D, Y, exact=True)
+    gemm.set_config(None)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_integer_exact_ragged_all_outputs(gemm, variant):
+    """Ragged shape, integer inputs, f32 C/X/D/Y: still exact (|acc| < 2^24)."""
+    _force(gemm, *variant)
+    case = Case(M=300, N=200, K=208, L=2, ab="bf16", c="f32", d="f32", x="f32", y="f32",
+                alpha=2.0, beta=-1.0, xf=0.5, dist="int2", seed=7)
+    prep = prepare(case)
+    D, Y = run_gpu(gemm, prep)
+    _finish(gemm)
+    compare_full(prep, D, Y, exact=True)
+    gemm.set_config(None)
+
+
+# ------------------------------------------------------------ reduced-size workloads
+
+SMALL = {
+    # custom epilogue, fp16 everywhere
+    "efc_f16": Case(M=520, N=392, K=328, L=1, ab="f16", c="f16", d="f16", x="f16", y="f16",
+                    alpha=2.0, beta=1.0, xf=3.0, dist="normal1", seed=2),
+    # bf16 GEMM with fp32 C/D
+    "bf16_f32": Case(M=384, N=640, K=512, L=1, ab="bf16", c="f32", d="f32", alpha=1.0,
+                     beta=1.0, dist="uniform1", seed=1),
+    # batched, A M-major, B N-major, C/D M-major
+    "batched_mn": Case(M=264, N=320, K=200, L=3, ab="bf16", c="bf16", d="bf16", a_mn=True,
+                       b_mn=True, cd_m=True, alpha=0.5, beta=0.0, dist="normal002", seed=3),
+    # ragged fp8
+    "ragged_e4m3": Case(M=300, N=504, K=272, L=1, ab="e4m3", c="f16", d="f16", alpha=0.25,
+                        beta=1.0, dist="e4m3_pm4", seed=4),
+}
+
+
+@pytest.mark.parametrize("variant", VARIANTS + [None])
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_workloads(gemm, name, variant):
+    case = SMALL[name]
+    if variant:
+        cg, bn = variant
+        # MN-major operands are staged in 128-byte atoms per CTA
+        if case.b_mn and (bn // cg) % (128 // W.ELEM_BYTES[case.ab]) != 0:
+            pytest.skip("variant cannot stage this MN-major B")
+        _force(gemm, *variant)
+    else:
+        gemm.set_config(None)
+    prep = prepare(case)
+    D, Y = run_gpu(gemm, prep)
+    _finish(gemm)
+    compare_full(prep, D, Y)
+    gemm.set_config(None)
+
+
+@pytest.mark.parametrize("ab", ["f16", "bf16", "e4m3"])
+@pytest.mark.parametrize("a_mn,b_mn,cd_m", [(False, False, False), (True, False, False),
+                                            (False, True, False), (True, True, True),
+                                            (False, False, True)])
+def test_layouts(gemm, ab, a_mn, b_mn, cd_m):
+    case = Case(M=400, N=256, K=320, L=2, ab=ab, c="bf16", d="f32", x="f16", y="bf16",
+                a_mn=a_mn, b_mn=b_mn, cd_m=cd_m, alpha=1.5, beta=-0.25, xf=0.75,
+                dist="e4m3_pm4" if ab == "e4m3" else "normal1", seed=9)
+    gemm.set_config(None)
+    prep = prepare(case)
+    D, Y = run_gpu(gemm, prep)
+    _finish(gemm)
+    compare_full(prep, D, Y)
+
+
+def test_layout_equivalence_bitwise(gemm):
+    """The same logical values in every layout give identical outputs."""
+    base = None
+    for a_mn in (False, True):
+        for b_mn in (False, True):
+            for cd_m in (False, True):
+                case = Case(M=256, N=256, K=192, L=2, ab="f16", c="f16", d="f16", y="f32",
+                            a_mn=a_mn, b_mn=b_mn, cd_m=cd_m, alpha=1.25, beta=0.5, seed=12)
+                gemm.set_config(None)
+                prep = prepare(case)
+                D, Y = run_gpu(gemm, prep)
+                _finish(gemm)
+                out = (logical(D, cd_m), logical(Y, cd_m))
+                if base is None:
+                    base = out
+                else:
+                    assert torch.equal(base[0], out[0]) and torch.equal(base[1], out[1])
+
+
+# ------------------------------------------------------------ edge cases
+
+@pytest.mark.parametrize("M,N,K,L", [(8, 8, 16, 1), (1, 8, 16, 1), (129, 136, 72, 1),
+                                     (130, 264, 1000, 3), (2048, 8, 64, 1), (8, 2000, 16, 2)])
+def test_ragged_shapes(gemm, M, N, K, L):
+    case = Case(M=M, N=N, K=K, L=L, ab="f16", c="f16", d="f16", y="f16", alpha=1.0, beta=2.0,
+                seed=M + N + K)
+    gemm.set_config(None)
+    prep = prepare(case)
+    D, Y = run_gpu(gemm, prep)
+    _finish(gemm)
+    compare_full(prep, D, Y)
+
+
+def test_k_zero(gemm):
+    case = Case(M=200, N=136, K=0, L=2, ab="bf16", c="f32", d="f32", x="f16", y="f32",
+                alpha=3.0, beta=0.5, xf=-2.0, seed=5)
+    prep = prepare(case)
+    D, Y = run_gpu(gemm, prep)
+    _finish(gemm)
+    D_ref, Y_ref = compare_full(prep, D, Y, exact=True)
+    assert np.all(Y_ref == 0)
+
+
+def test_empty_problems_are_noops(gemm):
+    D = torch.full((4, 16), 7.0, device="cuda")
+    dt = G.make_dtypes("f16")
+    for M, N, L in [(0, 16, 1), (4, 0, 1), (4, 16, 0)]:
+        st = G.gemm_run(gemm.handle, M, N, 32, L, 0, 32, 0, 0, 32, 0, 0, 0, D, 0, 1.0, 0.0, 0.0,
+                        dt)
+        assert st == G.GEMM_OK
+    _finish(gemm)
+    assert torch.all(D == 7.0)
+
+
+def test_inputs_unchanged_canaries_and_alias(gemm):
+    """C and X are read-only, nothing outside D and Y is written, and D may
+    alias C (each element of C is read before it is overwritten)."""
+    case = Case(M=200, N=264, K=136, L=2, ab="f16", c="f16", d="f16", x="f16", y="f16",
+                alpha=1.0, beta=1.0, xf=2.0, seed=17)
+    prep = prepare(case)
+    dev = torch.device("cuda")
+    n = case.L * case.M * case.N
+    pad = 4096
+    Dbuf = torch.full((n + 2 * pad,), 1234.0, dtype=torch.float16, device=dev)
+    Ybuf = torch.full((n + 2 * pad,), -77.0, dtype=torch.float16, device=dev)
+    D = Dbuf[pad:pad + n].view(case.L, case.M, case.N)
+    Y = Ybuf[pad:pad + n].view(case.L, case.M, case.N)
+    C_dev = prep.C.to(dev)
+    X_dev_before = prep.X.clone()
+    D, Y = run_gpu(gemm, prep, D=D, Y=Y, C_dev=C_dev)
+    _finish(gemm)
+    assert torch.equal(C_dev.cpu(), prep.C) and torch.equal(prep.X, X_dev_before)
+    for buf, v in ((Dbuf, 1234.0), (Ybuf, -77.0)):
+        assert torch.all(buf[:pad] == v) and torch.all(buf[pad + n:] == v)
+    compare_full(prep, D, Y)
+    # alias: D == C
+    C_alias = prep.C.to(dev)
+    D2, _ = run_gpu(gemm, prep, D=C_alias, C_dev=C_alias)
+    _finish(gemm)
+    assert torch.equal(D2.cpu(), D.cpu())
+
+
+def test_beta_zero_does_not_read_C(gemm):
+    case = Case(M=136, N=128, K=64, L=1, ab="bf16", c="f32", d="f32", alpha=1.0, beta=0.0,
+                seed=23)
+    prep = prepare(case)
+    C_nan = torch.full_like(prep.C, float("nan")).cuda()
+    D, _ = run_gpu(gemm, prep, C_dev=C_nan)
+    _finish(gemm)
+    assert not torch.isnan(D).any()
+    compare_full(prep, D, None)
+
+
+def test_x_null_means_no_x_term(gemm):
+    case = Case(M=256, N=256, K=128, L=1, ab="f16", c="f16", d="f16", x="f16", y="f16",
+                alpha=1.0, beta=1.0, xf=3.0, seed=29)
+    prep = prepare(case)
+    D, Y = run_gpu(gemm, prep, use_x=False)
+    _finish(gemm)
+    compare_full(prep, D, Y, use_x=False)
+
+
+def test_lda_ldb_padding(gemm):
+    case = Case(M=200, N=136, K=100, L=2, ab="bf16", c="f32", d="f32", alpha=1.0, beta=0.5,
+                lda_pad=28, ldb_pad=12, seed=31)
+    prep = prepare(case)
+    D, _ = run_gpu(gemm, prep)
+    _finish(gemm)
+    compare_full(prep, D, None)
+
+
+def test_streams_and_repeat_determinism(gemm):
+    case = SMALL["efc_f16"]
+    prep = prepare(case)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        D1, Y1 = run_gpu(gemm, prep, stream=s)
+        D2, Y2 = run_gpu(gemm, prep, stream=s)
+    st, _ = gemm.sync_status(s)
+    assert st == G.GEMM_OK
+    assert torch.equal(D1, D2) and torch.equal(Y1, Y2)
+
+
+# ------------------------------------------------------------ full-size workloads
+
+FULL = ["gemm2048_bf16_f32", "efc8192_f16", "gemm8192_bf16", "batched16_bf16_mn",
+        "ragged_e4m3_f16"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workloads_sampled(gemm, name):
+    """Each full-size workload in the launch configuration the benchmark uses
+    (automatic selection), checked on sampled entries and boundary lines."""
+    w = W.WORKLOADS[name]
+    gemm.set_config(None)
+    case = Case.from_workload(w)
+    prep = prepare(case)
+    D, Y = run_gpu(gemm, prep)
+    _finish(gemm)
+    cfg = gemm.last_config()
+    n = compare_sampled(prep, D, Y, cfg.tile_m, cfg.tile_n, seed=w.seed + 1000)
+    assert n >= 4096
