@@ -1,0 +1,471 @@
+#!/usr/bin/env python
+"""Throughput of the persistent batched GEMM with fused epilogue on GB300.
+
+One step = one gemm_run of the benchmark workload (the whole path: persistent
+tile scheduler, TMA ring, tcgen05 MMA into tensor memory, fused epilogue) on
+synthetic inputs already resident in HBM.  Default workload: the 8192^3 fp16
+custom-epilogue GEMM (Y = A*B, D = 2*A*B + 1*C + 3*X, fp32 accumulate and
+epilogue, fp16 C/X/D/Y).  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on the host cores instead (a
+bounded sample of the same workload per step).  With several GPUs (torchrun)
+every rank runs its own replica of the workload: the GEMM has no data-path
+exchange, so scaling is weak and no collective touches the data.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s (2MNKL/t) and % of GB300 dense tensor peak per config"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "source": "fallback"}
+SMI_FIELDS = ("pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="efc8192_f16")
+    ap.add_argument("--no-per-config", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return dict(FALLBACK_PEAKS, bf16_tflops_sustained=1700.0)
+
+
+def tensor_peak(peaks, ab: str, sustained=False):
+    """Dense tensor peak for the input type: fp16 runs at the bf16 rate; fp8
+    at twice it (nominal ratio 4.5 / 2.25 PFLOP/s)."""
+    base = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    return base * (2.0 if ab == "e4m3" else 1.0)
+
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_gemm_epilogue_persistent_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f).get(workload)
+    if not d or d.get("kernel_src_digest") != kernel_source_digest():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of this GPU's clocks, power and
+    throttle reasons while the timed region runs."""
+
+    def __init__(self, pci_bus: int | None):
+        self.pci_bus = pci_bus
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = open(os.path.join("/tmp", f"clocks_{os.getpid()}.csv"), "w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={SMI_FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.seek(0)
+        rows = [[c.strip() for c in r] for r in csv.reader(io.StringIO(self.out.read()))
+                if len(r) >= 9]
+        self.out.close()
+
+        def bus(r):
+            try:
+                return int(r[0].split(":")[1], 16)
+            except Exception:
+                return None
+
+        mine = [r for r in rows if self.pci_bus is None or bus(r) == self.pci_bus] or rows
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+
+        sm = [x for x in (num(r[1]) for r in mine) if x is not None]
+        smax = [x for x in (num(r[2]) for r in mine) if x is not None]
+        power = [x for x in (num(r[3]) for r in mine) if x is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in mine for i in range(4)
+                          if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(mine), "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_problem_for(w, inp):
+    import oracle
+    import workloads as W
+    st = W.storage_view_np
+    As = W.to_storage(inp.A, w.a_mn_major)
+    Bs = W.to_storage(inp.B, w.b_mn_major)
+    Cs = W.to_storage(inp.C, w.cd_m_major) if inp.C is not None else None
+    Xs = W.to_storage(inp.X, w.cd_m_major) if inp.X is not None else None
+    return oracle.Problem(w.M, w.N, w.K, w.L, st(As), As.shape[-1], w.a_mn_major, st(Bs),
+                          Bs.shape[-1], w.b_mn_major, None if Cs is None else st(Cs),
+                          None if Xs is None else st(Xs), w.ab, w.c or "f32", w.x or "f32",
+                          w.cd_m_major, w.alpha, w.beta, w.x_factor)
+
+
+def time_oracle_sample(w, inp, seconds: float):
+    """Time the oracle as it stands on whole rows of the workload until about
+    `seconds` of CPU work; return the throughput and the sample it ran."""
+    import oracle
+    p = oracle_problem_for(w, inp)
+    cores = oracle.max_threads()
+    rows, t_total, m = 0, 0.0, 0
+    while t_total < seconds and m < w.M:
+        chunk = min(cores, w.M - m)
+        t0 = time.perf_counter()
+        oracle.gemm_rows(p, m, m + chunk)
+        t_total += time.perf_counter() - t0
+        rows += chunk * w.L
+        m += chunk
+    flops = 2.0 * rows * w.N * w.K
+    return {"value": flops / t_total / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{rows} full output rows ({rows * w.N} entries, K={w.K}) of {w.name}, "
+                      f"fp64 triple loop, {t_total:.1f} s"}
+
+
+def run_reference(args, rank):
+    """The reference arm: the fp64 CPU oracle on host cores, a bounded sample
+    of the workload per step."""
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    import workloads as W
+    oracle.build()
+    w = W.WORKLOADS[args.workload]
+    inp = W.make_inputs(w)
+    p = oracle_problem_for(w, inp)
+    cores = oracle.max_threads()
+    g = np.random.default_rng(0)
+    # calibrate: entries per second
+    n_cal = 4 * cores
+    ms, ns = g.integers(0, w.M, n_cal), g.integers(0, w.N, n_cal)
+    ls = g.integers(0, w.L, n_cal)
+    t0 = time.perf_counter()
+    oracle.gemm_entries(p, ms, ns, ls)
+    per_entry = (time.perf_counter() - t0) / n_cal
+    budget = 120.0 / max(1, args.steps + args.warmup)        # seconds per step
+    n_step = int(max(cores, min(64 * cores, budget / max(per_entry, 1e-9))))
+    for _ in range(args.warmup):
+        oracle.gemm_entries(p, g.integers(0, w.M, n_step), g.integers(0, w.N, n_step),
+                            g.integers(0, w.L, n_step))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.gemm_entries(p, g.integers(0, w.M, n_step), g.integers(0, w.N, n_step),
+                            g.integers(0, w.L, n_step))
+    dt = time.perf_counter() - t0
+    value = 2.0 * w.K * n_step * args.steps / dt / 1e12
+    sample = f"{n_step} random output entries per step (K={w.K}) of {w.name}"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "L": w.L},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+
+class Bound:
+    """One workload's device buffers and a closure launching it."""
+
+    def __init__(self, G, g, w, inp, device):
+        import torch
+        import workloads as W
+        self.w = w
+        dev = torch.device("cuda", device)
+        self.A = W.to_storage(inp.A, w.a_mn_major).to(dev)
+        self.B = W.to_storage(inp.B, w.b_mn_major).to(dev)
+        self.C = W.to_storage(inp.C, w.cd_m_major).to(dev) if inp.C is not None else None
+        self.X = W.to_storage(inp.X, w.cd_m_major).to(dev) if inp.X is not None else None
+        shape = (w.L, w.N, w.M) if w.cd_m_major else (w.L, w.M, w.N)
+        self.D = torch.empty(shape, dtype=W.TORCH_DTYPE[w.d], device=dev)
+        self.Y = torch.empty(shape, dtype=W.TORCH_DTYPE[w.y], device=dev) if w.y else None
+        self.dt = G.make_dtypes(w.ab, w.c or "f32", w.d, w.x or "f32", w.y or "f32",
+                                G.GEMM_MN_MAJOR if w.cd_m_major else G.GEMM_K_MAJOR)
+        self.G, self.g = G, g
+
+    def launch(self, stream, A=None, B=None, C=None, X=None, D=None, Y=None):
+        w = self.w
+        A = self.A if A is None else A
+        B = self.B if B is None else B
+        self.G.gemm_run(self.g.handle, w.M, w.N, w.K, w.L, A, A.shape[-1], int(w.a_mn_major),
+                        B, B.shape[-1], int(w.b_mn_major), self.C if C is None else C,
+                        self.X if X is None else X, self.D if D is None else D,
+                        self.Y if Y is None else Y, w.alpha, w.beta, w.x_factor, self.dt,
+                        stream.cuda_stream)
+
+    def nbytes_in(self):
+        return sum(t.numel() * t.element_size() for t in (self.A, self.B, self.C, self.X)
+                   if t is not None and (t is not self.C or self.w.beta != 0))
+
+    def nbytes_out(self):
+        return sum(t.numel() * t.element_size() for t in (self.D, self.Y) if t is not None)
+
+
+def time_launches(torch, bound, stream, iters, warmup):
+    for _ in range(warmup):
+        bound.launch(stream)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(iters):
+        bound.launch(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / iters
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import workloads as W
+    from dense_gemm_epilogue_persistent_gb300 import build as _build
+    _build.build()
+    import dense_gemm_epilogue_persistent_gb300 as G
+
+    if world > 1:
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl", rank=rank, world_size=world)
+    torch.cuda.set_device(local_rank)
+    device = local_rank
+    peaks = load_peaks()
+    w = W.WORKLOADS[args.workload]
+    inp = W.make_inputs(w)
+    g = G.Gemm(device)
+    bound = Bound(G, g, w, inp, device)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # warm-up (and a status check: the watchdog must be clean)
+    warm = max(3, args.warmup)
+    for _ in range(warm):
+        bound.launch(stream)
+    st, detail = g.sync_status(stream.cuda_stream)
+    if st != G.GEMM_OK:
+        raise SystemExit(f"warm-up failed: {G.gemm_status_string(st)} {detail:#x}")
+    cfg = g.last_config()
+
+    # timed region: K steps, one launch each, events on the launching stream
+    props = torch.cuda.get_device_properties(device)
+    sampler = ClockSampler(getattr(props, "pci_bus_id", None))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    sampler.start()
+    time.sleep(0.25)
+    barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for e0, e1 in evs:
+        e0.record(stream)
+        bound.launch(stream)
+        e1.record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    st, detail = g.sync_status(stream.cuda_stream)
+    if st != G.GEMM_OK:
+        raise SystemExit(f"timed region failed: {G.gemm_status_string(st)} {detail:#x}")
+    total_ms = t_start.elapsed_time(t_end)
+    per_launch = [e0.elapsed_time(e1) for e0, e1 in evs]
+    kernel_ms = sum(per_launch) / len(per_launch)
+    t = torch.tensor([total_ms], device="cuda")
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    max_ms = float(t.item())
+    flops = w.flops
+    value = flops * args.steps * world / (max_ms / 1e3) / 1e12
+
+    # end to end through the public API: pinned host inputs -> device ->
+    # gemm_run -> device outputs -> pinned host, every step
+    e2e = None
+    if not args.no_e2e:
+        h_in = [t.cpu().pin_memory() for t in (bound.A, bound.B, bound.C, bound.X)
+                if t is not None]
+        h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                 for t in (bound.D, bound.Y) if t is not None]
+        d_in = [torch.empty_like(t, device="cuda") for t in h_in]
+        names = [n for n, t in zip("ABCX", (bound.A, bound.B, bound.C, bound.X)) if t is not None]
+
+        def e2e_step():
+            for h, d in zip(h_in, d_in):
+                d.copy_(h, non_blocking=True)
+            kw = dict(zip(names, d_in))
+            bound.launch(stream, **kw)
+            outs = [t for t in (bound.D, bound.Y) if t is not None]
+            for h, d in zip(h_out, outs):
+                h.copy_(d, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        barrier()
+        a.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        et = torch.tensor([a.elapsed_time(b)], device="cuda")
+        if world > 1:
+            dist.all_reduce(et, op=dist.ReduceOp.MAX)
+        e2e_ms = float(et.item()) / args.e2e_steps
+        st, _ = g.sync_status(stream.cuda_stream)
+        h2d = sum(t.numel() * t.element_size() for t in h_in)
+        d2h = sum(t.numel() * t.element_size() for t in h_out)
+        e2e = {"value": flops * world / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+               "status": G.gemm_status_string(st)}
+        del h_in, h_out, d_in
+
+    peak = tensor_peak(peaks, w.ab)
+    achieved = flops / (kernel_ms / 1e3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": recorded_traffic(w.name),
+                "peak_source": f"{peaks['source']} bf16 burst"
+                               + (" x2 (fp8/bf16 nominal ratio)" if w.ab == "e4m3" else "")}
+
+    per_config = None
+    cpu_baseline = None
+    if rank == 0:
+        if not args.no_per_config:
+            per_config = {}
+            for name, wc in W.WORKLOADS.items():
+                if name == w.name:
+                    ms = kernel_ms
+                    c2 = cfg
+                else:
+                    bc = Bound(G, g, wc, W.make_inputs(wc), device)
+                    ms = time_launches(torch, bc, stream, iters=50, warmup=10)
+                    c2 = g.last_config()
+                    del bc
+                tf = wc.flops / (ms / 1e3) / 1e12
+                pk = tensor_peak(peaks, wc.ab)
+                per_config[name] = {"us": round(ms * 1e3, 2), "tflops": round(tf, 1),
+                                    "pct_of_peak": round(100 * tf / pk, 1), "peak_tflops": pk,
+                                    "kernel": f"{c2.tile_m}x{c2.tile_n} cta_group={c2.cta_group}"
+                                              f" stages={c2.stages} grid={c2.grid_ctas}"}
+            st, _ = g.sync_status(stream.cuda_stream)
+            if st != G.GEMM_OK:
+                raise SystemExit(f"per-config timing failed: {G.gemm_status_string(st)}")
+        if not args.no_cpu_baseline:
+            cpu_baseline = time_oracle_sample(w, inp, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": warm, "ms_per_step": max_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": {"f16": "f16", "bf16": "bf16", "e4m3": "e4m3"}[w.ab] + " in, f32 accumulate",
+            "data": "synthetic",
+            "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "L": w.L,
+                       "ab": w.ab, "c": w.c, "d": w.d, "x": w.x, "y": w.y,
+                       "epilogue": f"Y=AB, D={w.alpha}*AB+{w.beta}*C+{w.x_factor}*X",
+                       "kernel": {"cta_group": cfg.cta_group, "tile": f"{cfg.tile_m}x{cfg.tile_n}",
+                                  "tile_k": cfg.tile_k, "stages": cfg.stages,
+                                  "grid_ctas": cfg.grid_ctas, "group_m": cfg.group_m},
+                       "l2": "no flush: inputs larger than L2 "
+                             f"({bound.nbytes_in() / 2**20:.0f} MiB of A,B,C,X vs 129 MB)",
+                       "parallelism": f"replicas x{world}"},
+            "pct_of_peak": 100.0 * value / world / peak,
+            "roofline": roofline,
+            "cpu_baseline": cpu_baseline,
+            "e2e": e2e,
+            "clocks": clocks,
+            "gpu_launches": args.steps,
+            "kernel_ms_mean": kernel_ms,
+            "per_config": per_config,
+        }
+        print(json.dumps(line), flush=True)
+    g.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

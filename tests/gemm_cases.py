@@ -107,14 +107,15 @@ def out_shape(case: Case):
 
 
 def run_gpu(gemm: G.Gemm, prep: Prepared, stream=None, D=None, Y=None, use_x=True,
-            C_dev=None):
+            C_dev=None, X_dev=None):
     """Copy storage to the GPU, call gemm_run, return (D, Y) device tensors."""
     c = prep.case
     dev = torch.device("cuda")
     A = prep.A.to(dev)
     B = prep.B.to(dev)
     C = C_dev if C_dev is not None else (prep.C.to(dev) if prep.C is not None else None)
-    X = prep.X.to(dev) if (prep.X is not None and use_x) else None
+    X = X_dev if X_dev is not None else (
+        prep.X.to(dev) if (prep.X is not None and use_x) else None)
     if D is None:
         D = torch.empty(out_shape(c), dtype=W.TORCH_DTYPE[c.d], device=dev)
     if Y is None and c.y is not None:

@@ -189,10 +189,10 @@ def test_inputs_unchanged_canaries_and_alias(gemm):
     D = Dbuf[pad:pad + n].view(case.L, case.M, case.N)
     Y = Ybuf[pad:pad + n].view(case.L, case.M, case.N)
     C_dev = prep.C.to(dev)
-    X_dev_before = prep.X.clone()
-    D, Y = run_gpu(gemm, prep, D=D, Y=Y, C_dev=C_dev)
+    X_dev = prep.X.to(dev)
+    D, Y = run_gpu(gemm, prep, D=D, Y=Y, C_dev=C_dev, X_dev=X_dev)
     _finish(gemm)
-    assert torch.equal(C_dev.cpu(), prep.C) and torch.equal(prep.X, X_dev_before)
+    assert torch.equal(C_dev.cpu(), prep.C) and torch.equal(X_dev.cpu(), prep.X)
     for buf, v in ((Dbuf, 1234.0), (Ybuf, -77.0)):
         assert torch.all(buf[:pad] == v) and torch.all(buf[pad + n:] == v)
     compare_full(prep, D, Y)
