@@ -46,7 +46,8 @@ class gemm_config_t(ctypes.Structure):
                 ("group_m", ctypes.c_int), ("tile_m", ctypes.c_int), ("tile_k", ctypes.c_int),
                 ("acc_stages", ctypes.c_int), ("ring_bytes", ctypes.c_int),
                 ("smem_bytes", ctypes.c_int), ("tiles", ctypes.c_int64),
-                ("grid_ctas", ctypes.c_int)]
+                ("grid_ctas", ctypes.c_int), ("epi_slots", ctypes.c_int),
+                ("epi_slot_bytes", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

@@ -135,6 +135,25 @@ int ring_bytes(int cta_group, int tile_n, int ab_bytes, int stages) {
   return stages * stage + 8 * (2 * stages + 2 * gb300::kAccStages) + 4;
 }
 
+// Bytes of one epilogue slot: C/D region + X/Y region, each 128 x 32
+// elements of the wider type stored there.
+int epi_slot_bytes(const gemm_problem_t& p) {
+  const int sub = 128 * gb300::kEpiChunk;
+  int cd = dtype_bytes(p.dtypes.d);
+  if (reads_c(p)) cd = std::max(cd, dtype_bytes(p.dtypes.c));
+  int xy = 0;
+  if (reads_x(p)) xy = dtype_bytes(p.dtypes.x);
+  if (p.Y) xy = std::max(xy, dtype_bytes(p.dtypes.y));
+  return sub * (cd + xy);
+}
+
+// Dynamic shared memory of one CTA: A/B ring, epilogue slots, every mbarrier
+// (full/empty per stage, full/empty per accumulator stage, one per epilogue
+// slot), tensor-memory address and abort flag, plus 1 KiB of alignment slack.
+int total_smem(int cg, int bn, int ab_bytes, int stages, int slots, int slot_bytes) {
+  return ring_bytes(cg, bn, ab_bytes, stages) + slots * slot_bytes + 8 * slots + 4 + kSmemSlack;
+}
+
 bool variant_supports(const gemm_problem_t& p, int cg, int bn) {
   if (cg != 1 && cg != 2) return false;
   if (bn != 128 && bn != 256) return false;
@@ -200,10 +219,16 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
   if (gemm_tmem_columns(128, bn) * gb300::kAccStages > (int)gb300::kTmemCols)
     return GEMM_ERR_UNSUPPORTED_CONFIG;
 
-  const int budget = smem_optin - kSmemSlack;
-  int max_stages = 0;
-  while (max_stages < kMaxStages && ring_bytes(cg, bn, ab_bytes, max_stages + 1) <= budget)
-    ++max_stages;
+  // Epilogue slots: a C/D region and an X/Y region of 128 x 32 elements each,
+  // sized for the wider of the two types that share it.
+  const int slot = epi_slot_bytes(p);
+  auto max_stages_for = [&](int slots) {
+    int n = 0;
+    while (n < kMaxStages && total_smem(cg, bn, ab_bytes, n + 1, slots, slot) <= smem_optin) ++n;
+    return n;
+  };
+  int slots = max_stages_for(3) >= 4 ? 3 : 2;
+  const int max_stages = max_stages_for(slots);
   int stages = forced && forced->stages ? forced->stages : max_stages;
   if (stages < 2 || stages > max_stages) return GEMM_ERR_UNSUPPORTED_CONFIG;
 
@@ -222,9 +247,12 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
   c.tile_k = 128 / ab_bytes;
   c.acc_stages = gb300::kAccStages;
   c.ring_bytes = ring_bytes(cg, bn, ab_bytes, stages);
+  c.epi_slots = slots;
+  c.epi_slot_bytes = slot;
   // At least half the opt-in limit: one CTA per SM, so no two CTAs ever
   // contend for the 512 tensor-memory columns each allocates.
-  c.smem_bytes = std::max(c.ring_bytes + kSmemSlack, smem_optin / 2 + 1024);
+  c.smem_bytes = std::max(total_smem(cg, bn, ab_bytes, stages, slots, slot),
+                          smem_optin / 2 + 1024);
   c.tiles = tiles;
   const int64_t units = std::max(1, sm_count / cg);
   c.grid_ctas = (int)(std::min<int64_t>(tiles, units) * cg);
@@ -262,6 +290,36 @@ bool encode_operand(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int dt
   CUresult r = enc(map, tma_type(dt), 3, const_cast<void*>(ptr), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Epilogue tensor map over a packed M x N x L tensor, box = 128 rows x 32
+// columns.  Row-major: dims {N, M, L}, 128-byte (fp32) or 64-byte (16-bit) rows
+// swizzled to match the epilogue's shared-memory reads.  Column-major: dims
+// {M, N, L}, unswizzled.
+bool encode_epi(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int dt, int64_t M,
+                int64_t N, int64_t L, bool m_major) {
+  const int64_t es = dtype_bytes(dt);
+  cuuint64_t dims[3], strides[2];
+  cuuint32_t box[3], estr[3] = {1, 1, 1};
+  CUtensorMapSwizzle sw;
+  CUtensorMapDataType ty = dt == GEMM_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : tma_type(dt);
+  if (!m_major) {
+    dims[0] = (cuuint64_t)N; dims[1] = (cuuint64_t)M; dims[2] = (cuuint64_t)L;
+    strides[0] = (cuuint64_t)(N * es);
+    strides[1] = (cuuint64_t)(N * es * M);
+    box[0] = gb300::kEpiChunk; box[1] = 128; box[2] = 1;
+    sw = es == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  } else {
+    dims[0] = (cuuint64_t)M; dims[1] = (cuuint64_t)N; dims[2] = (cuuint64_t)L;
+    strides[0] = (cuuint64_t)(M * es);
+    strides[1] = (cuuint64_t)(M * es * N);
+    box[0] = 128; box[1] = gb300::kEpiChunk; box[2] = 1;
+    sw = CU_TENSOR_MAP_SWIZZLE_NONE;
+  }
+  CUresult r = enc(map, ty, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -470,6 +528,17 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
       return GEMM_ERR_CUDA;
   }
 
+  const bool cd_m = dtypes->cdxy_major == GEMM_MN_MAJOR;
+  CUtensorMap tmC, tmX, tmD, tmY;
+  std::memset(&tmC, 0, sizeof(tmC));
+  std::memset(&tmX, 0, sizeof(tmX));
+  std::memset(&tmY, 0, sizeof(tmY));
+  if (!encode_epi(h->encode, &tmD, D, dtypes->d, M, N, L, cd_m) ||
+      (reads_c(p) && !encode_epi(h->encode, &tmC, C, dtypes->c, M, N, L, cd_m)) ||
+      (reads_x(p) && !encode_epi(h->encode, &tmX, X, dtypes->x, M, N, L, cd_m)) ||
+      (Y && !encode_epi(h->encode, &tmY, Y, dtypes->y, M, N, L, cd_m)))
+    return GEMM_ERR_CUDA;
+
   KernelParams kp{};
   kp.M = (int)M; kp.N = (int)N; kp.K = (int)K; kp.L = (int)L;
   kp.tiles_m = (int)cdiv(M, cfg.tile_m);
@@ -483,23 +552,27 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
   kp.idesc = make_idesc(dtypes->ab, cfg.cta_group, cfg.tile_n, a_mn, b_mn);
   kp.status = h->d_status;
   kp.timeout_ns = h->timeout_ns;
-  kp.epi.C = C;
-  kp.epi.X = X;
-  kp.epi.D = D;
-  kp.epi.Y = Y;
   kp.epi.c_dt = dtypes->c;
   kp.epi.d_dt = dtypes->d;
   kp.epi.x_dt = dtypes->x;
   kp.epi.y_dt = dtypes->y;
-  kp.epi.cd_m_major = dtypes->cdxy_major == GEMM_MN_MAJOR;
+  kp.epi.cd_m_major = cd_m;
   kp.epi.read_c = reads_c(p);
   kp.epi.read_x = reads_x(p);
   kp.epi.write_y = Y != nullptr;
   kp.epi.alpha = alpha;
   kp.epi.beta = beta;
   kp.epi.x_factor = x_factor;
+  kp.epi.slots = cfg.epi_slots;
+  {
+    const int sub = 128 * gb300::kEpiChunk;
+    int cd = dtype_bytes(dtypes->d);
+    if (reads_c(p)) cd = std::max(cd, dtype_bytes(dtypes->c));
+    kp.epi.cd_bytes = (uint32_t)(sub * cd);
+    kp.epi.xy_bytes = (uint32_t)(cfg.epi_slot_bytes - sub * cd);
+  }
 
-  void* args[3] = {&tmA, &tmB, &kp};
+  void* args[7] = {&tmA, &tmB, &tmC, &tmX, &tmD, &tmY, &kp};
   if (cudaLaunchKernelExC(&lc, kern, args) != cudaSuccess) {
     cudaGetLastError();
     return GEMM_ERR_CUDA;

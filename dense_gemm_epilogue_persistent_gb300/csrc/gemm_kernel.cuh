@@ -4,13 +4,15 @@
 //
 // What the kernel computes and its warp roles follow "custom_epilogue_dense_gemm.py"
 // (CuTeDSL Blackwell example), module docstring "This GEMM works as follows" (DMA
-// warp, MMA warp, EPILOGUE warps; persistent tile scheduling) and the 2-SM tcgen05
-// scheme of "04_mma_tma_2sm_sm100.cu" (CuTe Blackwell tutorial 04, "Step 2: The
-// Mainloop" -- the leader CTA issues the pair's MMA; tensor-memory allocation and
-// MMA-completion arrivals reach both CTAs).  The thread roles (128 epilogue threads +
-// one MMA warp + one TMA warp = 192 threads, one CTA per SM, the whole 512-column
-// tensor memory split into accumulator stages) follow the cuBLASDx "API Card:
-// Blackwell Pipeline (tcgen05)", host-side and "Depth and shared memory" bullets.
+// warp; MMA warp; EPILOGUE warps that tcgen05.ld the accumulator, TMA-load C and X
+// through shared memory, compute Y and D, and TMA-store D and Y; persistent tile
+// scheduling) and the 2-SM tcgen05 scheme of "04_mma_tma_2sm_sm100.cu" (CuTe
+// Blackwell tutorial 04, "Step 2: The Mainloop": the leader CTA issues the pair's
+// MMA; tensor-memory allocation and MMA-completion arrivals reach both CTAs).  The
+// thread roles (128 epilogue threads + one MMA warp + one TMA warp = 192 threads,
+// one CTA per SM, the whole 512-column tensor memory split into accumulator stages)
+// follow the cuBLASDx "API Card: Blackwell Pipeline (tcgen05)", host-side and
+// "Depth and shared memory" bullets.
 //
 // Block = 6 warps:
 //   warp 0      TMA producer: one lane streams A and B k-blocks into a ring of
@@ -19,16 +21,21 @@
 //               issues tcgen05.mma into one of two accumulator stages in tensor
 //               memory, frees ring slots with tcgen05.commit, and hands finished
 //               accumulators to the epilogue with another commit.
-//   warps 2..5  epilogue: tcgen05.ld the accumulator (warp w owns TMEM lanes
-//               32*(w%4)..+31 = tile rows), release the accumulator stage, read C
-//               and X, compute in fp32, convert and store D and Y.
+//   warps 2..5  epilogue: warp w owns TMEM lanes 32*(w%4)..+31 (= tile rows).  The
+//               tile is processed in 32-column chunks through a ring of `slots`
+//               shared-memory slots: C and X sub-tiles are TMA-loaded `slots-1`
+//               chunks ahead (across tile boundaries, so the next tile's C/X arrive
+//               during its main loop); each thread reads its row, computes in fp32,
+//               writes D and Y back into the slot, and one thread TMA-stores them.
 // Every CTA (pair) walks the same static persistent tile sequence
 // t = cluster_id, cluster_id + num_clusters, ...; with two accumulator stages the
 // epilogue of tile i overlaps the main loop of tile i+1.
 //
 // Every barrier wait is bounded (watchdog): on expiry the kernel records a code
 // in a device status word, raises a CTA-wide abort flag, lets in-flight copies
-// drain, frees its tensor memory and returns.
+// drain, frees its tensor memory and returns.  Epilogue decisions that follow a
+// wait are made uniform across the 128 epilogue threads with bar.red.and, so no
+// thread is ever left alone at a named barrier.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -41,14 +48,13 @@ namespace gb300 {
 enum : int { DT_F32 = 0, DT_F16 = 1, DT_BF16 = 2, DT_E4M3 = 3 };
 
 struct EpiParams {
-  const void* C;
-  const void* X;
-  void* D;
-  void* Y;
   int c_dt, d_dt, x_dt, y_dt;
   int cd_m_major;            // 0: (l*M + m)*N + n   1: (l*N + n)*M + m
   int read_c, read_x, write_y;
   float alpha, beta, x_factor;
+  int slots;                 // epilogue shared-memory slots (>= 2)
+  uint32_t cd_bytes;         // bytes of a slot's C/D region
+  uint32_t xy_bytes;         // bytes of a slot's X/Y region (0: neither X nor Y)
 };
 
 struct KernelParams {
@@ -57,7 +63,7 @@ struct KernelParams {
   int num_tiles;             // tiles_m * tiles_n * L
   int k_blocks;              // ceil(K / tile_k)
   int group_m;               // rasterisation strip height (tiles)
-  int stages;                // ring depth
+  int stages;                // A/B ring depth
   int a_mn_major, b_mn_major;
   uint32_t idesc;            // tcgen05 instruction descriptor
   uint32_t* status;          // device status word (watchdog)
@@ -68,6 +74,9 @@ struct KernelParams {
 constexpr int kThreads = 192;
 constexpr int kAccStages = 2;
 constexpr uint32_t kTmemCols = 512;
+constexpr int kEpiChunk = 32;          // columns per epilogue chunk
+constexpr int kEpiLeader = 64;         // thread that issues the epilogue's TMA
+constexpr uint32_t kEpiBarrier = 1;    // named barrier of the 128 epilogue threads
 
 template <int CG, int BN, int AB_BYTES>
 struct Geometry {
@@ -80,12 +89,15 @@ struct Geometry {
   static constexpr int K_STEPS = BK / UMMA_K;    // instructions per stage
   static constexpr int ATOM_MN = 128 / AB_BYTES; // MN extent of one MN-major swizzle atom
   static constexpr int ATOM_BYTES = BK * 128;    // bytes of one MN-major atom column
-  static_assert(BN % 32 == 0 && BN <= 256, "tile_n");
+  static constexpr int CHUNKS = BN / kEpiChunk;  // epilogue chunks per tile
+  static_assert(BN % kEpiChunk == 0 && BN <= 256, "tile_n");
   static_assert(kAccStages * BN <= (int)kTmemCols, "accumulators must fit tensor memory");
 };
 
 // Watchdog codes: 0xE0RRBBBB, RR = role, BBBB = low 16 bits of blockIdx.x.
-enum : uint32_t { kWaitProducer = 1, kWaitMmaFull = 2, kWaitMmaAcc = 3, kWaitEpilogue = 4 };
+enum : uint32_t {
+  kWaitProducer = 1, kWaitMmaFull = 2, kWaitMmaAcc = 3, kWaitEpilogue = 4, kWaitEpiLoad = 5
+};
 
 struct Watch {
   volatile uint32_t* abort;
@@ -124,7 +136,7 @@ __device__ __forceinline__ void tile_coords(int t, const KernelParams& p, int& t
   tn = rr / gm;
 }
 
-// ------------------------------------------------------------------ epilogue I/O
+// ------------------------------------------------------------------ epilogue smem
 
 __device__ __forceinline__ float bits16_to_f32(uint32_t b, int dt) {
   return dt == DT_BF16 ? __uint_as_float(b << 16) : __half2float(__ushort_as_half((uint16_t)b));
@@ -135,109 +147,81 @@ __device__ __forceinline__ uint32_t f32_to_bits16(float v, int dt) {
                        : (uint32_t)__half_as_ushort(__float2half_rn(v));
 }
 
-// Load 8 consecutive row elements starting at element `off` (16-byte aligned)
-// of a row-major tensor; `valid` elements of the 8 exist (8 or 4).
-__device__ __forceinline__ void load8(const void* base, int dt, int64_t off, int valid,
-                                      float (&v)[8]) {
-  if (dt == DT_F32) {
-    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + off);
-    const float4 a = p[0];
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    if (valid > 4) {
-      const float4 b = p[1];
-      v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+// Epilogue sub-tiles hold 128 rows x 32 columns of one tensor, as TMA lays them out:
+//   row-major tensors: [row][32 columns], 128-byte rows (fp32, 128-byte swizzle:
+//     16-byte chunk j of row r sits at chunk j ^ (r & 7)) or 64-byte rows (16-bit,
+//     64-byte swizzle: chunk j ^ ((r >> 1) & 3));
+//   column-major tensors: [column][128 rows], unswizzled.
+// Thread r touches only row r; the swizzles make each 8-row group of a warp hit
+// distinct banks.
+__device__ __forceinline__ void smem_read_row(const uint8_t* sub, int dt, int m_major, int r,
+                                              float (&v)[kEpiChunk]) {
+  if (!m_major) {
+    if (dt == DT_F32) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 q = *reinterpret_cast<const float4*>(sub + r * 128 + ((j ^ (r & 7)) << 4));
+        v[4 * j] = q.x; v[4 * j + 1] = q.y; v[4 * j + 2] = q.z; v[4 * j + 3] = q.w;
+      }
     } else {
-      v[4] = v[5] = v[6] = v[7] = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 q =
+            *reinterpret_cast<const uint4*>(sub + r * 64 + ((j ^ ((r >> 1) & 3)) << 4));
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          v[8 * j + 2 * i] = bits16_to_f32(w[i] & 0xFFFFu, dt);
+          v[8 * j + 2 * i + 1] = bits16_to_f32(w[i] >> 16, dt);
+        }
+      }
     }
   } else {
-    const uint4 q = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + off);
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    if (dt == DT_F32) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      v[2 * i] = bits16_to_f32(w[i] & 0xFFFFu, dt);
-      v[2 * i + 1] = bits16_to_f32(w[i] >> 16, dt);
+      for (int c = 0; c < kEpiChunk; ++c)
+        v[c] = *reinterpret_cast<const float*>(sub + (c * 128 + r) * 4);
+    } else {
+#pragma unroll
+      for (int c = 0; c < kEpiChunk; ++c)
+        v[c] = bits16_to_f32(*reinterpret_cast<const uint16_t*>(sub + (c * 128 + r) * 2), dt);
     }
   }
 }
 
-__device__ __forceinline__ void store8(void* base, int dt, int64_t off, int valid,
-                                       const float (&v)[8]) {
-  if (dt == DT_F32) {
-    float4* p = reinterpret_cast<float4*>(static_cast<float*>(base) + off);
-    p[0] = make_float4(v[0], v[1], v[2], v[3]);
-    if (valid > 4) p[1] = make_float4(v[4], v[5], v[6], v[7]);
-  } else {
-    uint4 q;
-    q.x = f32_to_bits16(v[0], dt) | (f32_to_bits16(v[1], dt) << 16);
-    q.y = f32_to_bits16(v[2], dt) | (f32_to_bits16(v[3], dt) << 16);
-    q.z = f32_to_bits16(v[4], dt) | (f32_to_bits16(v[5], dt) << 16);
-    q.w = f32_to_bits16(v[6], dt) | (f32_to_bits16(v[7], dt) << 16);
-    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(base) + off) = q;
-  }
-}
-
-__device__ __forceinline__ float load1(const void* base, int dt, int64_t off) {
-  if (dt == DT_F32) return static_cast<const float*>(base)[off];
-  return bits16_to_f32(static_cast<const uint16_t*>(base)[off], dt);
-}
-
-__device__ __forceinline__ void store1(void* base, int dt, int64_t off, float v) {
-  if (dt == DT_F32)
-    static_cast<float*>(base)[off] = v;
-  else
-    static_cast<uint16_t*>(base)[off] = (uint16_t)f32_to_bits16(v, dt);
-}
-
-__device__ __forceinline__ float epi_combine(const EpiParams& e, float acc, float c, float x) {
-  // alpha*acc + beta*c + x_factor*x in fp32 (terms that are not read are 0).
-  return fmaf(e.alpha, acc, fmaf(e.beta, c, e.x_factor * x));
-}
-
-// One thread's 32 consecutive columns [col0, col0+32) of output row `row`.
-__device__ __forceinline__ void epilogue_row_chunk(const EpiParams& e, int M, int N, int row,
-                                                   int col0, int l, const float (&acc)[32]) {
-  if (row >= M) return;
-  const int64_t batch = (int64_t)l * M * N;
-  if (!e.cd_m_major) {
-    const int64_t rowoff = batch + (int64_t)row * N;
+__device__ __forceinline__ void smem_write_row(uint8_t* sub, int dt, int m_major, int r,
+                                               const float (&v)[kEpiChunk]) {
+  if (!m_major) {
+    if (dt == DT_F32) {
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      const int c = col0 + 8 * g;
-      if (c >= N) break;
-      const int valid = min(8, N - c);
-      float cv[8], xv[8], dv[8], yv[8];
-      if (e.read_c) load8(e.C, e.c_dt, rowoff + c, valid, cv);
-      else {
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<float4*>(sub + r * 128 + ((j ^ (r & 7)) << 4)) =
+            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) cv[i] = 0.f;
+      for (int j = 0; j < 4; ++j) {
+        uint4 q;
+        q.x = f32_to_bits16(v[8 * j + 0], dt) | (f32_to_bits16(v[8 * j + 1], dt) << 16);
+        q.y = f32_to_bits16(v[8 * j + 2], dt) | (f32_to_bits16(v[8 * j + 3], dt) << 16);
+        q.z = f32_to_bits16(v[8 * j + 4], dt) | (f32_to_bits16(v[8 * j + 5], dt) << 16);
+        q.w = f32_to_bits16(v[8 * j + 6], dt) | (f32_to_bits16(v[8 * j + 7], dt) << 16);
+        *reinterpret_cast<uint4*>(sub + r * 64 + ((j ^ ((r >> 1) & 3)) << 4)) = q;
       }
-      if (e.read_x) load8(e.X, e.x_dt, rowoff + c, valid, xv);
-      else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) xv[i] = 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        yv[i] = acc[8 * g + i];
-        dv[i] = epi_combine(e, yv[i], cv[i], xv[i]);
-      }
-      store8(e.D, e.d_dt, rowoff + c, valid, dv);
-      if (e.write_y) store8(e.Y, e.y_dt, rowoff + c, valid, yv);
     }
   } else {
-    // Column-major outputs: each store instruction of the warp covers 32
-    // consecutive rows of one column.
-#pragma unroll 4
-    for (int j = 0; j < 32; ++j) {
-      const int col = col0 + j;
-      if (col >= N) break;
-      const int64_t off = batch + (int64_t)col * M + row;
-      const float c = e.read_c ? load1(e.C, e.c_dt, off) : 0.f;
-      const float x = e.read_x ? load1(e.X, e.x_dt, off) : 0.f;
-      store1(e.D, e.d_dt, off, epi_combine(e, acc[j], c, x));
-      if (e.write_y) store1(e.Y, e.y_dt, off, acc[j]);
+    if (dt == DT_F32) {
+#pragma unroll
+      for (int c = 0; c < kEpiChunk; ++c) *reinterpret_cast<float*>(sub + (c * 128 + r) * 4) = v[c];
+    } else {
+#pragma unroll
+      for (int c = 0; c < kEpiChunk; ++c)
+        *reinterpret_cast<uint16_t*>(sub + (c * 128 + r) * 2) = (uint16_t)f32_to_bits16(v[c], dt);
     }
   }
+}
+
+__device__ __forceinline__ uint32_t sub_bytes(int dt) {
+  return (uint32_t)(128 * kEpiChunk) * (dt == DT_F32 ? 4u : 2u);
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -246,13 +230,17 @@ template <int CG, int BN, int AB_BYTES>
 __global__ void __launch_bounds__(kThreads, 1)
 persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmC,
+                       const __grid_constant__ CUtensorMap tmX,
+                       const __grid_constant__ CUtensorMap tmD,
+                       const __grid_constant__ CUtensorMap tmY,
                        const __grid_constant__ KernelParams p) {
   using G = Geometry<CG, BN, AB_BYTES>;
   constexpr int KIND = (AB_BYTES == 1) ? 1 : 0;
 
   extern __shared__ uint8_t smem_raw[];
-  // 1024-byte alignment for the 128-byte-swizzle atoms (identical in both CTAs
-  // of a pair: same kernel, same layout).
+  // 1024-byte alignment for the swizzle atoms (identical in both CTAs of a pair:
+  // same kernel, same layout).
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const gbase = smem_raw + (base - raw);
@@ -263,14 +251,20 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   const int cluster_id = blockIdx.x / CG;
   const int num_clusters = gridDim.x / CG;
   const int S = p.stages;
+  const EpiParams& e = p.epi;
+  const int E = e.slots;
+  const uint32_t slot_bytes = e.cd_bytes + e.xy_bytes;
 
-  // Shared layout: [B ring][A ring][full x S][empty x S][tfull x 2][tempty x 2][tmem addr][abort]
+  // [B ring][A ring][epilogue slots][full x S][empty x S][tfull x 2][tempty x 2]
+  // [cfull x E][tmem address][abort flag]
   const uint32_t b_ring = base;
   const uint32_t a_ring = b_ring + S * G::B_STAGE;
-  const uint32_t bars = a_ring + S * G::A_STAGE;
+  const uint32_t epi0 = a_ring + S * G::A_STAGE;
+  const uint32_t bars = epi0 + E * slot_bytes;
   const uint32_t full0 = bars, empty0 = bars + 8u * S;
   const uint32_t tfull0 = bars + 16u * S, tempty0 = tfull0 + 16u;
-  const uint32_t holder = tempty0 + 16u;
+  const uint32_t cfull0 = tempty0 + 16u;
+  const uint32_t holder = cfull0 + 8u * E;
   volatile uint32_t* const holder_ptr = reinterpret_cast<volatile uint32_t*>(gbase + (holder - base));
   volatile uint32_t* const abort_ptr = holder_ptr + 1;
 
@@ -283,6 +277,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       mbar_init(tfull0 + 8u * a, 1);
       mbar_init(tempty0 + 8u * a, 4 * CG);   // every epilogue warp of the CTA (pair)
     }
+    for (int s = 0; s < E; ++s) mbar_init(cfull0 + 8u * s, 1);
     *abort_ptr = 0u;
     fence_barrier_init();
   }
@@ -383,22 +378,64 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   } else {
     // ---------------------------------------------------------- epilogue
     const int q = warp & 3;                 // TMEM lane quarter this warp may read
+    const int r = q * 32 + lane;            // this thread's row within the CTA's 128
+    const bool leader = threadIdx.x == kEpiLeader;
+    const bool loads = e.read_c || e.read_x;
+    const uint32_t load_tx = (e.read_c ? sub_bytes(e.c_dt) : 0u) + (e.read_x ? sub_bytes(e.x_dt) : 0u);
+
+    // Epilogue chunk c of this CTA's stream: tile ordinal c / CHUNKS, columns
+    // 32*(c % CHUNKS).. of that tile.  TMA coordinates are (column, row, batch)
+    // for row-major C/D/X/Y and (row, column, batch) for column-major ones.
+    auto chunk_origin = [&](int c, int& row0, int& col0, int& tl) -> bool {
+      const int ord = c / G::CHUNKS;
+      const int t = cluster_id + ord * num_clusters;
+      if (t >= p.num_tiles) return false;
+      int tm, tn;
+      tile_coords(t, p, tm, tn, tl);
+      row0 = tm * (G::BM * CG) + (int)rank * G::BM;
+      col0 = tn * BN + (c - ord * G::CHUNKS) * kEpiChunk;
+      return true;
+    };
+    auto issue_loads = [&](int c) {         // leader only
+      int row0, col0, tl;
+      if (!chunk_origin(c, row0, col0, tl)) return;
+      const uint32_t slot = epi0 + (uint32_t)(c % E) * slot_bytes;
+      const uint32_t bar = cfull0 + 8u * (uint32_t)(c % E);
+      const int x0 = e.cd_m_major ? row0 : col0, x1 = e.cd_m_major ? col0 : row0;
+      mbar_arrive_expect_tx(bar, load_tx);
+      if (e.read_c) tma_load_3d(slot, &tmC, bar, x0, x1, tl);
+      if (e.read_x) tma_load_3d(slot + e.cd_bytes, &tmX, bar, x0, x1, tl);
+    };
+
+    if (leader) {
+      prefetch_tensormap(&tmD);
+      if (e.write_y) prefetch_tensormap(&tmY);
+      if (loads) {
+        if (e.read_c) prefetch_tensormap(&tmC);
+        if (e.read_x) prefetch_tensormap(&tmX);
+        for (int c = 0; c < E - 1; ++c) issue_loads(c);
+      }
+    }
+
     int acc = 0;
     uint32_t aph = 0;
-    for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
+    int gc = 0;                             // chunk counter of this CTA's stream
+    bool ok = true;
+    for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
       int tm, tn, tl;
       tile_coords(t, p, tm, tn, tl);
-      if (!wait_phase(tfull0 + 8u * acc, aph, w, kWaitEpilogue)) break;
+      ok = named_barrier_and(kEpiBarrier, 128, wait_phase(tfull0 + 8u * acc, aph, w, kWaitEpilogue));
+      if (!ok) break;
       tc_fence_after_sync();
-      const int row = tm * (G::BM * CG) + (int)rank * G::BM + q * 32 + lane;
+      const int row0 = tm * (G::BM * CG) + (int)rank * G::BM;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_load_32cols(tbase + 32u * c, r);
+      for (int j = 0; j < G::CHUNKS; ++j, ++gc) {
+        uint32_t raw_acc[32];
+        tmem_load_32cols(tbase + 32u * j, raw_acc);
         tmem_wait_ld();
-        if (c == BN / 32 - 1) {
-          // The whole stage has been read: hand it back to the MMA warp.
+        if (j == G::CHUNKS - 1) {
+          // The whole accumulator stage has been read: hand it back to the MMA warp.
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) {
@@ -406,13 +443,47 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             else mbar_arrive_cluster(map_to_rank(tempty0 + 8u * acc, 0));
           }
         }
-        float v[32];
+        const int slot_idx = gc % E;
+        uint8_t* const slot = gbase + (epi0 - base) + (uint32_t)slot_idx * slot_bytes;
+        float cv[kEpiChunk], xv[kEpiChunk];
+        bool got = true;
+        if (loads) got = wait_phase(cfull0 + 8u * slot_idx, (uint32_t)(gc / E) & 1u, w, kWaitEpiLoad);
+        if (got && e.read_c) smem_read_row(slot, e.c_dt, e.cd_m_major, r, cv);
+        if (got && e.read_x) smem_read_row(slot + e.cd_bytes, e.x_dt, e.cd_m_major, r, xv);
+        // Every thread has read the slot (and agrees whether to go on) before any
+        // thread overwrites it with D and Y.
+        ok = named_barrier_and(kEpiBarrier, 128, got);
+        if (!ok) break;
+        float dv[kEpiChunk], yv[kEpiChunk];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = p.k_blocks > 0 ? __uint_as_float(r[j]) : 0.f;
-        epilogue_row_chunk(p.epi, p.M, p.N, row, tn * BN + 32 * c, tl, v);
+        for (int i = 0; i < kEpiChunk; ++i) {
+          const float a = p.k_blocks > 0 ? __uint_as_float(raw_acc[i]) : 0.f;
+          const float c = e.read_c ? cv[i] : 0.f;
+          const float x = e.read_x ? xv[i] : 0.f;
+          yv[i] = a;
+          dv[i] = fmaf(e.alpha, a, fmaf(e.beta, c, e.x_factor * x));
+        }
+        smem_write_row(slot, e.d_dt, e.cd_m_major, r, dv);
+        if (e.write_y) smem_write_row(slot + e.cd_bytes, e.y_dt, e.cd_m_major, r, yv);
+        fence_proxy_async_smem();
+        named_barrier_sync(kEpiBarrier, 128);
+        if (leader) {
+          const int col0 = tn * BN + j * kEpiChunk;
+          const int x0 = e.cd_m_major ? row0 : col0, x1 = e.cd_m_major ? col0 : row0;
+          const uint32_t s_addr = epi0 + (uint32_t)slot_idx * slot_bytes;
+          tma_store_3d(&tmD, s_addr, x0, x1, tl);
+          if (e.write_y) tma_store_3d(&tmY, s_addr + e.cd_bytes, x0, x1, tl);
+          bulk_commit_group();
+          // The slot of chunk gc+1 (and, with loads, of chunk gc+E-1, i.e. the
+          // slot of chunk gc-1) is free once at most one store group -- this
+          // chunk's -- still reads shared memory.
+          bulk_wait_group_read<1>();
+          if (loads) issue_loads(gc + E - 1);
+        }
       }
       if (++acc == kAccStages) { acc = 0; aph ^= 1u; }
     }
+    if (leader) bulk_wait_group_all();
   }
 
   // ------------------------------------------------------------ teardown

@@ -85,7 +85,12 @@ typedef struct {
  *   ring_bytes  ring bytes per CTA: stages*(A stage + B stage) + 8 bytes per
  *               mbarrier (2 per stage, 2 per accumulator stage) + 4 bytes of
  *               tensor-memory address.
- *   smem_bytes  dynamic shared memory per CTA (ring + alignment slack).
+ *   epi_slots   epilogue shared-memory slots: C/X sub-tiles (128 rows x 32
+ *               columns) are TMA-loaded epi_slots-1 chunks ahead; D/Y are staged
+ *               in the same slot and TMA-stored.
+ *   epi_slot_bytes  bytes of one epilogue slot.
+ *   smem_bytes  dynamic shared memory per CTA (ring + epilogue slots + their
+ *               barriers + alignment slack).
  *   tiles       number of output tiles; grid_ctas: CTAs launched. */
 typedef struct {
   int cta_group, tile_n, stages, group_m;
@@ -93,6 +98,7 @@ typedef struct {
   int ring_bytes, smem_bytes;
   int64_t tiles;
   int grid_ctas;
+  int epi_slots, epi_slot_bytes;
 } gemm_config_t;
 
 /* Every argument of one gemm_run call, for the host-only planning calls. */
