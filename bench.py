@@ -403,12 +403,22 @@ def main():
                "status": G.gemm_status_string(st)}
         del h_in, h_out, d_in
 
-    peak = tensor_peak(peaks, w.ab)
+    # The measured peaks come as a burst (cuBLAS, best of 10) and a sustained
+    # figure (back to back for seconds, under the power cap).  A timed region
+    # of a second or more of back-to-back launches is compared with the
+    # sustained one; a short region with the burst one.
+    sustained = max_ms >= 1000.0
+    peak = tensor_peak(peaks, w.ab, sustained=sustained)
+    burst = tensor_peak(peaks, w.ab, sustained=False)
     achieved = flops / (kernel_ms / 1e3) / 1e12
+    ratio_note = " x2 (fp8/bf16 nominal ratio)" if w.ab == "e4m3" else ""
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": recorded_traffic(w.name),
-                "peak_source": f"{peaks['source']} bf16 burst"
-                               + (" x2 (fp8/bf16 nominal ratio)" if w.ab == "e4m3" else "")}
+                "algorithmic_flops_per_launch": flops,
+                "peak_source": f"{peaks['source']} bf16 "
+                               f"{'sustained' if sustained else 'burst'}{ratio_note}; timed "
+                               f"region {max_ms / 1e3:.2f} s of back-to-back launches",
+                "frac_of_burst_peak": achieved / burst}
 
     per_config = None
     cpu_baseline = None
@@ -453,6 +463,7 @@ def main():
                              f"({bound.nbytes_in() / 2**20:.0f} MiB of A,B,C,X vs 129 MB)",
                        "parallelism": f"replicas x{world}"},
             "pct_of_peak": 100.0 * value / world / peak,
+            "peak_tflops": peak,
             "roofline": roofline,
             "cpu_baseline": cpu_baseline,
             "e2e": e2e,

@@ -165,17 +165,23 @@ bool variant_supports(const gemm_problem_t& p, int cg, int bn) {
   return true;
 }
 
-// Relative cost of running `tiles` tiles of one variant: full waves of
-// 128 x tile_n work per SM, weighted by how close the variant's shared-memory
-// operand traffic comes to the SM's read bandwidth.
-double plan_cost(int64_t tiles, int cg, int bn, int sm_count) {
+// Relative cost of running `tiles` tiles of one variant on `sm_count` SMs:
+// waves of tiles times the time of one tile, in units of one k-block of a CTA
+// pair's 256 x 256 tile.  Fitted to sweeps of the five benchmark shapes on
+// GB300 (8192^3, 2048^3, 16 x 1024^2 x 4096, 3000 x 5000 x 4096 fp8):
+//   per k-block  2x256: 1.0   1x256: 1.13   2x128: 1.3   1x128: 0.93
+//   (128-wide tiles halve the MMA work per k-block but not the operand
+//   traffic, so L2->SM bandwidth, not the tensor pipe, sets their pace; a CTA
+//   pair halves the B traffic of each SM)
+//   fixed per tile (pipeline fill, epilogue tail): pair 17, single CTA 10.
+double plan_cost(int64_t tiles, int64_t k_blocks, int cg, int bn, int sm_count) {
   const int64_t units = std::max(1, sm_count / cg);
   const double waves = (double)cdiv(tiles, units);
-  double eff = 1.0;
-  if (cg == 1 && bn == 256) eff = 1.06;
-  if (cg == 2 && bn == 128) eff = 1.12;
-  if (cg == 1 && bn == 128) eff = 1.25;
-  return waves * bn * eff;
+  double per_kb;
+  if (bn == 256) per_kb = cg == 2 ? 1.0 : 1.13;
+  else per_kb = cg == 2 ? 1.3 : 0.93;
+  const double fixed = cg == 2 ? 17.0 : 10.0;
+  return waves * ((double)k_blocks * per_kb + fixed);
 }
 
 gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
@@ -198,7 +204,7 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
         if (!variant_supports(p, a, b)) continue;
         const int64_t tiles = cdiv(std::max<int64_t>(p.M, 1), 128 * a) *
                               cdiv(std::max<int64_t>(p.N, 1), b) * std::max<int64_t>(p.L, 1);
-        const double c = plan_cost(tiles, a, b, sm_count);
+        const double c = plan_cost(tiles, cdiv(p.K, 128 / ab_bytes), a, b, sm_count);
         if (c < best) { best = c; bcg = a; bbn = b; }
       }
     if (!bcg) return GEMM_ERR_UNSUPPORTED_CONFIG;
@@ -211,7 +217,7 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
         if (!variant_supports(p, a, b)) continue;
         const int64_t tiles = cdiv(std::max<int64_t>(p.M, 1), 128 * a) *
                               cdiv(std::max<int64_t>(p.N, 1), b) * std::max<int64_t>(p.L, 1);
-        const double c = plan_cost(tiles, a, b, sm_count);
+        const double c = plan_cost(tiles, cdiv(p.K, 128 / ab_bytes), a, b, sm_count);
         if (c < best - 1e-9) { best = c; cg = a; bn = b; }
       }
     if (!cg) return GEMM_ERR_UNSUPPORTED_CONFIG;
