@@ -54,7 +54,7 @@ struct gemm_handle {
   gemm_config_t forced_cfg{};
   gemm_config_t last{};
   uint64_t timeout_ns = kDefaultTimeoutNs;
-  VariantState variants[2][2][2];   // [ab 16/8][cta_group 1/2][tile_n 128/256]
+  VariantState variants[2][2][2][2];   // [ab 16/8][cta_group 1/2][tile_n 128/256][mc 1/2]
   std::mutex mu;
 };
 
@@ -154,13 +154,14 @@ int total_smem(int cg, int bn, int ab_bytes, int stages, int slots, int slot_byt
   return ring_bytes(cg, bn, ab_bytes, stages) + slots * slot_bytes + 8 * slots + 4 + kSmemSlack;
 }
 
-bool variant_supports(const gemm_problem_t& p, int cg, int bn) {
+bool variant_supports(const gemm_problem_t& p, int cg, int bn, int mc) {
   if (cg != 1 && cg != 2) return false;
   if (bn != 128 && bn != 256) return false;
+  if (mc != 1 && mc != 2) return false;
   const int ab_bytes = dtype_bytes(p.dtypes.ab);
   const int atom = 128 / ab_bytes;
-  // MN-major B is staged in swizzle atoms of `atom` rows per CTA.
-  if (p.layoutB == GEMM_MN_MAJOR && (bn / cg) % atom != 0) return false;
+  // MN-major B is staged (and multicast) in swizzle atoms of `atom` rows.
+  if (p.layoutB == GEMM_MN_MAJOR && (bn / cg / mc) % atom != 0) return false;
   if (p.layoutA == GEMM_MN_MAJOR && 128 % atom != 0) return false;
   return true;
 }
@@ -174,8 +175,8 @@ bool variant_supports(const gemm_problem_t& p, int cg, int bn) {
 //   traffic, so L2->SM bandwidth, not the tensor pipe, sets their pace; a CTA
 //   pair halves the B traffic of each SM)
 //   fixed per tile (pipeline fill, epilogue tail): pair 17, single CTA 10.
-double plan_cost(int64_t tiles, int64_t k_blocks, int cg, int bn, int sm_count) {
-  const int64_t units = std::max(1, sm_count / cg);
+double plan_cost(int64_t tiles, int64_t k_blocks, int cg, int mc, int bn, int sm_count) {
+  const int64_t units = std::max(1, sm_count / (cg * mc));
   const double waves = (double)cdiv(tiles, units);
   double per_kb;
   if (bn == 256) per_kb = cg == 2 ? 1.0 : 1.13;
@@ -192,36 +193,24 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
   const gemm_problem_t& p = *pp;
   const int ab_bytes = dtype_bytes(p.dtypes.ab);
 
-  int cg = forced ? forced->cta_group : 0;
-  int bn = forced ? forced->tile_n : 0;
-  if (cg || bn) {
-    const int cgs[2] = {1, 2}, bns[2] = {128, 256};
-    double best = 1e300;
-    int bcg = 0, bbn = 0;
-    for (int a : cgs)
-      for (int b : bns) {
-        if ((cg && a != cg) || (bn && b != bn)) continue;
-        if (!variant_supports(p, a, b)) continue;
-        const int64_t tiles = cdiv(std::max<int64_t>(p.M, 1), 128 * a) *
+  const int fcg = forced ? forced->cta_group : 0;
+  const int fbn = forced ? forced->tile_n : 0;
+  const int fmc = forced ? forced->cluster_m : 0;
+  int cg = 0, bn = 0, mc = 0;
+  double best = 1e300;
+  for (int a : {2, 1})
+    for (int b : {256, 128})
+      for (int m : {1, 2}) {
+        if ((fcg && a != fcg) || (fbn && b != fbn)) continue;
+        // Multicast clusters are used only when asked for.
+        if (fmc ? m != fmc : m != 1) continue;
+        if (!variant_supports(p, a, b, m)) continue;
+        const int64_t tiles = cdiv(std::max<int64_t>(p.M, 1), 128 * a * m) *
                               cdiv(std::max<int64_t>(p.N, 1), b) * std::max<int64_t>(p.L, 1);
-        const double c = plan_cost(tiles, cdiv(p.K, 128 / ab_bytes), a, b, sm_count);
-        if (c < best) { best = c; bcg = a; bbn = b; }
+        const double c = plan_cost(tiles, cdiv(p.K, 128 / ab_bytes), a, m, b, sm_count);
+        if (c < best - 1e-9) { best = c; cg = a; bn = b; mc = m; }
       }
-    if (!bcg) return GEMM_ERR_UNSUPPORTED_CONFIG;
-    cg = bcg;
-    bn = bbn;
-  } else {
-    double best = 1e300;
-    for (int a : {2, 1})
-      for (int b : {256, 128}) {
-        if (!variant_supports(p, a, b)) continue;
-        const int64_t tiles = cdiv(std::max<int64_t>(p.M, 1), 128 * a) *
-                              cdiv(std::max<int64_t>(p.N, 1), b) * std::max<int64_t>(p.L, 1);
-        const double c = plan_cost(tiles, cdiv(p.K, 128 / ab_bytes), a, b, sm_count);
-        if (c < best - 1e-9) { best = c; cg = a; bn = b; }
-      }
-    if (!cg) return GEMM_ERR_UNSUPPORTED_CONFIG;
-  }
+  if (!cg) return GEMM_ERR_UNSUPPORTED_CONFIG;
   if (gemm_tmem_columns(128, bn) * gb300::kAccStages > (int)gb300::kTmemCols)
     return GEMM_ERR_UNSUPPORTED_CONFIG;
 
@@ -238,7 +227,7 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
   int stages = forced && forced->stages ? forced->stages : max_stages;
   if (stages < 2 || stages > max_stages) return GEMM_ERR_UNSUPPORTED_CONFIG;
 
-  const int64_t tiles_m = cdiv(std::max<int64_t>(p.M, 1), 128 * cg);
+  const int64_t tiles_m = cdiv(std::max<int64_t>(p.M, 1), 128 * cg * mc);
   const int64_t tiles_n = cdiv(std::max<int64_t>(p.N, 1), bn);
   const int64_t tiles = tiles_m * tiles_n * std::max<int64_t>(p.L, 1);
   int group_m = forced && forced->group_m ? forced->group_m : 8;
@@ -250,6 +239,7 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
   c.stages = stages;
   c.group_m = group_m;
   c.tile_m = 128 * cg;
+  c.cluster_m = mc;
   c.tile_k = 128 / ab_bytes;
   c.acc_stages = gb300::kAccStages;
   c.ring_bytes = ring_bytes(cg, bn, ab_bytes, stages);
@@ -260,8 +250,8 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
   c.smem_bytes = std::max(total_smem(cg, bn, ab_bytes, stages, slots, slot),
                           smem_optin / 2 + 1024);
   c.tiles = tiles;
-  const int64_t units = std::max(1, sm_count / cg);
-  c.grid_ctas = (int)(std::min<int64_t>(tiles, units) * cg);
+  const int64_t units = std::max(1, sm_count / (cg * mc));
+  c.grid_ctas = (int)(std::min<int64_t>(tiles, units) * cg * mc);
   *out = c;
   return GEMM_OK;
 }
@@ -443,6 +433,7 @@ GEMM_API gemm_status_t gemm_set_config(gemm_handle_t h, const gemm_config_t* cfg
   }
   if ((cfg->cta_group && cfg->cta_group != 1 && cfg->cta_group != 2) ||
       (cfg->tile_n && cfg->tile_n != 128 && cfg->tile_n != 256) || cfg->stages < 0 ||
+      (cfg->cluster_m && cfg->cluster_m != 1 && cfg->cluster_m != 2) ||
       cfg->stages > kMaxStages || cfg->group_m < 0)
     return GEMM_ERR_INVALID_ARG;
   h->forced = true;
@@ -486,11 +477,11 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
   if (st != GEMM_OK) return st;
 
   const int ab_bytes = dtype_bytes(dtypes->ab);
-  const void* kern = ab_bytes == 2 ? gb300::kernel_ab16(cfg.cta_group, cfg.tile_n)
-                                   : gb300::kernel_ab8(cfg.cta_group, cfg.tile_n);
+  const int csize = cfg.cta_group * cfg.cluster_m;
+  const void* kern = gb300::kernel_for(ab_bytes, cfg.cta_group, cfg.tile_n, cfg.cluster_m);
   if (!kern) return GEMM_ERR_UNSUPPORTED_CONFIG;
-  VariantState& vs =
-      h->variants[ab_bytes == 2 ? 0 : 1][cfg.cta_group - 1][cfg.tile_n == 256 ? 1 : 0];
+  VariantState& vs = h->variants[ab_bytes == 2 ? 0 : 1][cfg.cta_group - 1]
+                                [cfg.tile_n == 256 ? 1 : 0][cfg.cluster_m - 1];
 
   cudaLaunchConfig_t lc{};
   cudaLaunchAttribute attr[1];
@@ -498,7 +489,7 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
   lc.dynamicSmemBytes = (size_t)cfg.smem_bytes;
   lc.stream = reinterpret_cast<cudaStream_t>(stream);
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)cfg.cta_group;
+  attr[0].val.clusterDim.x = (unsigned)csize;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   lc.attrs = attr;
@@ -511,7 +502,7 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
       return GEMM_ERR_CUDA;
     }
     int nclusters = 0;
-    lc.gridDim = dim3((unsigned)(cfg.cta_group * h->sm_count));
+    lc.gridDim = dim3((unsigned)(csize * h->sm_count));
     if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &lc) != cudaSuccess || nclusters <= 0) {
       cudaGetLastError();
       return GEMM_ERR_CUDA;
@@ -520,7 +511,7 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
     vs.max_clusters = nclusters;
   }
   const int64_t clusters = std::min<int64_t>(cfg.tiles, vs.max_clusters);
-  cfg.grid_ctas = (int)(clusters * cfg.cta_group);
+  cfg.grid_ctas = (int)(clusters * csize);
   lc.gridDim = dim3((unsigned)cfg.grid_ctas);
 
   const bool a_mn = layoutA == GEMM_MN_MAJOR, b_mn = layoutB == GEMM_MN_MAJOR;
@@ -530,7 +521,7 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
   if (K > 0) {
     if (!encode_operand(h->encode, &tmA, A, dtypes->ab, M, K, L, lda, a_mn, 128, cfg.tile_k) ||
         !encode_operand(h->encode, &tmB, B, dtypes->ab, N, K, L, ldb, b_mn,
-                        cfg.tile_n / cfg.cta_group, cfg.tile_k))
+                        cfg.tile_n / cfg.cta_group / cfg.cluster_m, cfg.tile_k))
       return GEMM_ERR_CUDA;
   }
 
@@ -547,7 +538,7 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
 
   KernelParams kp{};
   kp.M = (int)M; kp.N = (int)N; kp.K = (int)K; kp.L = (int)L;
-  kp.tiles_m = (int)cdiv(M, cfg.tile_m);
+  kp.tiles_m = (int)cdiv(M, (int64_t)cfg.tile_m * cfg.cluster_m);
   kp.tiles_n = (int)cdiv(N, cfg.tile_n);
   kp.num_tiles = (int)cfg.tiles;
   kp.k_blocks = (int)cdiv(K, cfg.tile_k);

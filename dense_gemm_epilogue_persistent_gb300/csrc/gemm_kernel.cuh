@@ -27,9 +27,17 @@
 //               chunks ahead (across tile boundaries, so the next tile's C/X arrive
 //               during its main loop); each thread reads its row, computes in fp32,
 //               writes D and Y back into the slot, and one thread TMA-stores them.
-// Every CTA (pair) walks the same static persistent tile sequence
+// Every cluster walks the same static persistent tile sequence
 // t = cluster_id, cluster_id + num_clusters, ...; with two accumulator stages the
 // epilogue of tile i overlaps the main loop of tile i+1.
+//
+// Clusters: CG*MC CTAs = MC CTA groups (pairs when CG = 2) stacked along M.  The
+// groups of a cluster compute MC vertically adjacent tiles that share the same B
+// columns, so each CTA loads only 1/MC of its B slice and TMA-multicasts it to
+// the matching CTA of every group (the multicast pattern of
+// "04_mma_tma_2sm_sm100.cu", "TMA Setup": B is multicast along cluster M).  A
+// ring slot may then be refilled only after every group's MMA has drained it,
+// so MMA completion is multicast to all CTAs of the cluster.
 //
 // Every barrier wait is bounded (watchdog): on expiry the kernel records a code
 // in a device status word, raises a CTA-wide abort flag, lets in-flight copies
@@ -59,7 +67,7 @@ struct EpiParams {
 
 struct KernelParams {
   int M, N, K, L;
-  int tiles_m, tiles_n;      // tiles per batch along M (of 128*cta_group rows) and N
+  int tiles_m, tiles_n;      // tiles per batch along M (of 128*cta_group*MC rows) and N
   int num_tiles;             // tiles_m * tiles_n * L
   int k_blocks;              // ceil(K / tile_k)
   int group_m;               // rasterisation strip height (tiles)
@@ -78,7 +86,7 @@ constexpr int kEpiChunk = 32;          // columns per epilogue chunk
 constexpr int kEpiLeader = 64;         // thread that issues the epilogue's TMA
 constexpr uint32_t kEpiBarrier = 1;    // named barrier of the 128 epilogue threads
 
-template <int CG, int BN, int AB_BYTES>
+template <int CG, int BN, int AB_BYTES, int MC>
 struct Geometry {
   static constexpr int BM = 128;                 // A rows staged per CTA
   static constexpr int BK = 128 / AB_BYTES;      // K per ring stage: one 128-byte row
@@ -90,6 +98,9 @@ struct Geometry {
   static constexpr int ATOM_MN = 128 / AB_BYTES; // MN extent of one MN-major swizzle atom
   static constexpr int ATOM_BYTES = BK * 128;    // bytes of one MN-major atom column
   static constexpr int CHUNKS = BN / kEpiChunk;  // epilogue chunks per tile
+  static constexpr int CLUSTER = CG * MC;        // CTAs per cluster
+  static constexpr int CM = BM * CG * MC;        // output rows per cluster tile
+  static constexpr int BN_PART = BN_CTA / MC;    // B rows each CTA loads (and multicasts)
   static_assert(BN % kEpiChunk == 0 && BN <= 256, "tile_n");
   static_assert(kAccStages * BN <= (int)kTmemCols, "accumulators must fit tensor memory");
 };
@@ -226,7 +237,7 @@ __device__ __forceinline__ uint32_t sub_bytes(int dt) {
 
 // ------------------------------------------------------------------ the kernel
 
-template <int CG, int BN, int AB_BYTES>
+template <int CG, int BN, int AB_BYTES, int MC>
 __global__ void __launch_bounds__(kThreads, 1)
 persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
@@ -235,8 +246,9 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmD,
                        const __grid_constant__ CUtensorMap tmY,
                        const __grid_constant__ KernelParams p) {
-  using G = Geometry<CG, BN, AB_BYTES>;
+  using G = Geometry<CG, BN, AB_BYTES, MC>;
   constexpr int KIND = (AB_BYTES == 1) ? 1 : 0;
+  constexpr bool MULTI = G::CLUSTER > 1;
 
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzle atoms (identical in both CTAs of a pair:
@@ -247,9 +259,18 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
-  const int cluster_id = blockIdx.x / CG;
-  const int num_clusters = gridDim.x / CG;
+  const uint32_t crank = MULTI ? cluster_ctarank() : 0u;
+  const uint32_t rank = crank % CG;               // CTA within its pair
+  const uint32_t grp = crank / CG;                // pair (group) within the cluster
+  const uint32_t leader = grp * CG;               // cluster rank of the pair's leader
+  const int cluster_id = blockIdx.x / G::CLUSTER;
+  const int num_clusters = gridDim.x / G::CLUSTER;
+  // CTAs receiving this CTA's B part: the same peer position in every group.
+  uint16_t b_mask = 0;
+#pragma unroll
+  for (int g = 0; g < MC; ++g) b_mask |= (uint16_t)(1u << (g * CG + rank));
+  const uint16_t all_mask = (uint16_t)((1u << G::CLUSTER) - 1u);
+  const uint16_t pair_mask = (uint16_t)(((1u << CG) - 1u) << leader);
   const int S = p.stages;
   const EpiParams& e = p.epi;
   const int E = e.slots;
@@ -271,7 +292,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8u * s, 1);
-      mbar_init(empty0 + 8u * s, 1);
+      mbar_init(empty0 + 8u * s, MC);          // one MMA commit per group
     }
     for (int a = 0; a < kAccStages; ++a) {
       mbar_init(tfull0 + 8u * a, 1);
@@ -287,7 +308,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   }
   tc_fence_before_sync();
   __syncthreads();
-  if constexpr (CG == 2) cluster_sync_all();
+  if constexpr (MULTI) cluster_sync_all();
   tc_fence_after_sync();
   const uint32_t tmem_base = *holder_ptr;
 
@@ -305,19 +326,24 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
         int tm, tn, tl;
         tile_coords(t, p, tm, tn, tl);
-        const int m0 = tm * (G::BM * CG) + (int)rank * G::BM;
-        const int n0 = tn * BN + (int)rank * G::BN_CTA;
+        const int m0 = tm * G::CM + (int)grp * (G::BM * CG) + (int)rank * G::BM;
+        const int n0 = tn * BN + (int)rank * G::BN_CTA + (int)grp * G::BN_PART;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!wait_phase(empty0 + 8u * s, ph ^ 1u, w, kWaitProducer)) { ok = false; break; }
           const uint32_t fb = full0 + 8u * s;
           if (rank == 0) mbar_arrive_expect_tx(fb, tx_bytes);
-          const uint32_t fb_target = (CG == 2) ? map_to_rank(fb, 0) : fb;
+          const uint32_t fb_target = (CG == 2) ? map_to_rank(fb, leader) : fb;
           const int k0 = kb * G::BK;
           const uint32_t sa = a_ring + s * G::A_STAGE;
           const uint32_t sb = b_ring + s * G::B_STAGE;
           auto issue = [&](const CUtensorMap* map, uint32_t dst, int c0, int c1) {
             if constexpr (CG == 1) tma_load_3d(dst, map, fb_target, c0, c1, tl);
             else tma_load_3d_pair(dst, map, fb_target, c0, c1, tl);
+          };
+          auto issue_b = [&](uint32_t dst, int c0, int c1) {
+            if constexpr (MC == 1) issue(&tmB, dst, c0, c1);
+            else if constexpr (CG == 1) tma_load_3d_mc(dst, &tmB, fb_target, c0, c1, tl, b_mask);
+            else tma_load_3d_pair_mc(dst, &tmB, fb_target, c0, c1, tl, b_mask);
           };
           if (!p.a_mn_major) {
             issue(&tmA, sa, k0, m0);                           // box {BK, 128}
@@ -327,11 +353,12 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
               issue(&tmA, sa + j * G::ATOM_BYTES, m0 + j * G::ATOM_MN, k0);
           }
           if (!p.b_mn_major) {
-            issue(&tmB, sb, k0, n0);                           // box {BK, BN_CTA}
+            issue_b(sb + grp * G::BN_PART * 128, k0, n0);      // box {BK, BN_PART}
           } else {
+            constexpr int ATOMS = G::BN_PART / G::ATOM_MN;     // boxes {ATOM_MN, BK}
 #pragma unroll
-            for (int j = 0; j < G::BN_CTA / G::ATOM_MN; ++j)
-              issue(&tmB, sb + j * G::ATOM_BYTES, n0 + j * G::ATOM_MN, k0);
+            for (int j = 0; j < ATOMS; ++j)
+              issue_b(sb + (grp * ATOMS + j) * G::ATOM_BYTES, n0 + j * G::ATOM_MN, k0);
           }
           if (++s == S) { s = 0; ph ^= 1u; }
         }
@@ -366,11 +393,11 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                 : smem_desc_sw128(sb + k * 32, 16, 1024);
             umma<CG, KIND>(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
           }
-          umma_commit<CG>(empty0 + 8u * s, (uint16_t)0x3);     // frees the slot in both CTAs
+          umma_commit<CG, MULTI>(empty0 + 8u * s, all_mask);   // slot drained: tell every loader
           if (++s == S) { s = 0; ph ^= 1u; }
         }
         if (!ok) break;
-        umma_commit<CG>(tfull0 + 8u * acc, (uint16_t)0x3);     // accumulator ready
+        umma_commit<CG, (CG == 2)>(tfull0 + 8u * acc, pair_mask);   // accumulator ready
         if (++acc == kAccStages) { acc = 0; aph ^= 1u; }
       }
     }
@@ -392,7 +419,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       if (t >= p.num_tiles) return false;
       int tm, tn;
       tile_coords(t, p, tm, tn, tl);
-      row0 = tm * (G::BM * CG) + (int)rank * G::BM;
+      row0 = tm * G::CM + (int)grp * (G::BM * CG) + (int)rank * G::BM;
       col0 = tn * BN + (c - ord * G::CHUNKS) * kEpiChunk;
       return true;
     };
@@ -427,7 +454,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       ok = named_barrier_and(kEpiBarrier, 128, wait_phase(tfull0 + 8u * acc, aph, w, kWaitEpilogue));
       if (!ok) break;
       tc_fence_after_sync();
-      const int row0 = tm * (G::BM * CG) + (int)rank * G::BM;
+      const int row0 = tm * G::CM + (int)grp * (G::BM * CG) + (int)rank * G::BM;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll 1
       for (int j = 0; j < G::CHUNKS; ++j, ++gc) {
@@ -440,7 +467,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           __syncwarp();
           if (lane == 0) {
             if constexpr (CG == 1) mbar_arrive(tempty0 + 8u * acc);
-            else mbar_arrive_cluster(map_to_rank(tempty0 + 8u * acc, 0));
+            else mbar_arrive_cluster(map_to_rank(tempty0 + 8u * acc, leader));
           }
         }
         const int slot_idx = gc % E;
@@ -495,7 +522,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     while (globaltimer_ns() - t0 < 2000000ull) {
     }
   }
-  if constexpr (CG == 2) cluster_sync_all();   // the peer may still use our smem/TMEM
+  if constexpr (MULTI) cluster_sync_all();    // other CTAs may still use our smem/TMEM
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc<CG>(tmem_base, kTmemCols);

@@ -127,6 +127,32 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// Multicast variants: the box lands at the same shared-memory offset in every
+// CTA of `cta_mask`, and each destination's barrier at the offset of `bar`
+// receives the completion.  With cta_group::2 the completion goes to the
+// barrier in the even (leader) CTA of each destination's pair.
+__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                               int32_t c0, int32_t c1, int32_t c2,
+                                               uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%3, %4, %5}], [%2], %6;"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2),
+         "h"(cta_mask)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair_mc(uint32_t dst, const CUtensorMap* map,
+                                                    uint32_t cluster_bar, int32_t c0, int32_t c1,
+                                                    int32_t c2, uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster.cta_group::2 [%0], [%1, {%3, %4, %5}], [%2], %6;"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(c0), "r"(c1),
+         "r"(c2), "h"(cta_mask)
+      : "memory");
+}
+
 // 3-D tiled TMA store from this CTA's shared memory (bulk-group completion).
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int32_t c0,
                                              int32_t c1, int32_t c2) {
@@ -218,13 +244,17 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a_desc, uint64_t 
 }
 
 // Arrive (once) on `bar` when every tcgen05.mma this thread issued so far has
-// completed.  For a CTA pair the arrival goes to the barrier at the same
-// offset in every CTA of `cta_mask`.
-template <int CG>
+// completed.  MULTI: the arrival goes to the barrier at the same offset in
+// every CTA of `cta_mask`; otherwise to this CTA's barrier only.
+template <int CG, bool MULTI>
 __device__ __forceinline__ void umma_commit(uint32_t bar, uint16_t cta_mask) {
-  if constexpr (CG == 1)
+  if constexpr (CG == 1 && !MULTI)
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                  :: "r"(bar) : "memory");
+  else if constexpr (CG == 1)
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" :: "r"(bar), "h"(cta_mask) : "memory");
   else
     asm volatile(
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"

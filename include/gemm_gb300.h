@@ -78,8 +78,11 @@ typedef struct {
  *   stages      depth of the shared-memory A/B ring (0 = as deep as fits).
  *   group_m     tile rasterisation: tiles are walked in column strips
  *               group_m tiles high (0 = automatic).
+ *   cluster_m   CTA groups per thread-block cluster, stacked along M, that share
+ *               their B tile through TMA multicast: 1 or 2 (0 = automatic).  The
+ *               cluster holds cta_group * cluster_m CTAs.
  * Filled in by gemm_plan / reported by gemm_last_config:
- *   tile_m      128 * cta_group.
+ *   tile_m      128 * cta_group (rows of one CTA group's tile).
  *   tile_k      K elements per ring stage (64 for 16-bit, 128 for 8-bit inputs).
  *   acc_stages  tensor-memory accumulator stages (2: double buffered).
  *   ring_bytes  ring bytes per CTA: stages*(A stage + B stage) + 8 bytes per
@@ -99,6 +102,7 @@ typedef struct {
   int64_t tiles;
   int grid_ctas;
   int epi_slots, epi_slot_bytes;
+  int cluster_m;
 } gemm_config_t;
 
 /* Every argument of one gemm_run call, for the host-only planning calls. */

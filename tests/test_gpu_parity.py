@@ -17,7 +17,10 @@ from gemm_cases import (Case, compare_full, compare_sampled, logical, prepare, r
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = [(1, 128), (1, 256), (2, 128), (2, 256)]
+# (cta_group, tile_n, cluster_m): single CTAs and CTA pairs, 128- and
+# 256-wide tiles, without and with B shared by TMA multicast across the cluster.
+VARIANTS = [(1, 128, 1), (1, 256, 1), (2, 128, 1), (2, 256, 1),
+            (1, 128, 2), (1, 256, 2), (2, 128, 2), (2, 256, 2)]
 
 
 @pytest.fixture(scope="module")
@@ -29,8 +32,8 @@ def gemm():
     g.close()
 
 
-def _force(gemm, cg, bn, stages=0):
-    gemm.set_config(cta_group=cg, tile_n=bn, stages=stages)
+def _force(gemm, cg, bn, mc=1, stages=0):
+    gemm.set_config(cta_group=cg, tile_n=bn, cluster_m=mc, stages=stages)
 
 
 def _finish(gemm):
@@ -92,9 +95,9 @@ SMALL = {
 def test_small_workloads(gemm, name, variant):
     case = SMALL[name]
     if variant:
-        cg, bn = variant
-        # MN-major operands are staged in 128-byte atoms per CTA
-        if case.b_mn and (bn // cg) % (128 // W.ELEM_BYTES[case.ab]) != 0:
+        cg, bn, mc = variant
+        # MN-major operands are staged (and multicast) in 128-byte atoms
+        if case.b_mn and (bn // cg // mc) % (128 // W.ELEM_BYTES[case.ab]) != 0:
             pytest.skip("variant cannot stage this MN-major B")
         _force(gemm, *variant)
     else:
