@@ -364,6 +364,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         }
       }
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (rank == 0 && lane == 0) {
@@ -451,7 +452,9 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
       int tm, tn, tl;
       tile_coords(t, p, tm, tn, tl);
-      ok = named_barrier_and(kEpiBarrier, 128, wait_phase(tfull0 + 8u * acc, aph, w, kWaitEpilogue));
+      const bool ready = wait_phase(tfull0 + 8u * acc, aph, w, kWaitEpilogue);
+      __syncwarp();
+      ok = named_barrier_and(kEpiBarrier, 128, ready);
       if (!ok) break;
       tc_fence_after_sync();
       const int row0 = tm * G::CM + (int)grp * (G::BM * CG) + (int)rank * G::BM;
@@ -469,6 +472,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             if constexpr (CG == 1) mbar_arrive(tempty0 + 8u * acc);
             else mbar_arrive_cluster(map_to_rank(tempty0 + 8u * acc, leader));
           }
+          __syncwarp();
         }
         const int slot_idx = gc % E;
         uint8_t* const slot = gbase + (epi0 - base) + (uint32_t)slot_idx * slot_bytes;
@@ -479,6 +483,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         if (got && e.read_x) smem_read_row(slot + e.cd_bytes, e.x_dt, e.cd_m_major, r, xv);
         // Every thread has read the slot (and agrees whether to go on) before any
         // thread overwrites it with D and Y.
+        __syncwarp();
         ok = named_barrier_and(kEpiBarrier, 128, got);
         if (!ok) break;
         float dv[kEpiChunk], yv[kEpiChunk];
@@ -507,10 +512,12 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           bulk_wait_group_read<1>();
           if (loads) issue_loads(gc + E - 1);
         }
+        __syncwarp();                       // the leader's warp reconverges
       }
       if (++acc == kAccStages) { acc = 0; aph ^= 1u; }
     }
     if (leader) bulk_wait_group_all();
+    __syncwarp();
   }
 
   // ------------------------------------------------------------ teardown
@@ -522,6 +529,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     while (globaltimer_ns() - t0 < 2000000ull) {
     }
   }
+  __syncwarp();
   if constexpr (MULTI) cluster_sync_all();    // other CTAs may still use our smem/TMEM
   if (warp == 1) {
     tc_fence_after_sync();

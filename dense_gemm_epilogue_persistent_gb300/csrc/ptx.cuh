@@ -40,9 +40,11 @@ __device__ __forceinline__ void cluster_sync_all() {
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Named barrier among `count` threads (multiple of 32).
+// Named barrier among `count` threads (multiple of 32).  The non-.aligned
+// form counts arriving threads, so it stays correct even if a warp reaches it
+// diverged (callers also reconverge with __syncwarp first).
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) {
-  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
+  asm volatile("barrier.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
 }
 
 // Named barrier that also ANDs a predicate over the `count` participating
@@ -52,7 +54,7 @@ __device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t count, b
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "barrier.red.and.pred q, %2, %3, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(out) : "r"((uint32_t)pred), "r"(id), "r"(count) : "memory");
   return out != 0;
