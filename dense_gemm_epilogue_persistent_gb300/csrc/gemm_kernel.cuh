@@ -262,7 +262,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   const uint32_t crank = MULTI ? cluster_ctarank() : 0u;
   const uint32_t rank = crank % CG;               // CTA within its pair
   const uint32_t grp = crank / CG;                // pair (group) within the cluster
-  const uint32_t leader = grp * CG;               // cluster rank of the pair's leader
+  const uint32_t pair_leader = grp * CG;          // cluster rank of the pair's leader
   const int cluster_id = blockIdx.x / G::CLUSTER;
   const int num_clusters = gridDim.x / G::CLUSTER;
   // CTAs receiving this CTA's B part: the same peer position in every group.
@@ -270,7 +270,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
   for (int g = 0; g < MC; ++g) b_mask |= (uint16_t)(1u << (g * CG + rank));
   const uint16_t all_mask = (uint16_t)((1u << G::CLUSTER) - 1u);
-  const uint16_t pair_mask = (uint16_t)(((1u << CG) - 1u) << leader);
+  const uint16_t pair_mask = (uint16_t)(((1u << CG) - 1u) << pair_leader);
   const int S = p.stages;
   const EpiParams& e = p.epi;
   const int E = e.slots;
@@ -332,7 +332,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           if (!wait_phase(empty0 + 8u * s, ph ^ 1u, w, kWaitProducer)) { ok = false; break; }
           const uint32_t fb = full0 + 8u * s;
           if (rank == 0) mbar_arrive_expect_tx(fb, tx_bytes);
-          const uint32_t fb_target = (CG == 2) ? map_to_rank(fb, leader) : fb;
+          const uint32_t fb_target = (CG == 2) ? map_to_rank(fb, pair_leader) : fb;
           const int k0 = kb * G::BK;
           const uint32_t sa = a_ring + s * G::A_STAGE;
           const uint32_t sb = b_ring + s * G::B_STAGE;
@@ -407,7 +407,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     // ---------------------------------------------------------- epilogue
     const int q = warp & 3;                 // TMEM lane quarter this warp may read
     const int r = q * 32 + lane;            // this thread's row within the CTA's 128
-    const bool leader = threadIdx.x == kEpiLeader;
+    const bool epi_leader = threadIdx.x == kEpiLeader;
     const bool loads = e.read_c || e.read_x;
     const uint32_t load_tx = (e.read_c ? sub_bytes(e.c_dt) : 0u) + (e.read_x ? sub_bytes(e.x_dt) : 0u);
 
@@ -424,7 +424,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       col0 = tn * BN + (c - ord * G::CHUNKS) * kEpiChunk;
       return true;
     };
-    auto issue_loads = [&](int c) {         // leader only
+    auto issue_loads = [&](int c) {         // epilogue leader only
       int row0, col0, tl;
       if (!chunk_origin(c, row0, col0, tl)) return;
       const uint32_t slot = epi0 + (uint32_t)(c % E) * slot_bytes;
@@ -435,7 +435,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       if (e.read_x) tma_load_3d(slot + e.cd_bytes, &tmX, bar, x0, x1, tl);
     };
 
-    if (leader) {
+    if (epi_leader) {
       prefetch_tensormap(&tmD);
       if (e.write_y) prefetch_tensormap(&tmY);
       if (loads) {
@@ -470,7 +470,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           __syncwarp();
           if (lane == 0) {
             if constexpr (CG == 1) mbar_arrive(tempty0 + 8u * acc);
-            else mbar_arrive_cluster(map_to_rank(tempty0 + 8u * acc, leader));
+            else mbar_arrive_cluster(map_to_rank(tempty0 + 8u * acc, pair_leader));
           }
           __syncwarp();
         }
@@ -499,7 +499,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         if (e.write_y) smem_write_row(slot + e.cd_bytes, e.y_dt, e.cd_m_major, r, yv);
         fence_proxy_async_smem();
         named_barrier_sync(kEpiBarrier, 128);
-        if (leader) {
+        if (epi_leader) {
           const int col0 = tn * BN + j * kEpiChunk;
           const int x0 = e.cd_m_major ? row0 : col0, x1 = e.cd_m_major ? col0 : row0;
           const uint32_t s_addr = epi0 + (uint32_t)slot_idx * slot_bytes;
@@ -516,7 +516,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       }
       if (++acc == kAccStages) { acc = 0; aph ^= 1u; }
     }
-    if (leader) bulk_wait_group_all();
+    if (epi_leader) bulk_wait_group_all();
     __syncwarp();
   }
 

@@ -72,6 +72,24 @@ def test_integer_exact_ragged_all_outputs(gemm, variant):
     gemm.set_config(None)
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_many_tiles_per_cluster(gemm, variant):
+    """Every persistent cluster walks several tiles (4096 x 4096 output), so
+    the accumulator double-buffering and the epilogue slot ring wrap around
+    many times; all outputs are compared with the oracle."""
+    _force(gemm, *variant)
+    case = Case(M=4096, N=4096, K=64, L=1, ab="f16", c="f16", d="f16", x="bf16", y="f16",
+                alpha=1.0, beta=0.5, xf=-1.0, seed=41)
+    prep = prepare(case)
+    D, Y = run_gpu(gemm, prep)
+    _finish(gemm)
+    cfg = gemm.last_config()
+    clusters = cfg.grid_ctas // (cfg.cta_group * cfg.cluster_m)
+    assert cfg.tiles >= 3 * clusters
+    compare_full(prep, D, Y)
+    gemm.set_config(None)
+
+
 # ------------------------------------------------------------ reduced-size workloads
 
 SMALL = {
