@@ -55,6 +55,7 @@ struct gemm_handle {
   gemm_config_t last{};
   uint64_t timeout_ns = kDefaultTimeoutNs;
   VariantState variants[2][2][2][2];   // [ab 16/8][cta_group 1/2][tile_n 128/256][mc 1/2]
+  int clusters_by_size[5] = {0, 0, 0, 0, 0};   // resident clusters of 1, 2, 4 CTAs
   std::mutex mu;
 };
 
@@ -175,18 +176,28 @@ bool variant_supports(const gemm_problem_t& p, int cg, int bn, int mc) {
 //   traffic, so L2->SM bandwidth, not the tensor pipe, sets their pace; a CTA
 //   pair halves the B traffic of each SM)
 //   fixed per tile (pipeline fill, epilogue tail): pair 17, single CTA 10.
-double plan_cost(int64_t tiles, int64_t k_blocks, int cg, int mc, int bn, int sm_count) {
-  const int64_t units = std::max(1, sm_count / (cg * mc));
-  const double waves = (double)cdiv(tiles, units);
+//   Two pairs sharing B through multicast (4-CTA cluster): 0.955 per pair-tile
+//   k-block, but fewer clusters fit the GPCs (36 of 38 on GB300), which the
+//   wave count sees through `clusters` (resident clusters of that size).
+double plan_cost(int64_t tiles, int64_t k_blocks, int cg, int mc, int bn, int64_t clusters) {
+  const double waves = (double)cdiv(tiles, std::max<int64_t>(1, clusters));
   double per_kb;
-  if (bn == 256) per_kb = cg == 2 ? 1.0 : 1.13;
+  if (bn == 256) per_kb = cg == 2 ? (mc == 2 ? 0.955 : 1.0) : 1.13;
   else per_kb = cg == 2 ? 1.3 : 0.93;
   const double fixed = cg == 2 ? 17.0 : 10.0;
   return waves * ((double)k_blocks * per_kb + fixed);
 }
 
+// Resident clusters of `csize` CTAs: the device's measured occupancy when
+// known (clusters_by_size[csize]), else SMs / csize.
+int64_t resident_clusters(int sm_count, const int* clusters_by_size, int csize) {
+  if (clusters_by_size && clusters_by_size[csize] > 0) return clusters_by_size[csize];
+  return std::max(1, sm_count / csize);
+}
+
 gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
-                   const gemm_config_t* forced, gemm_config_t* out) {
+                   const gemm_config_t* forced, gemm_config_t* out,
+                   const int* clusters_by_size = nullptr) {
   gemm_status_t st = validate(pp);
   if (st != GEMM_OK) return st;
   if (!out || sm_count <= 0 || smem_optin <= 0) return GEMM_ERR_INVALID_ARG;
@@ -202,12 +213,13 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
     for (int b : {256, 128})
       for (int m : {1, 2}) {
         if ((fcg && a != fcg) || (fbn && b != fbn)) continue;
-        // Multicast clusters are used only when asked for.
-        if (fmc ? m != fmc : m != 1) continue;
+        // Automatic choice: multicast only for CTA pairs with 256-wide tiles.
+        if (fmc ? m != fmc : (m == 2 && !(a == 2 && b == 256))) continue;
         if (!variant_supports(p, a, b, m)) continue;
         const int64_t tiles = cdiv(std::max<int64_t>(p.M, 1), 128 * a * m) *
                               cdiv(std::max<int64_t>(p.N, 1), b) * std::max<int64_t>(p.L, 1);
-        const double c = plan_cost(tiles, cdiv(p.K, 128 / ab_bytes), a, m, b, sm_count);
+        const double c = plan_cost(tiles, cdiv(p.K, 128 / ab_bytes), a, m, b,
+                                   resident_clusters(sm_count, clusters_by_size, a * m));
         if (c < best - 1e-9) { best = c; cg = a; bn = b; mc = m; }
       }
   if (!cg) return GEMM_ERR_UNSUPPORTED_CONFIG;
@@ -250,7 +262,7 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
   c.smem_bytes = std::max(total_smem(cg, bn, ab_bytes, stages, slots, slot),
                           smem_optin / 2 + 1024);
   c.tiles = tiles;
-  const int64_t units = std::max(1, sm_count / (cg * mc));
+  const int64_t units = resident_clusters(sm_count, clusters_by_size, cg * mc);
   c.grid_ctas = (int)(std::min<int64_t>(tiles, units) * cg * mc);
   *out = c;
   return GEMM_OK;
@@ -403,7 +415,37 @@ GEMM_API gemm_status_t gemm_create(gemm_handle_t* out, int device) {
     cudaGetLastError();
     return GEMM_ERR_CUDA;
   }
+  // Resident clusters of 1, 2 and 4 CTAs at one CTA per SM (every
+  // configuration uses more than half of the shared memory), from the
+  // occupancy calculator on a representative kernel.
+  int clusters[5] = {0, 0, 0, 0, 0};
+  {
+    const void* kern = gb300::kernel_for(2, 2, 256, 2);
+    const int smem = optin / 2 + 1024;
+    if (cudaSetDevice(device) == cudaSuccess &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
+            cudaSuccess) {
+      for (int cs : {1, 2, 4}) {
+        cudaLaunchConfig_t lc{};
+        cudaLaunchAttribute attr[1];
+        lc.gridDim = dim3((unsigned)(cs * sms));
+        lc.blockDim = dim3(gb300::kThreads);
+        lc.dynamicSmemBytes = (size_t)smem;
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)cs;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        lc.attrs = attr;
+        lc.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &lc) == cudaSuccess) clusters[cs] = n;
+      }
+    }
+    cudaGetLastError();
+    cudaSetDevice(prev);
+  }
   gemm_handle* h = new gemm_handle();
+  for (int i = 0; i < 5; ++i) h->clusters_by_size[i] = clusters[i];
   h->device = device;
   h->sm_count = sms;
   h->smem_optin = optin;
@@ -473,7 +515,8 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
 
   std::lock_guard<std::mutex> guard(h->mu);
   gemm_config_t cfg{};
-  st = plan(&p, h->sm_count, h->smem_optin, h->forced ? &h->forced_cfg : nullptr, &cfg);
+  st = plan(&p, h->sm_count, h->smem_optin, h->forced ? &h->forced_cfg : nullptr, &cfg,
+            h->clusters_by_size);
   if (st != GEMM_OK) return st;
 
   const int ab_bytes = dtype_bytes(dtypes->ab);
