@@ -169,8 +169,10 @@ def test_plan_every_workload(lib, name):
     assert cfg.cta_group in (1, 2) and cfg.tile_n in (128, 256)
     assert cfg.tile_k == (128 if w.ab == "e4m3" else 64)
     assert 2 <= cfg.stages and cfg.smem_bytes <= 232448
-    assert cfg.tiles == (-(-w.M // cfg.tile_m)) * (-(-w.N // cfg.tile_n)) * w.L
-    assert cfg.grid_ctas % cfg.cta_group == 0 and cfg.grid_ctas <= 152
+    rows = cfg.tile_m * cfg.cluster_m                  # output rows per cluster tile
+    assert cfg.tiles == (-(-w.M // rows)) * (-(-w.N // cfg.tile_n)) * w.L
+    assert cfg.cluster_m in (1, 2)
+    assert cfg.grid_ctas % (cfg.cta_group * cfg.cluster_m) == 0 and cfg.grid_ctas <= 152
     assert 2 * G.gemm_tmem_columns(128, cfg.tile_n) <= 512
 
 
