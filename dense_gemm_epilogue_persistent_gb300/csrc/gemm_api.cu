@@ -35,6 +35,10 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 
 constexpr uint64_t kDefaultTimeoutNs = 4000000000ull;
 constexpr int kMaxStages = 12;
+constexpr int kMaxEpiSlots = 4;
+// Default L2 priorities: A/B evict-normal, C/X loads and D/Y stores
+// evict-first (streamed once; they should not displace A/B blocks).
+constexpr int kDefaultL2Hints = 0 | (2 << 2) | (2 << 4);
 constexpr int kSmemSlack = 1024 + 16;   // base alignment + abort flag
 
 struct VariantState {
@@ -234,7 +238,8 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
     while (n < kMaxStages && total_smem(cg, bn, ab_bytes, n + 1, slots, slot) <= smem_optin) ++n;
     return n;
   };
-  int slots = max_stages_for(3) >= 4 ? 3 : 2;
+  int slots = forced && forced->epi_slots ? forced->epi_slots : (max_stages_for(3) >= 4 ? 3 : 2);
+  if (slots < 2 || slots > kMaxEpiSlots) return GEMM_ERR_UNSUPPORTED_CONFIG;
   const int max_stages = max_stages_for(slots);
   int stages = forced && forced->stages ? forced->stages : max_stages;
   if (stages < 2 || stages > max_stages) return GEMM_ERR_UNSUPPORTED_CONFIG;
@@ -252,6 +257,7 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
   c.group_m = group_m;
   c.tile_m = 128 * cg;
   c.cluster_m = mc;
+  c.l2_hints = forced && (forced->l2_hints & 0x100) ? (forced->l2_hints & 0x3F) : kDefaultL2Hints;
   c.tile_k = 128 / ab_bytes;
   c.acc_stages = gb300::kAccStages;
   c.ring_bytes = ring_bytes(cg, bn, ab_bytes, stages);
@@ -476,6 +482,7 @@ GEMM_API gemm_status_t gemm_set_config(gemm_handle_t h, const gemm_config_t* cfg
   if ((cfg->cta_group && cfg->cta_group != 1 && cfg->cta_group != 2) ||
       (cfg->tile_n && cfg->tile_n != 128 && cfg->tile_n != 256) || cfg->stages < 0 ||
       (cfg->cluster_m && cfg->cluster_m != 1 && cfg->cluster_m != 2) ||
+      cfg->epi_slots < 0 || cfg->epi_slots > kMaxEpiSlots ||
       cfg->stages > kMaxStages || cfg->group_m < 0)
     return GEMM_ERR_INVALID_ARG;
   h->forced = true;
@@ -590,6 +597,7 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
   kp.a_mn_major = a_mn;
   kp.b_mn_major = b_mn;
   kp.idesc = make_idesc(dtypes->ab, cfg.cta_group, cfg.tile_n, a_mn, b_mn);
+  kp.l2_hints = (uint32_t)cfg.l2_hints;
   kp.status = h->d_status;
   kp.timeout_ns = h->timeout_ns;
   kp.epi.c_dt = dtypes->c;

@@ -74,6 +74,8 @@ struct KernelParams {
   int stages;                // A/B ring depth
   int a_mn_major, b_mn_major;
   uint32_t idesc;            // tcgen05 instruction descriptor
+  uint32_t l2_hints;         // L2 eviction priority (0 normal, 1 last, 2 first):
+                             //   bits 0-1 A/B loads, 2-3 C/X loads, 4-5 D/Y stores
   uint32_t* status;          // device status word (watchdog)
   unsigned long long timeout_ns;
   EpiParams epi;
@@ -319,6 +321,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     if (lane == 0) {
       prefetch_tensormap(&tmA);
       prefetch_tensormap(&tmB);
+      const uint64_t pol = make_l2_policy(p.l2_hints & 3u);
       const uint32_t tx_bytes = (uint32_t)(CG * (G::A_STAGE + G::B_STAGE));
       int s = 0;
       uint32_t ph = 0;
@@ -337,13 +340,14 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           const uint32_t sa = a_ring + s * G::A_STAGE;
           const uint32_t sb = b_ring + s * G::B_STAGE;
           auto issue = [&](const CUtensorMap* map, uint32_t dst, int c0, int c1) {
-            if constexpr (CG == 1) tma_load_3d(dst, map, fb_target, c0, c1, tl);
-            else tma_load_3d_pair(dst, map, fb_target, c0, c1, tl);
+            if constexpr (CG == 1) tma_load_3d(dst, map, fb_target, c0, c1, tl, pol);
+            else tma_load_3d_pair(dst, map, fb_target, c0, c1, tl, pol);
           };
           auto issue_b = [&](uint32_t dst, int c0, int c1) {
             if constexpr (MC == 1) issue(&tmB, dst, c0, c1);
-            else if constexpr (CG == 1) tma_load_3d_mc(dst, &tmB, fb_target, c0, c1, tl, b_mask);
-            else tma_load_3d_pair_mc(dst, &tmB, fb_target, c0, c1, tl, b_mask);
+            else if constexpr (CG == 1)
+              tma_load_3d_mc(dst, &tmB, fb_target, c0, c1, tl, b_mask, pol);
+            else tma_load_3d_pair_mc(dst, &tmB, fb_target, c0, c1, tl, b_mask, pol);
           };
           if (!p.a_mn_major) {
             issue(&tmA, sa, k0, m0);                           // box {BK, 128}
@@ -410,6 +414,8 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     const bool epi_leader = threadIdx.x == kEpiLeader;
     const bool loads = e.read_c || e.read_x;
     const uint32_t load_tx = (e.read_c ? sub_bytes(e.c_dt) : 0u) + (e.read_x ? sub_bytes(e.x_dt) : 0u);
+    const uint64_t pol_in = make_l2_policy((p.l2_hints >> 2) & 3u);
+    const uint64_t pol_out = make_l2_policy((p.l2_hints >> 4) & 3u);
 
     // Epilogue chunk c of this CTA's stream: tile ordinal c / CHUNKS, columns
     // 32*(c % CHUNKS).. of that tile.  TMA coordinates are (column, row, batch)
@@ -431,8 +437,8 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       const uint32_t bar = cfull0 + 8u * (uint32_t)(c % E);
       const int x0 = e.cd_m_major ? row0 : col0, x1 = e.cd_m_major ? col0 : row0;
       mbar_arrive_expect_tx(bar, load_tx);
-      if (e.read_c) tma_load_3d(slot, &tmC, bar, x0, x1, tl);
-      if (e.read_x) tma_load_3d(slot + e.cd_bytes, &tmX, bar, x0, x1, tl);
+      if (e.read_c) tma_load_3d(slot, &tmC, bar, x0, x1, tl, pol_in);
+      if (e.read_x) tma_load_3d(slot + e.cd_bytes, &tmX, bar, x0, x1, tl, pol_in);
     };
 
     if (epi_leader) {
@@ -503,8 +509,8 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           const int col0 = tn * BN + j * kEpiChunk;
           const int x0 = e.cd_m_major ? row0 : col0, x1 = e.cd_m_major ? col0 : row0;
           const uint32_t s_addr = epi0 + (uint32_t)slot_idx * slot_bytes;
-          tma_store_3d(&tmD, s_addr, x0, x1, tl);
-          if (e.write_y) tma_store_3d(&tmY, s_addr + e.cd_bytes, x0, x1, tl);
+          tma_store_3d(&tmD, s_addr, x0, x1, tl, pol_out);
+          if (e.write_y) tma_store_3d(&tmY, s_addr + e.cd_bytes, x0, x1, tl, pol_out);
           bulk_commit_group();
           // The slot of chunk gc+1 (and, with loads, of chunk gc+E-1, i.e. the
           // slot of chunk gc-1) is free once at most one store group -- this

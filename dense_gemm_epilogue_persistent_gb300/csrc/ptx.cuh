@@ -105,14 +105,28 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// L2 eviction-priority policy for the cache_hint operand of TMA copies:
+// 0 = evict_normal, 1 = evict_last, 2 = evict_first.
+__device__ __forceinline__ uint64_t make_l2_policy(uint32_t kind) {
+  uint64_t pol;
+  if (kind == 1)
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  else if (kind == 2)
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  else
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 // 3-D tiled TMA load into this CTA's shared memory; completion (bytes) is
 // signalled on barrier `bar` of this CTA.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int32_t c0, int32_t c1, int32_t c2) {
+                                            int32_t c0, int32_t c1, int32_t c2, uint64_t pol) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];"
-      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2),
+         "l"(pol)
       : "memory");
 }
 
@@ -120,12 +134,12 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
 // completion is signalled on `cluster_bar`, which may be the peer's barrier.
 __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map,
                                                  uint32_t cluster_bar, int32_t c0, int32_t c1,
-                                                 int32_t c2) {
+                                                 int32_t c2, uint64_t pol) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
-      " [%0], [%1, {%3, %4, %5}], [%2];"
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".cta_group::2.L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;"
       :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(c0), "r"(c1),
-         "r"(c2)
+         "r"(c2), "l"(pol)
       : "memory");
 }
 
@@ -135,32 +149,33 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
 // barrier in the even (leader) CTA of each destination's pair.
 __device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                                int32_t c0, int32_t c1, int32_t c2,
-                                               uint16_t cta_mask) {
+                                               uint16_t cta_mask, uint64_t pol) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4, %5}], [%2], %6;"
+      ".multicast::cluster.L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6, %7;"
       :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2),
-         "h"(cta_mask)
+         "h"(cta_mask), "l"(pol)
       : "memory");
 }
 
 __device__ __forceinline__ void tma_load_3d_pair_mc(uint32_t dst, const CUtensorMap* map,
                                                     uint32_t cluster_bar, int32_t c0, int32_t c1,
-                                                    int32_t c2, uint16_t cta_mask) {
+                                                    int32_t c2, uint16_t cta_mask, uint64_t pol) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster.cta_group::2 [%0], [%1, {%3, %4, %5}], [%2], %6;"
+      ".multicast::cluster.cta_group::2.L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6, %7;"
       :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(c0), "r"(c1),
-         "r"(c2), "h"(cta_mask)
+         "r"(c2), "h"(cta_mask), "l"(pol)
       : "memory");
 }
 
 // 3-D tiled TMA store from this CTA's shared memory (bulk-group completion).
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int32_t c0,
-                                             int32_t c1, int32_t c2) {
+                                             int32_t c1, int32_t c2, uint64_t pol) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
-      :: "l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(c0), "r"(c1), "r"(c2)
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group.L2::cache_hint"
+      " [%0, {%2, %3, %4}], [%1], %5;"
+      :: "l"(reinterpret_cast<uint64_t>(map)), "r"(src), "r"(c0), "r"(c1), "r"(c2), "l"(pol)
       : "memory");
 }
 

@@ -81,6 +81,11 @@ typedef struct {
  *   cluster_m   CTA groups per thread-block cluster, stacked along M, that share
  *               their B tile through TMA multicast: 1 or 2 (0 = automatic).  The
  *               cluster holds cta_group * cluster_m CTAs.
+ *   epi_slots   (also an input) epilogue slots, 2..4 (0 = automatic).
+ *   l2_hints    (also an input) L2 eviction priority of the TMA copies, 2 bits
+ *               each (0 normal, 1 evict-last, 2 evict-first): bits 0-1 A/B
+ *               loads, 2-3 C/X loads, 4-5 D/Y stores.  As an input it applies
+ *               only with bit 8 set (0 = automatic).
  * Filled in by gemm_plan / reported by gemm_last_config:
  *   tile_m      128 * cta_group (rows of one CTA group's tile).
  *   tile_k      K elements per ring stage (64 for 16-bit, 128 for 8-bit inputs).
@@ -103,6 +108,7 @@ typedef struct {
   int grid_ctas;
   int epi_slots, epi_slot_bytes;
   int cluster_m;
+  int l2_hints;
 } gemm_config_t;
 
 /* Every argument of one gemm_run call, for the host-only planning calls. */
