@@ -74,6 +74,7 @@ struct KernelParams {
   int stages;                // A/B ring depth
   int a_mn_major, b_mn_major;
   uint32_t idesc;            // tcgen05 instruction descriptor
+  int prefetch;              // L2 prefetch distance of the A/B stream, in k-blocks (0: off)
   uint32_t l2_hints;         // L2 eviction priority (0 normal, 1 last, 2 first):
                              //   bits 0-1 A/B loads, 2-3 C/X loads, 4-5 D/Y stores
   uint32_t* status;          // device status word (watchdog)
@@ -355,6 +356,25 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
             for (int j = 0; j < G::BM / G::ATOM_MN; ++j)       // boxes {ATOM_MN, BK}
               issue(&tmA, sa + j * G::ATOM_BYTES, m0 + j * G::ATOM_MN, k0);
+          }
+          // Warm L2 `prefetch` k-blocks ahead with the same boxes, so the ring's
+          // loads hit in L2 instead of waiting a DRAM round trip.
+          if (p.prefetch > 0 && kb + p.prefetch < p.k_blocks) {
+            const int kp = (kb + p.prefetch) * G::BK;
+            if (!p.a_mn_major) {
+              tma_prefetch_3d(&tmA, kp, m0, tl);
+            } else {
+#pragma unroll
+              for (int j = 0; j < G::BM / G::ATOM_MN; ++j)
+                tma_prefetch_3d(&tmA, m0 + j * G::ATOM_MN, kp, tl);
+            }
+            if (!p.b_mn_major) {
+              tma_prefetch_3d(&tmB, kp, n0, tl);
+            } else {
+#pragma unroll
+              for (int j = 0; j < G::BN_PART / G::ATOM_MN; ++j)
+                tma_prefetch_3d(&tmB, n0 + j * G::ATOM_MN, kp, tl);
+            }
           }
           if (!p.b_mn_major) {
             issue_b(sb + grp * G::BN_PART * 128, k0, n0);      // box {BK, BN_PART}

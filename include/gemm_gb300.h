@@ -86,6 +86,8 @@ typedef struct {
  *               each (0 normal, 1 evict-last, 2 evict-first): bits 0-1 A/B
  *               loads, 2-3 C/X loads, 4-5 D/Y stores.  As an input it applies
  *               only with bit 8 set (0 = automatic).
+ *   prefetch    (also an input) L2 prefetch distance of the A/B stream in
+ *               k-blocks; as an input, prefetch - 1 (0 = automatic, 1 = off).
  * Filled in by gemm_plan / reported by gemm_last_config:
  *   tile_m      128 * cta_group (rows of one CTA group's tile).
  *   tile_k      K elements per ring stage (64 for 16-bit, 128 for 8-bit inputs).
@@ -109,6 +111,7 @@ typedef struct {
   int epi_slots, epi_slot_bytes;
   int cluster_m;
   int l2_hints;
+  int prefetch;
 } gemm_config_t;
 
 /* Every argument of one gemm_run call, for the host-only planning calls. */
