@@ -74,7 +74,7 @@ struct KernelParams {
   int stages;                // A/B ring depth
   int a_mn_major, b_mn_major;
   uint32_t idesc;            // tcgen05 instruction descriptor
-  int prefetch;              // L2 prefetch distance of the A/B stream, in k-blocks (0: off)
+  uint32_t epi_wait_ns;      // suspend-time hint of the epilogue's accumulator wait (0: none)
   uint32_t l2_hints;         // L2 eviction priority (0 normal, 1 last, 2 first):
                              //   bits 0-1 A/B loads, 2-3 C/X loads, 4-5 D/Y stores
   uint32_t* status;          // device status word (watchdog)
@@ -119,12 +119,16 @@ struct Watch {
   unsigned long long timeout_ns;
 };
 
+// Bounded wait for the phase with parity `parity`.  A non-zero `hint_ns` lets
+// the hardware suspend the thread up to that long per probe (for long waits
+// whose spinning would take issue slots from the TMA and MMA warps).
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Watch& w,
-                                           uint32_t role) {
+                                           uint32_t role, uint32_t hint_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (hint_ns ? mbar_try_wait_hint(bar, parity, hint_ns) : mbar_try_wait(bar, parity))
+      return true;
     if (*w.abort) return false;
     if (globaltimer_ns() - t0 > w.timeout_ns) {
       *w.abort = 1u;
@@ -357,25 +361,6 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             for (int j = 0; j < G::BM / G::ATOM_MN; ++j)       // boxes {ATOM_MN, BK}
               issue(&tmA, sa + j * G::ATOM_BYTES, m0 + j * G::ATOM_MN, k0);
           }
-          // Warm L2 `prefetch` k-blocks ahead with the same boxes, so the ring's
-          // loads hit in L2 instead of waiting a DRAM round trip.
-          if (p.prefetch > 0 && kb + p.prefetch < p.k_blocks) {
-            const int kp = (kb + p.prefetch) * G::BK;
-            if (!p.a_mn_major) {
-              tma_prefetch_3d(&tmA, kp, m0, tl);
-            } else {
-#pragma unroll
-              for (int j = 0; j < G::BM / G::ATOM_MN; ++j)
-                tma_prefetch_3d(&tmA, m0 + j * G::ATOM_MN, kp, tl);
-            }
-            if (!p.b_mn_major) {
-              tma_prefetch_3d(&tmB, kp, n0, tl);
-            } else {
-#pragma unroll
-              for (int j = 0; j < G::BN_PART / G::ATOM_MN; ++j)
-                tma_prefetch_3d(&tmB, n0 + j * G::ATOM_MN, kp, tl);
-            }
-          }
           if (!p.b_mn_major) {
             issue_b(sb + grp * G::BN_PART * 128, k0, n0);      // box {BK, BN_PART}
           } else {
@@ -478,7 +463,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
       int tm, tn, tl;
       tile_coords(t, p, tm, tn, tl);
-      const bool ready = wait_phase(tfull0 + 8u * acc, aph, w, kWaitEpilogue);
+      const bool ready = wait_phase(tfull0 + 8u * acc, aph, w, kWaitEpilogue, p.epi_wait_ns);
       __syncwarp();
       ok = named_barrier_and(kEpiBarrier, 128, ready);
       if (!ok) break;

@@ -86,8 +86,9 @@ typedef struct {
  *               each (0 normal, 1 evict-last, 2 evict-first): bits 0-1 A/B
  *               loads, 2-3 C/X loads, 4-5 D/Y stores.  As an input it applies
  *               only with bit 8 set (0 = automatic).
- *   prefetch    (also an input) L2 prefetch distance of the A/B stream in
- *               k-blocks; as an input, prefetch - 1 (0 = automatic, 1 = off).
+ *   epi_wait_ns (also an input) suspend-time hint, in ns, of the epilogue's
+ *               wait for a finished accumulator; as an input, value + 1
+ *               (0 = automatic, 1 = no hint).
  * Filled in by gemm_plan / reported by gemm_last_config:
  *   tile_m      128 * cta_group (rows of one CTA group's tile).
  *   tile_k      K elements per ring stage (64 for 16-bit, 128 for 8-bit inputs).
@@ -111,7 +112,7 @@ typedef struct {
   int epi_slots, epi_slot_bytes;
   int cluster_m;
   int l2_hints;
-  int prefetch;
+  int epi_wait_ns;
 } gemm_config_t;
 
 /* Every argument of one gemm_run call, for the host-only planning calls. */
