@@ -137,8 +137,13 @@ gemm_status_t validate(const gemm_problem_t* pp) {
   return GEMM_OK;
 }
 
+// A/B ring bytes per CTA: stages x (A stage + B stage) + 8 bytes per
+// mbarrier (full and empty per stage, full and empty per accumulator stage)
+// + 4 bytes of tensor-memory address.  A stage holds k_atoms 128-byte-wide
+// K atoms of 128 A rows and tile_n / cta_group B rows.
 int ring_bytes(int cta_group, int tile_n, int ab_bytes, int stages) {
-  const int stage = 128 * 128 + (tile_n / cta_group) * 128;   // A + B, 128-byte rows
+  (void)ab_bytes;
+  const int stage = (128 * 128 + (tile_n / cta_group) * 128) * gb300::k_atoms(cta_group, tile_n);
   return stages * stage + 8 * (2 * stages + 2 * gb300::kAccStages) + 4;
 }
 
@@ -261,7 +266,7 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
   c.cluster_m = mc;
   c.l2_hints = forced && (forced->l2_hints & 0x100) ? (forced->l2_hints & 0x3F) : kDefaultL2Hints;
   c.epi_wait_ns = forced && forced->epi_wait_ns > 0 ? forced->epi_wait_ns - 1 : kDefaultEpiWaitNs;
-  c.tile_k = 128 / ab_bytes;
+  c.tile_k = 128 / ab_bytes * gb300::k_atoms(cg, bn);
   c.acc_stages = gb300::kAccStages;
   c.ring_bytes = ring_bytes(cg, bn, ab_bytes, stages);
   c.epi_slots = slots;
@@ -285,8 +290,8 @@ CUtensorMapDataType tma_type(int dt) {
   }
 }
 
-// Operand tensor map.  K-major: dims {K, rows, L}, box {tile_k, box_rows}.
-// MN-major: dims {rows, K, L}, box {128 bytes of rows, tile_k}.
+// Operand tensor map.  K-major: dims {K, rows, L}, box {one 128-byte atom of
+// K, box_rows}.  MN-major: dims {rows, K, L}, box {128 bytes of rows, tile_k}.
 // Out-of-range elements of a box are filled with zeros.
 bool encode_operand(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int dt, int64_t rows,
                     int64_t K, int64_t L, int64_t ld, bool mn_major, int box_rows, int tile_k) {
@@ -297,7 +302,7 @@ bool encode_operand(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int dt
     dims[0] = (cuuint64_t)K; dims[1] = (cuuint64_t)rows; dims[2] = (cuuint64_t)L;
     strides[0] = (cuuint64_t)(ld * es);
     strides[1] = (cuuint64_t)(ld * es * rows);
-    box[0] = (cuuint32_t)tile_k; box[1] = (cuuint32_t)box_rows; box[2] = 1;
+    box[0] = (cuuint32_t)(128 / es); box[1] = (cuuint32_t)box_rows; box[2] = 1;
   } else {
     dims[0] = (cuuint64_t)rows; dims[1] = (cuuint64_t)K; dims[2] = (cuuint64_t)L;
     strides[0] = (cuuint64_t)(ld * es);

@@ -49,6 +49,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "kernels.h"
 #include "ptx.cuh"
 
 namespace gb300 {
@@ -91,13 +92,18 @@ constexpr uint32_t kEpiBarrier = 1;    // named barrier of the 128 epilogue thre
 
 template <int CG, int BN, int AB_BYTES, int MC>
 struct Geometry {
+  static constexpr int KA = k_atoms(CG, BN);     // 128-byte K atoms per ring stage
   static constexpr int BM = 128;                 // A rows staged per CTA
-  static constexpr int BK = 128 / AB_BYTES;      // K per ring stage: one 128-byte row
+  static constexpr int ATOM_K = 128 / AB_BYTES;  // K of one 128-byte swizzle row
+  static constexpr int BK = ATOM_K * KA;         // K per ring stage
   static constexpr int BN_CTA = BN / CG;         // B rows staged per CTA
-  static constexpr int A_STAGE = BM * 128;       // bytes
-  static constexpr int B_STAGE = BN_CTA * 128;   // bytes
+  static constexpr int A_ATOM = BM * 128;        // bytes of one K-major A atom (128 rows)
+  static constexpr int B_ATOM = BN_CTA * 128;    // bytes of one K-major B atom
+  static constexpr int A_STAGE = A_ATOM * KA;    // bytes
+  static constexpr int B_STAGE = B_ATOM * KA;    // bytes
   static constexpr int UMMA_K = 32 / AB_BYTES;   // K per tcgen05.mma (32 bytes)
   static constexpr int K_STEPS = BK / UMMA_K;    // instructions per stage
+  static constexpr int STEPS_PER_ATOM = ATOM_K / UMMA_K;   // 4
   static constexpr int ATOM_MN = 128 / AB_BYTES; // MN extent of one MN-major swizzle atom
   static constexpr int ATOM_BYTES = BK * 128;    // bytes of one MN-major atom column
   static constexpr int CHUNKS = BN / kEpiChunk;  // epilogue chunks per tile
@@ -355,14 +361,18 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             else tma_load_3d_pair_mc(dst, &tmB, fb_target, c0, c1, tl, b_mask, pol);
           };
           if (!p.a_mn_major) {
-            issue(&tmA, sa, k0, m0);                           // box {BK, 128}
+#pragma unroll
+            for (int a = 0; a < G::KA; ++a)                    // boxes {ATOM_K, 128}
+              issue(&tmA, sa + a * G::A_ATOM, k0 + a * G::ATOM_K, m0);
           } else {
 #pragma unroll
             for (int j = 0; j < G::BM / G::ATOM_MN; ++j)       // boxes {ATOM_MN, BK}
               issue(&tmA, sa + j * G::ATOM_BYTES, m0 + j * G::ATOM_MN, k0);
           }
           if (!p.b_mn_major) {
-            issue_b(sb + grp * G::BN_PART * 128, k0, n0);      // box {BK, BN_PART}
+#pragma unroll
+            for (int a = 0; a < G::KA; ++a)                    // boxes {ATOM_K, BN_PART}
+              issue_b(sb + a * G::B_ATOM + grp * G::BN_PART * 128, k0 + a * G::ATOM_K, n0);
           } else {
             constexpr int ATOMS = G::BN_PART / G::ATOM_MN;     // boxes {ATOM_MN, BK}
 #pragma unroll
@@ -391,16 +401,18 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           const uint32_t sb = b_ring + s * G::B_STAGE;
 #pragma unroll
           for (int k = 0; k < G::K_STEPS; ++k) {
-            // K-major: rows of 128 bytes, 8-row groups 1024 bytes apart; step k
-            // moves 32 bytes along the swizzled row.  MN-major: K rows of 128
-            // bytes, 8-row groups 1024 apart, MN atoms ATOM_BYTES apart; step k
-            // moves UMMA_K rows.
+            // K-major: atoms of rows x 128 bytes, 8-row groups 1024 bytes
+            // apart; step k selects atom k / STEPS_PER_ATOM and moves 32 bytes
+            // along its swizzled rows.  MN-major: K rows of 128 bytes, 8-row
+            // groups 1024 apart, MN atoms ATOM_BYTES apart; step k moves
+            // UMMA_K rows.
+            const int ka = k / G::STEPS_PER_ATOM, kk = k % G::STEPS_PER_ATOM;
             const uint64_t ad = p.a_mn_major
                 ? smem_desc_sw128(sa + k * G::UMMA_K * 128, G::ATOM_BYTES, 1024)
-                : smem_desc_sw128(sa + k * 32, 16, 1024);
+                : smem_desc_sw128(sa + ka * G::A_ATOM + kk * 32, 16, 1024);
             const uint64_t bd = p.b_mn_major
                 ? smem_desc_sw128(sb + k * G::UMMA_K * 128, G::ATOM_BYTES, 1024)
-                : smem_desc_sw128(sb + k * 32, 16, 1024);
+                : smem_desc_sw128(sb + ka * G::B_ATOM + kk * 32, 16, 1024);
             umma<CG, KIND>(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
           }
           umma_commit<CG, MULTI>(empty0 + 8u * s, all_mask);   // slot drained: tell every loader

@@ -91,7 +91,9 @@ typedef struct {
  *               (0 = automatic, 1 = no hint).
  * Filled in by gemm_plan / reported by gemm_last_config:
  *   tile_m      128 * cta_group (rows of one CTA group's tile).
- *   tile_k      K elements per ring stage (64 for 16-bit, 128 for 8-bit inputs).
+ *   tile_k      K elements per ring stage: one or two 128-byte swizzle atoms (64
+ *               or 128 K for 16-bit inputs, 128 or 256 for 8-bit); two unless the
+ *               tile is a single CTA's 128 x 256.
  *   acc_stages  tensor-memory accumulator stages (2: double buffered).
  *   ring_bytes  ring bytes per CTA: stages*(A stage + B stage) + 8 bytes per
  *               mbarrier (2 per stage, 2 per accumulator stage) + 4 bytes of

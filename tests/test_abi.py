@@ -167,7 +167,9 @@ def test_plan_every_workload(lib, name):
     st, cfg = G.gemm_plan(p, 152, 232448)
     assert st == G.GEMM_OK
     assert cfg.cta_group in (1, 2) and cfg.tile_n in (128, 256)
-    assert cfg.tile_k == (128 if w.ab == "e4m3" else 64)
+    atom_k = 128 if w.ab == "e4m3" else 64            # K of one 128-byte swizzle atom
+    k_atoms = 1 if (cfg.cta_group, cfg.tile_n) == (1, 256) else 2
+    assert cfg.tile_k == atom_k * k_atoms
     assert 2 <= cfg.stages and cfg.smem_bytes <= 232448
     rows = cfg.tile_m * cfg.cluster_m                  # output rows per cluster tile
     assert cfg.tiles == (-(-w.M // rows)) * (-(-w.N // cfg.tile_n)) * w.L
