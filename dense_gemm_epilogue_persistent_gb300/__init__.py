@@ -92,6 +92,10 @@ def library():
             lib.gemm_run.argtypes = [vp, i64, i64, i64, i64, vp, i64, i32, vp, i64, i32, vp, vp,
                                      vp, vp, f32, f32, f32, ctypes.POINTER(gemm_dtypes_t), vp]
             lib.gemm_sync_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
+            lib.gemm_run_noalloc.argtypes = [i64, i64, i64, i64, vp, i64, i32, vp, i64, i32, vp,
+                                             vp, vp, vp, f32, f32, f32,
+                                             ctypes.POINTER(gemm_dtypes_t), vp,
+                                             ctypes.POINTER(ctypes.c_uint32)]
             lib.gemm_status_string.argtypes = [i32]
             lib.gemm_status_string.restype = ctypes.c_char_p
             lib.gemm_check.argtypes = [ctypes.POINTER(gemm_problem_t)]
@@ -101,7 +105,8 @@ def library():
             lib.gemm_last_config.argtypes = [vp, ctypes.POINTER(gemm_config_t)]
             lib.gemm_tmem_columns.argtypes = [i32, i32]
             lib.gemm_set_timeout_ns.argtypes = [vp, ctypes.c_uint64]
-            for name in ("gemm_create", "gemm_destroy", "gemm_run", "gemm_sync_status",
+            for name in ("gemm_create", "gemm_destroy", "gemm_run", "gemm_run_noalloc",
+                         "gemm_sync_status",
                          "gemm_check", "gemm_plan", "gemm_set_config", "gemm_last_config",
                          "gemm_tmem_columns", "gemm_set_timeout_ns"):
                 getattr(lib, name).restype = i32
@@ -158,6 +163,23 @@ def gemm_run(handle, M, N, K, L, A, lda, layoutA, B, ldb, layoutB, C, X, D, Y,
     if check and st != GEMM_OK:
         raise GemmError(st, "gemm_run")
     return st
+
+
+def gemm_run_noalloc(M, N, K, L, A, lda, layoutA, B, ldb, layoutB, C, X, D, Y, alpha, beta,
+                     x_factor, dtypes: gemm_dtypes_t, stream=None, check=True,
+                     watchdog=False) -> tuple[int, int]:
+    """gemm_run without a handle and without allocating device memory (the
+    watchdog status word lives in a static device array); see the C header.
+    watchdog=True makes the call synchronise and report the status word.
+    Returns (status, watchdog word)."""
+    word = ctypes.c_uint32(0)
+    st = library().gemm_run_noalloc(M, N, K, L, _ptr(A), lda, layoutA, _ptr(B), ldb, layoutB,
+                                    _ptr(C), _ptr(X), _ptr(D), _ptr(Y), alpha, beta, x_factor,
+                                    ctypes.byref(dtypes), _stream(stream),
+                                    ctypes.byref(word) if watchdog else None)
+    if check and st != GEMM_OK:
+        raise GemmError(st, "gemm_run_noalloc")
+    return st, word.value
 
 
 def gemm_sync_status(handle, stream=None) -> tuple[int, int]:

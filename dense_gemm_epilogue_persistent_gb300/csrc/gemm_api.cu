@@ -660,3 +660,137 @@ GEMM_API gemm_status_t gemm_sync_status(gemm_handle_t h, struct CUstream_st* str
   }
   return GEMM_OK;
 }
+
+// ====================================================================== no-allocation entry point
+//
+// gemm_run_noalloc: the same GEMM for callers that must not allocate device
+// memory.  The only device memory the kernel needs beyond the caller's
+// tensors is its 4-byte watchdog status word, which gemm_create obtains with
+// cudaMalloc; here it lives in a file-scope __device__ array instead, and the
+// per-device state a handle would hold lives in static host storage.
+
+// Scratch of gemm_run_noalloc: 64 words (256 bytes) on every GPU that loads
+// this library, kept until the process exits.  A call uses one word (the
+// watchdog status), whatever the problem size.
+static constexpr int kNoallocScratchWords = 64;
+static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoallocScratchWords];
+
+namespace {
+
+constexpr int kNoallocWordsPerCall = 1;
+constexpr int kNoallocMaxDevices = 64;
+
+struct NoallocSlot {
+  std::mutex mu;
+  bool ready = false;
+  gemm_handle handle;   // static storage; its d_status points at the scratch
+};
+NoallocSlot g_noalloc_slots[kNoallocMaxDevices];
+
+// One-time set-up for `device` (which must be current): device checks, the
+// tensor-map encoder, resident-cluster counts, and the device address of the
+// scratch array.  Nothing is allocated.
+gemm_status_t noalloc_setup(gemm_handle& h, int device) {
+  int major = 0, minor = 0, sms = 0, optin = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) !=
+          cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  if (major != 10 || minor != 3) return GEMM_ERR_UNSUPPORTED_ARCH;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  // The array's name is only a host-side stand-in: the kernel needs the
+  // device address, which the runtime resolves for the current device.
+  void* scratch = nullptr;
+  if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess || !scratch) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  int clusters[5] = {0, 0, 0, 0, 0};
+  {
+    const void* kern = gb300::kernel_for(2, 2, 256, 2);
+    const int smem = optin / 2 + 1024;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
+        cudaSuccess) {
+      for (int cs : {1, 2, 4}) {
+        cudaLaunchConfig_t lc{};
+        cudaLaunchAttribute attr[1];
+        lc.gridDim = dim3((unsigned)(cs * sms));
+        lc.blockDim = dim3(gb300::kThreads);
+        lc.dynamicSmemBytes = (size_t)smem;
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)cs;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        lc.attrs = attr;
+        lc.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &lc) == cudaSuccess) clusters[cs] = n;
+      }
+    }
+    cudaGetLastError();
+  }
+  for (int i = 0; i < 5; ++i) h.clusters_by_size[i] = clusters[i];
+  h.device = device;
+  h.sm_count = sms;
+  h.smem_optin = optin;
+  h.encode = reinterpret_cast<EncodeTiledFn>(fn);
+  h.d_status = static_cast<uint32_t*>(scratch);
+  return GEMM_OK;
+}
+
+}  // namespace
+
+GEMM_API gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int64_t L,
+                                        const void* A, int64_t lda, gemm_layout_t layoutA,
+                                        const void* B, int64_t ldb, gemm_layout_t layoutB,
+                                        const void* C, const void* X, void* D, void* Y,
+                                        float alpha, float beta, float x_factor,
+                                        const gemm_dtypes_t* dtypes, struct CUstream_st* stream,
+                                        uint32_t* watchdog_out) {
+  if (watchdog_out) *watchdog_out = 0;
+  // Scratch a call needs against what the array holds (a constant one word).
+  if (kNoallocWordsPerCall > kNoallocScratchWords) return GEMM_ERR_INVALID_ARG;
+  int device = -1;
+  if (cudaGetDevice(&device) != cudaSuccess) { cudaGetLastError(); return GEMM_ERR_CUDA; }
+  if (device < 0 || device >= kNoallocMaxDevices) return GEMM_ERR_INVALID_ARG;
+  NoallocSlot& slot = g_noalloc_slots[device];
+  {
+    std::lock_guard<std::mutex> g(slot.mu);
+    if (!slot.ready) {
+      const gemm_status_t st = noalloc_setup(slot.handle, device);
+      if (st != GEMM_OK) return st;
+      slot.ready = true;
+    }
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // The status word must read zero when the kernel starts: the array keeps
+  // whatever the previous call left in it.
+  if (cudaMemsetAsync(slot.handle.d_status, 0, sizeof(uint32_t) * kNoallocWordsPerCall, s) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  const gemm_status_t st = gemm_run(&slot.handle, M, N, K, L, A, lda, layoutA, B, ldb, layoutB,
+                                    C, X, D, Y, alpha, beta, x_factor, dtypes, stream);
+  if (st != GEMM_OK || !watchdog_out) return st;
+  uint32_t word = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess ||
+      cudaMemcpy(&word, slot.handle.d_status, sizeof(word), cudaMemcpyDeviceToHost) !=
+          cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  *watchdog_out = word;
+  return word ? GEMM_ERR_DEVICE_TIMEOUT : GEMM_OK;
+}

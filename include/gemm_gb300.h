@@ -199,6 +199,39 @@ int gemm_tmem_columns(int tile_m, int tile_n);
  * (0 restores the default of 4 seconds). */
 gemm_status_t gemm_set_timeout_ns(gemm_handle_t h, uint64_t ns);
 
+/* gemm_run without allocating anything: for callers that must not call
+ * cudaMalloc -- code paths under a framework's memory pool that owns all of
+ * the device's memory, latency-critical loops where cudaMalloc's device-wide
+ * synchronisation would stall other work, and environments that forbid
+ * dynamic allocation after start-up.  (The pages have no counterpart: this
+ * is a library-level addition.)
+ *
+ * Same arguments, layouts, validation and result as gemm_run, but without a
+ * handle: it runs on the calling thread's current device.  The kernel's one
+ * piece of scratch memory, its 4-byte watchdog status word, lives in a
+ * file-scope device array of 64 words (256 bytes) that every GPU loading the
+ * library holds until the process exits; a call needs one word whatever the
+ * problem size, and a call needing more than the array holds would be
+ * rejected with GEMM_ERR_INVALID_ARG.
+ *
+ * The first call on a device does a one-time set-up there (device checks,
+ * tensor-map encoder, the array's device address); make that first call
+ * before any stream capture.  Each call clears the status word on `stream`
+ * before its launch.  Every call shares the array, so calls that overlap on
+ * the GPU (different streams, no ordering between them) race on the status
+ * word: one may clear or report the other's watchdog record.
+ *
+ * watchdog_out NULL: asynchronous, like gemm_run.  Non-NULL: the call then
+ * synchronises `stream`, stores the status word there and returns
+ * GEMM_ERR_DEVICE_TIMEOUT if it is non-zero. */
+gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int64_t L,
+                               const void* A, int64_t lda, gemm_layout_t layoutA,
+                               const void* B, int64_t ldb, gemm_layout_t layoutB,
+                               const void* C, const void* X, void* D, void* Y,
+                               float alpha, float beta, float x_factor,
+                               const gemm_dtypes_t* dtypes, struct CUstream_st* stream,
+                               uint32_t* watchdog_out);
+
 #ifdef __cplusplus
 }
 #endif
