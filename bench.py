@@ -70,24 +70,36 @@ def tensor_peak(peaks, ab: str, sustained=False):
     return base * (2.0 if ab == "e4m3" else 1.0)
 
 
+DEVICE_SOURCES = ("gemm_kernel.cuh", "ptx.cuh", "kernels.h")
+
+
 def kernel_source_digest():
+    """Digest of the device code (the kernel template, its PTX wrappers and
+    the instantiation units)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_gemm_epilogue_persistent_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        if f in DEVICE_SOURCES or f.startswith("kern_"):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def config_key(cfg) -> str:
+    return (f"cg{cfg.cta_group}_n{cfg.tile_n}_mc{cfg.cluster_m}_k{cfg.tile_k}_st{cfg.stages}"
+            f"_e{cfg.epi_slots}_gm{cfg.group_m}_l2{cfg.l2_hints}")
+
+
+def recorded_traffic(workload: str, cfg):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources (else None)."""
+    on the current device code and launch configuration (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f).get(workload)
-    if not d or d.get("kernel_src_digest") != kernel_source_digest():
+    if (not d or d.get("kernel_src_digest") != kernel_source_digest()
+            or d.get("config") != config_key(cfg)):
         return None
     return d.get("dram_bytes_per_launch")
 
@@ -413,7 +425,7 @@ def main():
     achieved = flops / (kernel_ms / 1e3) / 1e12
     ratio_note = " x2 (fp8/bf16 nominal ratio)" if w.ab == "e4m3" else ""
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": recorded_traffic(w.name),
+                "frac": achieved / peak, "traffic": recorded_traffic(w.name, cfg),
                 "algorithmic_flops_per_launch": flops,
                 "peak_source": f"{peaks['source']} bf16 "
                                f"{'sustained' if sustained else 'burst'}{ratio_note}; timed "
