@@ -41,7 +41,7 @@ constexpr int kMaxEpiSlots = 4;
 // on all five benchmark shapes (fp8 3000x5000x4096: +11% over evict-normal).
 constexpr int kDefaultL2Hints = 2 | (2 << 2) | (2 << 4);
 constexpr int kDefaultEpiWaitNs = 0;
-constexpr int kSmemSlack = 1024 + 16;   // base alignment + abort flag
+constexpr int kSmemSlack = 1024 + 16;   // base alignment + abort flag + watchdog-test barrier
 
 struct VariantState {
   int smem_set = 0;          // dynamic smem attribute last set
@@ -266,6 +266,7 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
   c.cluster_m = mc;
   c.l2_hints = forced && (forced->l2_hints & 0x100) ? (forced->l2_hints & 0x3F) : kDefaultL2Hints;
   c.epi_wait_ns = forced && forced->epi_wait_ns > 0 ? forced->epi_wait_ns - 1 : kDefaultEpiWaitNs;
+  c.inject_stall = forced && forced->inject_stall ? 1 : 0;
   c.tile_k = 128 / ab_bytes * gb300::k_atoms(cg, bn);
   c.acc_stages = gb300::kAccStages;
   c.ring_bytes = ring_bytes(cg, bn, ab_bytes, stages);
@@ -608,6 +609,7 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
   kp.idesc = make_idesc(dtypes->ab, cfg.cta_group, cfg.tile_n, a_mn, b_mn);
   kp.l2_hints = (uint32_t)cfg.l2_hints;
   kp.epi_wait_ns = (uint32_t)cfg.epi_wait_ns;
+  kp.inject_stall = cfg.inject_stall;
   kp.status = h->d_status;
   kp.timeout_ns = h->timeout_ns;
   kp.epi.c_dt = dtypes->c;

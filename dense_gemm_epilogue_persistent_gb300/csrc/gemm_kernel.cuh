@@ -76,6 +76,7 @@ struct KernelParams {
   int a_mn_major, b_mn_major;
   uint32_t idesc;            // tcgen05 instruction descriptor
   uint32_t epi_wait_ns;      // suspend-time hint of the epilogue's accumulator wait (0: none)
+  int inject_stall;          // test only: the MMA warp first waits on a barrier nobody arrives at
   uint32_t l2_hints;         // L2 eviction priority (0 normal, 1 last, 2 first):
                              //   bits 0-1 A/B loads, 2-3 C/X loads, 4-5 D/Y stores
   uint32_t* status;          // device status word (watchdog)
@@ -116,7 +117,8 @@ struct Geometry {
 
 // Watchdog codes: 0xE0RRBBBB, RR = role, BBBB = low 16 bits of blockIdx.x.
 enum : uint32_t {
-  kWaitProducer = 1, kWaitMmaFull = 2, kWaitMmaAcc = 3, kWaitEpilogue = 4, kWaitEpiLoad = 5
+  kWaitProducer = 1, kWaitMmaFull = 2, kWaitMmaAcc = 3, kWaitEpilogue = 4, kWaitEpiLoad = 5,
+  kWaitInjected = 6
 };
 
 struct Watch {
@@ -290,7 +292,8 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   const uint32_t slot_bytes = e.cd_bytes + e.xy_bytes;
 
   // [B ring][A ring][epilogue slots][full x S][empty x S][tfull x 2][tempty x 2]
-  // [cfull x E][tmem address][abort flag]
+  // [cfull x E][tmem address][abort flag][never]  ("never": a barrier nothing
+  // arrives at, waited on only when a stall is injected to test the watchdog)
   const uint32_t b_ring = base;
   const uint32_t a_ring = b_ring + S * G::B_STAGE;
   const uint32_t epi0 = a_ring + S * G::A_STAGE;
@@ -301,6 +304,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   const uint32_t holder = cfull0 + 8u * E;
   volatile uint32_t* const holder_ptr = reinterpret_cast<volatile uint32_t*>(gbase + (holder - base));
   volatile uint32_t* const abort_ptr = holder_ptr + 1;
+  const uint32_t never_bar = holder + 8u;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -312,6 +316,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       mbar_init(tempty0 + 8u * a, 4 * CG);   // every epilogue warp of the CTA (pair)
     }
     for (int s = 0; s < E; ++s) mbar_init(cfull0 + 8u * s, 1);
+    mbar_init(never_bar, 1);
     *abort_ptr = 0u;
     fence_barrier_init();
   }
@@ -389,7 +394,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     if (rank == 0 && lane == 0) {
       int s = 0, acc = 0;
       uint32_t ph = 0, aph = 0;
-      bool ok = true;
+      bool ok = !p.inject_stall || wait_phase(never_bar, 0u, w, kWaitInjected);
       for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
         if (!wait_phase(tempty0 + 8u * acc, aph ^ 1u, w, kWaitMmaAcc)) break;
         tc_fence_after_sync();

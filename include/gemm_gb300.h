@@ -89,6 +89,10 @@ typedef struct {
  *   epi_wait_ns (also an input) suspend-time hint, in ns, of the epilogue's
  *               wait for a finished accumulator; as an input, value + 1
  *               (0 = automatic, 1 = no hint).
+ *   inject_stall  (input, tests of the watchdog only) non-zero: the MMA warp
+ *               first waits on a barrier nothing ever arrives at, so every launch
+ *               ends through the watchdog with GEMM_ERR_DEVICE_TIMEOUT (role 6 in
+ *               the status word) after the configured timeout.
  * Filled in by gemm_plan / reported by gemm_last_config:
  *   tile_m      128 * cta_group (rows of one CTA group's tile).
  *   tile_k      K elements per ring stage: one or two 128-byte swizzle atoms (64
@@ -115,6 +119,7 @@ typedef struct {
   int cluster_m;
   int l2_hints;
   int epi_wait_ns;
+  int inject_stall;
 } gemm_config_t;
 
 /* Every argument of one gemm_run call, for the host-only planning calls. */
