@@ -47,7 +47,7 @@ def parse_args():
     ap.add_argument("--no-per-config", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
 
@@ -283,6 +283,38 @@ class Bound:
         return sum(t.numel() * t.element_size() for t in (self.D, self.Y) if t is not None)
 
 
+# ---------------------------------------------------------------- ranks
+
+def init_ranks(world: int, rank: int):
+    """One process per GPU: NCCL when CUDA is present, gloo otherwise (tests).
+    Only the barrier and the max-time reduction use it."""
+    import torch
+    import torch.distributed as dist
+    if world <= 1:
+        return None
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    dist.init_process_group(backend, rank=rank, world_size=world)
+    return dist
+
+
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """The largest of every rank's `value` (the slowest rank's time)."""
+    import torch
+    if dist is None:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Every rank runs `steps` steps of the same replica; the job's throughput
+    is all ranks' work over the slowest rank's time."""
+    return flops_per_step * steps * world / (max_ms / 1e3) / 1e12
+
+
 def time_launches(torch, bound, stream, iters, warmup):
     for _ in range(warmup):
         bound.launch(stream)
@@ -307,17 +339,14 @@ def main():
         return
 
     import torch
-    import torch.distributed as dist
 
     import workloads as W
     from dense_gemm_epilogue_persistent_gb300 import build as _build
     _build.build()
     import dense_gemm_epilogue_persistent_gb300 as G
 
-    if world > 1:
-        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
-        dist.init_process_group("nccl", rank=rank, world_size=world)
     torch.cuda.set_device(local_rank)
+    pg = init_ranks(world, rank)
     device = local_rank
     peaks = load_peaks()
     w = W.WORKLOADS[args.workload]
@@ -327,8 +356,8 @@ def main():
     stream = torch.cuda.current_stream()
 
     def barrier():
-        if world > 1:
-            dist.barrier()
+        if pg is not None:
+            pg.barrier()
 
     # warm-up (and a status check: the watchdog must be clean)
     warm = max(3, args.warmup)
@@ -365,55 +394,82 @@ def main():
     total_ms = t_start.elapsed_time(t_end)
     per_launch = [e0.elapsed_time(e1) for e0, e1 in evs]
     kernel_ms = sum(per_launch) / len(per_launch)
-    t = torch.tensor([total_ms], device="cuda")
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    max_ms = float(t.item())
+    max_ms = max_over_ranks(total_ms, pg, device="cuda")
     flops = w.flops
-    value = flops * args.steps * world / (max_ms / 1e3) / 1e12
+    value = whole_job_tflops(flops, args.steps, world, max_ms)
 
-    # end to end through the public API: pinned host inputs -> device ->
-    # gemm_run -> device outputs -> pinned host, every step
+    # End to end through the public API: every step copies its inputs from
+    # pinned host memory to the device, runs gemm_run, and copies D and Y back
+    # to pinned host memory.  Steps are pipelined the way a serving loop would
+    # run them: host-to-device copies, the GEMM and device-to-host copies run
+    # on three streams over two device buffer sets, ordered by events, so step
+    # i+1's inputs stream in while step i computes and step i-1's results
+    # stream out.  The timed region spans every step's copies and GEMM.
     e2e = None
     if not args.no_e2e:
+        names = [n for n, t in zip("ABCX", (bound.A, bound.B, bound.C, bound.X)) if t is not None]
         h_in = [t.cpu().pin_memory() for t in (bound.A, bound.B, bound.C, bound.X)
                 if t is not None]
-        h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                 for t in (bound.D, bound.Y) if t is not None]
-        d_in = [torch.empty_like(t, device="cuda") for t in h_in]
-        names = [n for n, t in zip("ABCX", (bound.A, bound.B, bound.C, bound.X)) if t is not None]
+        outs0 = [t for t in (bound.D, bound.Y) if t is not None]
+        h_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs0]
+                 for _ in range(2)]
+        d_in = [[torch.empty_like(t, device="cuda") for t in h_in] for _ in range(2)]
+        d_out = [[torch.empty_like(t) for t in outs0] for _ in range(2)]
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        s_mm = stream
+        ev_in = [torch.cuda.Event() for _ in range(2)]      # inputs of set b landed
+        ev_mm = [torch.cuda.Event() for _ in range(2)]      # GEMM on set b finished
+        ev_out = [torch.cuda.Event() for _ in range(2)]     # results of set b copied out
+        primed = [False, False]
 
-        def e2e_step():
-            for h, d in zip(h_in, d_in):
-                d.copy_(h, non_blocking=True)
-            kw = dict(zip(names, d_in))
-            bound.launch(stream, **kw)
-            outs = [t for t in (bound.D, bound.Y) if t is not None]
-            for h, d in zip(h_out, outs):
-                h.copy_(d, non_blocking=True)
+        def e2e_step(i):
+            b = i % 2
+            with torch.cuda.stream(s_in):
+                if primed[b]:
+                    s_in.wait_event(ev_mm[b])               # set b's inputs consumed
+                for h, d in zip(h_in, d_in[b]):
+                    d.copy_(h, non_blocking=True)
+                ev_in[b].record(s_in)
+            s_mm.wait_event(ev_in[b])
+            if primed[b]:
+                s_mm.wait_event(ev_out[b])                  # set b's outputs drained
+            kw = dict(zip(names, d_in[b]))
+            kw["D"] = d_out[b][0]
+            if len(d_out[b]) > 1:
+                kw["Y"] = d_out[b][1]
+            bound.launch(s_mm, **kw)
+            ev_mm[b].record(s_mm)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_mm[b])
+                for h, d in zip(h_out[b], d_out[b]):
+                    h.copy_(d, non_blocking=True)
+                ev_out[b].record(s_out)
+            primed[b] = True
 
-        e2e_step()
+        for i in range(2):                                  # warm-up of both sets
+            e2e_step(i)
         torch.cuda.synchronize()
         a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
+        b_ev = torch.cuda.Event(enable_timing=True)
         barrier()
-        a.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
-        b.record(stream)
+        torch.cuda.synchronize()
+        a.record(s_in)
+        for i in range(args.e2e_steps):
+            e2e_step(i)
+        s_in.wait_stream(s_out)
+        s_in.wait_stream(s_mm)
+        b_ev.record(s_in)
         torch.cuda.synchronize()
         barrier()
-        et = torch.tensor([a.elapsed_time(b)], device="cuda")
-        if world > 1:
-            dist.all_reduce(et, op=dist.ReduceOp.MAX)
-        e2e_ms = float(et.item()) / args.e2e_steps
+        e2e_ms = max_over_ranks(a.elapsed_time(b_ev), pg, device="cuda") / args.e2e_steps
         st, _ = g.sync_status(stream.cuda_stream)
         h2d = sum(t.numel() * t.element_size() for t in h_in)
-        d2h = sum(t.numel() * t.element_size() for t in h_out)
+        d2h = sum(t.numel() * t.element_size() for t in h_out[0])
         e2e = {"value": flops * world / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-               "status": G.gemm_status_string(st)}
-        del h_in, h_out, d_in
+               "steps": args.e2e_steps, "pipelined": "H2D / GEMM / D2H on three streams, "
+               "two device buffer sets", "status": G.gemm_status_string(st)}
+        del h_in, h_out, d_in, d_out
 
     # The measured peaks come as a burst (cuBLAS, best of 10) and a sustained
     # figure (back to back for seconds, under the power cap).  A timed region
@@ -486,8 +542,8 @@ def main():
         }
         print(json.dumps(line), flush=True)
     g.close()
-    if world > 1:
-        dist.destroy_process_group()
+    if pg is not None:
+        pg.destroy_process_group()
 
 
 if __name__ == "__main__":
