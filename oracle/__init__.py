@@ -49,7 +49,10 @@ def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
+            # ORACLE_LIB_OVERRIDE: a deliberately broken copy, built by the
+            # mutation tests to show that the pins catch planted mistakes.
+            override = os.environ.get("ORACLE_LIB_OVERRIDE")
+            lib = ctypes.CDLL(override if override else build())
             i64, i32, f64, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_double, ctypes.c_void_p
             lib.oracle_decode.restype = f64
             lib.oracle_decode.argtypes = [i32, ctypes.c_uint32]
