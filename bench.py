@@ -67,7 +67,7 @@ def tensor_peak(peaks, ab: str, sustained=False):
     """Dense tensor peak for the input type: fp16 runs at the bf16 rate; fp8
     at twice it (nominal ratio 4.5 / 2.25 PFLOP/s)."""
     base = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
-    return base * (2.0 if ab == "e4m3" else 1.0)
+    return base * (2.0 if ab in ("e4m3", "e5m2") else 1.0)
 
 
 DEVICE_SOURCES = ("gemm_kernel.cuh", "ptx.cuh", "kernels.h")
@@ -175,7 +175,7 @@ def oracle_problem_for(w, inp):
     return oracle.Problem(w.M, w.N, w.K, w.L, st(As), As.shape[-1], w.a_mn_major, st(Bs),
                           Bs.shape[-1], w.b_mn_major, None if Cs is None else st(Cs),
                           None if Xs is None else st(Xs), w.ab, w.c or "f32", w.x or "f32",
-                          w.cd_m_major, w.alpha, w.beta, w.x_factor)
+                          w.cd_m_major, w.alpha, w.beta, w.x_factor, b_dtype=w.b, relu=w.relu)
 
 
 def time_oracle_sample(w, inp, seconds: float):
@@ -262,7 +262,8 @@ class Bound:
         self.D = torch.empty(shape, dtype=W.TORCH_DTYPE[w.d], device=dev)
         self.Y = torch.empty(shape, dtype=W.TORCH_DTYPE[w.y], device=dev) if w.y else None
         self.dt = G.make_dtypes(w.ab, w.c or "f32", w.d, w.x or "f32", w.y or "f32",
-                                G.GEMM_MN_MAJOR if w.cd_m_major else G.GEMM_K_MAJOR)
+                                G.GEMM_MN_MAJOR if w.cd_m_major else G.GEMM_K_MAJOR, b=w.b,
+                                epilogue=G.GEMM_EPI_RELU if w.relu else G.GEMM_EPI_LINEAR)
         self.G, self.g = G, g
 
     def launch(self, stream, A=None, B=None, C=None, X=None, D=None, Y=None):
@@ -479,7 +480,7 @@ def main():
     peak = tensor_peak(peaks, w.ab, sustained=sustained)
     burst = tensor_peak(peaks, w.ab, sustained=False)
     achieved = flops / (kernel_ms / 1e3) / 1e12
-    ratio_note = " x2 (fp8/bf16 nominal ratio)" if w.ab == "e4m3" else ""
+    ratio_note = " x2 (fp8/bf16 nominal ratio)" if w.ab in ("e4m3", "e5m2") else ""
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": recorded_traffic(w.name, cfg),
                 "algorithmic_flops_per_launch": flops,
@@ -519,11 +520,13 @@ def main():
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": warm, "ms_per_step": max_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": {"f16": "f16", "bf16": "bf16", "e4m3": "e4m3"}[w.ab] + " in, f32 accumulate",
+            "dtype": w.ab + (f"/{w.b}" if w.b else "") + " in, f32 accumulate",
             "data": "synthetic",
             "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "L": w.L,
                        "ab": w.ab, "c": w.c, "d": w.d, "x": w.x, "y": w.y,
-                       "epilogue": f"Y=AB, D={w.alpha}*AB+{w.beta}*C+{w.x_factor}*X",
+                       "epilogue": (f"Y=AB, D=relu({w.alpha}*AB+{w.beta}*C)+{w.x_factor}*X"
+                                    if w.relu else
+                                    f"Y=AB, D={w.alpha}*AB+{w.beta}*C+{w.x_factor}*X"),
                        "kernel": {"cta_group": cfg.cta_group, "tile": f"{cfg.tile_m}x{cfg.tile_n}",
                                   "tile_k": cfg.tile_k, "stages": cfg.stages,
                                   "grid_ctas": cfg.grid_ctas, "group_m": cfg.group_m},

@@ -30,15 +30,18 @@ GEMM_ERR_CUDA = 5
 GEMM_ERR_DEVICE_TIMEOUT = 6
 GEMM_ERR_UNSUPPORTED_CONFIG = 7
 
-GEMM_F32, GEMM_F16, GEMM_BF16, GEMM_E4M3 = 0, 1, 2, 3
+GEMM_F32, GEMM_F16, GEMM_BF16, GEMM_E4M3, GEMM_E5M2 = 0, 1, 2, 3, 4
 GEMM_K_MAJOR, GEMM_MN_MAJOR = 0, 1
+GEMM_EPI_LINEAR, GEMM_EPI_RELU = 0, 1
 
-DTYPE_CODES = {"f32": GEMM_F32, "f16": GEMM_F16, "bf16": GEMM_BF16, "e4m3": GEMM_E4M3}
+DTYPE_CODES = {"f32": GEMM_F32, "f16": GEMM_F16, "bf16": GEMM_BF16, "e4m3": GEMM_E4M3,
+               "e5m2": GEMM_E5M2}
 
 
 class gemm_dtypes_t(ctypes.Structure):
     _fields_ = [("ab", ctypes.c_int), ("c", ctypes.c_int), ("d", ctypes.c_int),
-                ("x", ctypes.c_int), ("y", ctypes.c_int), ("cdxy_major", ctypes.c_int)]
+                ("x", ctypes.c_int), ("y", ctypes.c_int), ("cdxy_major", ctypes.c_int),
+                ("b", ctypes.c_int), ("epilogue", ctypes.c_int)]
 
 
 class gemm_config_t(ctypes.Structure):
@@ -131,9 +134,12 @@ def _stream(s) -> int | None:
     return int(s.cuda_stream)
 
 
-def make_dtypes(ab, c="f32", d="f32", x="f32", y="f32", cdxy_major=GEMM_K_MAJOR) -> gemm_dtypes_t:
+def make_dtypes(ab, c="f32", d="f32", x="f32", y="f32", cdxy_major=GEMM_K_MAJOR, b=None,
+                epilogue=GEMM_EPI_LINEAR) -> gemm_dtypes_t:
+    """b: B's type when it differs from A's (fp8 pairs); epilogue: GEMM_EPI_*."""
     code = lambda v: DTYPE_CODES[v] if isinstance(v, str) else int(v)
-    return gemm_dtypes_t(code(ab), code(c), code(d), code(x), code(y), int(cdxy_major))
+    return gemm_dtypes_t(code(ab), code(c), code(d), code(x), code(y), int(cdxy_major),
+                         GEMM_F32 if b is None or b == ab else code(b), int(epilogue))
 
 
 # ------------------------------------------------------------------ C entry points

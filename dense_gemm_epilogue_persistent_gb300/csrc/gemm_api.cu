@@ -73,12 +73,16 @@ int dtype_bytes(int dt) {
     case GEMM_F16: return 2;
     case GEMM_BF16: return 2;
     case GEMM_E4M3: return 1;
+    case GEMM_E5M2: return 1;
   }
   return 0;
 }
 
 bool is_epi_type(int dt) { return dt == GEMM_F32 || dt == GEMM_F16 || dt == GEMM_BF16; }
-bool is_ab_type(int dt) { return dt == GEMM_F16 || dt == GEMM_BF16 || dt == GEMM_E4M3; }
+bool is_fp8(int dt) { return dt == GEMM_E4M3 || dt == GEMM_E5M2; }
+bool is_ab_type(int dt) { return dt == GEMM_F16 || dt == GEMM_BF16 || is_fp8(dt); }
+// B's type: the descriptor's b when set (0 = GEMM_F32 means "same as ab").
+int b_type(const gemm_dtypes_t& t) { return t.b == GEMM_F32 ? t.ab : t.b; }
 bool is_layout(int v) { return v == GEMM_K_MAJOR || v == GEMM_MN_MAJOR; }
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -99,6 +103,10 @@ gemm_status_t validate(const gemm_problem_t* pp) {
   if (!is_ab_type(t.ab) || !is_epi_type(t.c) || !is_epi_type(t.d) || !is_epi_type(t.x) ||
       !is_epi_type(t.y))
     return GEMM_ERR_UNSUPPORTED_DTYPE;
+  // A and B share one type, except fp8 pairs (the tensor core's f8f6f4 kind
+  // takes E4M3 and E5M2 in any pairing).
+  if (t.b != GEMM_F32 && !(is_fp8(t.ab) && is_fp8(t.b))) return GEMM_ERR_UNSUPPORTED_DTYPE;
+  if (t.epilogue != GEMM_EPI_LINEAR && t.epilogue != GEMM_EPI_RELU) return GEMM_ERR_INVALID_ARG;
   if (p.M == 0 || p.N == 0 || p.L == 0) return GEMM_OK;   // nothing to compute
 
   // Sizes the kernel indexes with 32-bit tile ids and 64-bit element offsets.
@@ -346,13 +354,13 @@ bool encode_epi(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int dt, in
   return r == CUDA_SUCCESS;
 }
 
-uint32_t make_idesc(int ab, int cg, int bn, bool a_mn, bool b_mn) {
-  // kind::f16: A/B format 0 = fp16, 1 = bf16.  kind::f8f6f4: 0 = e4m3.
-  const uint32_t fmt = (ab == GEMM_BF16) ? 1u : 0u;
+uint32_t make_idesc(int a_type, int b_type_, int cg, int bn, bool a_mn, bool b_mn) {
+  // kind::f16: format 0 = fp16, 1 = bf16.  kind::f8f6f4: 0 = e4m3, 1 = e5m2.
+  auto fmt = [](int t) { return (t == GEMM_BF16 || t == GEMM_E5M2) ? 1u : 0u; };
   uint32_t d = 0;
   d |= 1u << 4;                                   // accumulator (D) format: fp32
-  d |= fmt << 7;                                  // A format
-  d |= fmt << 10;                                 // B format
+  d |= fmt(a_type) << 7;                          // A format
+  d |= fmt(b_type_) << 10;                        // B format
   d |= (a_mn ? 1u : 0u) << 15;                    // A MN-major
   d |= (b_mn ? 1u : 0u) << 16;                    // B MN-major
   d |= (uint32_t)(bn >> 3) << 17;                 // N >> 3
@@ -606,7 +614,7 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
   kp.stages = cfg.stages;
   kp.a_mn_major = a_mn;
   kp.b_mn_major = b_mn;
-  kp.idesc = make_idesc(dtypes->ab, cfg.cta_group, cfg.tile_n, a_mn, b_mn);
+  kp.idesc = make_idesc(dtypes->ab, b_type(*dtypes), cfg.cta_group, cfg.tile_n, a_mn, b_mn);
   kp.l2_hints = (uint32_t)cfg.l2_hints;
   kp.epi_wait_ns = (uint32_t)cfg.epi_wait_ns;
   kp.inject_stall = cfg.inject_stall;
@@ -623,6 +631,7 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
   kp.epi.alpha = alpha;
   kp.epi.beta = beta;
   kp.epi.x_factor = x_factor;
+  kp.epi.relu = dtypes->epilogue == GEMM_EPI_RELU;
   kp.epi.slots = cfg.epi_slots;
   {
     const int sub = 128 * gb300::kEpiChunk;

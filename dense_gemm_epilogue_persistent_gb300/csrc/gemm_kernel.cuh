@@ -61,6 +61,7 @@ struct EpiParams {
   int cd_m_major;            // 0: (l*M + m)*N + n   1: (l*N + n)*M + m
   int read_c, read_x, write_y;
   float alpha, beta, x_factor;
+  int relu;                  // D = max(alpha*acc + beta*C, 0) + x_factor*X
   int slots;                 // epilogue shared-memory slots (>= 2)
   uint32_t cd_bytes;         // bytes of a slot's C/D region
   uint32_t xy_bytes;         // bytes of a slot's X/Y region (0: neither X nor Y)
@@ -521,7 +522,10 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           const float c = e.read_c ? cv[i] : 0.f;
           const float x = e.read_x ? xv[i] : 0.f;
           yv[i] = a;
-          dv[i] = fmaf(e.alpha, a, fmaf(e.beta, c, e.x_factor * x));
+          if (e.relu)
+            dv[i] = fmaf(e.x_factor, x, fmaxf(fmaf(e.alpha, a, e.beta * c), 0.f));
+          else
+            dv[i] = fmaf(e.alpha, a, fmaf(e.beta, c, e.x_factor * x));
         }
         smem_write_row(slot, e.d_dt, e.cd_m_major, r, dv);
         if (e.write_y) smem_write_row(slot + e.cd_bytes, e.y_dt, e.cd_m_major, r, yv);

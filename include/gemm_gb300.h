@@ -57,16 +57,31 @@ typedef enum {
   GEMM_ERR_UNSUPPORTED_CONFIG = 7  /* a forced kernel configuration cannot run this problem */
 } gemm_status_t;
 
-typedef enum { GEMM_F32 = 0, GEMM_F16 = 1, GEMM_BF16 = 2, GEMM_E4M3 = 3 } gemm_dtype_t;
+typedef enum {
+  GEMM_F32 = 0, GEMM_F16 = 1, GEMM_BF16 = 2, GEMM_E4M3 = 3, GEMM_E5M2 = 4
+} gemm_dtype_t;
+
+/* Epilogue variants ("custom_epilogue_dense_gemm.py": the docstring's linear
+ * form, and the relu its epilogue() function applies before X is added). */
+typedef enum {
+  GEMM_EPI_LINEAR = 0,   /* D = alpha*acc + beta*C + x_factor*X */
+  GEMM_EPI_RELU = 1      /* D = max(alpha*acc + beta*C, 0) + x_factor*X */
+} gemm_epilogue_t;
 
 typedef enum { GEMM_K_MAJOR = 0, GEMM_MN_MAJOR = 1 } gemm_layout_t;
 
-/* Element types.  ab: F16, BF16 or E4M3 (A and B share it).  c, x: F32, F16
- * or BF16 (inputs).  d, y: F32, F16 or BF16 (outputs).  cdxy_major: the one
- * major order of C, D, X and Y. */
+/* Per-call descriptor of types and epilogue.
+ *   ab: A's type, F16, BF16, E4M3 or E5M2 (and B's, unless b is set).
+ *   c, x: F32, F16 or BF16 (inputs).  d, y: F32, F16 or BF16 (outputs).
+ *   cdxy_major: the one major order of C, D, X and Y.
+ *   b: B's type when it differs from A's -- only fp8 pairs (E4M3 x E5M2 in
+ *      either order, which tcgen05 kind::f8f6f4 takes); 0 (GEMM_F32) = same as ab.
+ *   epilogue: GEMM_EPI_LINEAR (0) or GEMM_EPI_RELU. */
 typedef struct {
   gemm_dtype_t ab, c, d, x, y;
   gemm_layout_t cdxy_major;
+  gemm_dtype_t b;
+  gemm_epilogue_t epilogue;
 } gemm_dtypes_t;
 
 /* Kernel configuration.  Chosen automatically per problem shape unless the

@@ -10,8 +10,8 @@ only compiles it with gcc and marshals numpy arrays.  See ``oracle.c`` for the
 definition, the page citations and the layout conventions.
 
 Type codes here are the oracle's own: ``"f32"``, ``"f16"``, ``"bf16"``,
-``"e4m3"``.  Input buffers are numpy arrays holding the raw storage
-(float32, uint16 bit patterns for f16/bf16, uint8 codes for e4m3), laid out as
+``"e4m3"``, ``"e5m2"``.  Input buffers are numpy arrays holding the raw storage
+(float32, uint16 bit patterns for f16/bf16, uint8 codes for fp8), laid out as
 ``oracle.c`` describes.  Outputs come back in logical [L, M, N] order.
 """
 from __future__ import annotations
@@ -29,8 +29,9 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-DTYPES = {"f32": 0, "f16": 1, "bf16": 2, "e4m3": 3}
-STORAGE = {"f32": np.float32, "f16": np.uint16, "bf16": np.uint16, "e4m3": np.uint8}
+DTYPES = {"f32": 0, "f16": 1, "bf16": 2, "e4m3": 3, "e5m2": 4}
+STORAGE = {"f32": np.float32, "f16": np.uint16, "bf16": np.uint16, "e4m3": np.uint8,
+           "e5m2": np.uint8}
 
 
 def build(force: bool = False) -> str:
@@ -59,7 +60,7 @@ def _load():
             lib.oracle_round.restype = None
             lib.oracle_round.argtypes = [i32, vp, i64, vp]
             common = [i64, i64, i64, i64, vp, i64, i32, vp, i64, i32, vp, vp, i32, i32, i32, i32,
-                      f64, f64, f64, i32, i32]
+                      i32, f64, f64, f64, i32, i32, i32]
             lib.oracle_gemm_rows.restype = i32
             lib.oracle_gemm_rows.argtypes = common + [i64, i64, vp, vp, vp, i32]
             lib.oracle_gemm_entries.restype = i32
@@ -97,11 +98,14 @@ class Problem:
     b_mn_major: B stored N-major ([L][K][ldb]) instead of K-major ([L][N][ldb]).
     cd_m_major: C/X stored M-major ([L][N][M]) instead of N-major ([L][M][N]).
     use_c / use_x: whether beta*C / x_factor*X take part (C, X may be None).
+    b_dtype: B's type when it differs from A's (fp8 pairs); None = ab_dtype.
+    relu: D = max(alpha*acc + beta*C, 0) + x_factor*X.
     """
 
     def __init__(self, M, N, K, L, A, lda, a_mn_major, B, ldb, b_mn_major, C, X,
                  ab_dtype, c_dtype="f32", x_dtype="f32", cd_m_major=False,
-                 alpha=1.0, beta=0.0, x_factor=0.0, use_c=None, use_x=None):
+                 alpha=1.0, beta=0.0, x_factor=0.0, use_c=None, use_x=None, b_dtype=None,
+                 relu=False):
         self.M, self.N, self.K, self.L = int(M), int(N), int(K), int(L)
         self.A = None if A is None else np.ascontiguousarray(A)
         self.B = None if B is None else np.ascontiguousarray(B)
@@ -110,6 +114,8 @@ class Problem:
         self.lda, self.ldb = int(lda), int(ldb)
         self.a_mn_major, self.b_mn_major = bool(a_mn_major), bool(b_mn_major)
         self.ab_dtype, self.c_dtype, self.x_dtype = ab_dtype, c_dtype, x_dtype
+        self.b_dtype = ab_dtype if b_dtype is None else b_dtype
+        self.relu = bool(relu)
         self.cd_m_major = bool(cd_m_major)
         self.alpha, self.beta, self.x_factor = float(alpha), float(beta), float(x_factor)
         self.use_c = (self.C is not None and self.beta != 0.0) if use_c is None else bool(use_c)
@@ -119,9 +125,9 @@ class Problem:
         ptr = lambda a: None if a is None else a.ctypes.data
         return [self.M, self.N, self.K, self.L, ptr(self.A), self.lda, int(self.a_mn_major),
                 ptr(self.B), self.ldb, int(self.b_mn_major), ptr(self.C), ptr(self.X),
-                DTYPES[self.ab_dtype], DTYPES[self.c_dtype], DTYPES[self.x_dtype],
-                int(self.cd_m_major), self.alpha, self.beta, self.x_factor,
-                int(self.use_c), int(self.use_x)]
+                DTYPES[self.ab_dtype], DTYPES[self.b_dtype], DTYPES[self.c_dtype],
+                DTYPES[self.x_dtype], int(self.cd_m_major), self.alpha, self.beta, self.x_factor,
+                int(self.use_c), int(self.use_x), int(self.relu)]
 
 
 def gemm_rows(p: Problem, m0: int = 0, m1: int | None = None, nthreads: int = 0):

@@ -10,6 +10,7 @@
  *   acc(m,n,l) = sum_{k=0}^{K-1} A(m,k,l) * B(n,k,l)          (B is N x K)
  *   Y(m,n,l)   = acc(m,n,l)
  *   D(m,n,l)   = alpha * acc(m,n,l) + beta * C(m,n,l) + x_factor * X(m,n,l)
+ *   relu variant: D = max(alpha * acc + beta * C, 0) + x_factor * X
  *
  * Sources:
  *   - "04_mma_tma_2sm_sm100.cu" (CUTLASS CuTe Blackwell tutorial 04), header
@@ -22,7 +23,7 @@
  *     docstring omits -- this oracle follows the docstring (no relu).
  *
  * Arithmetic: every input is decoded exactly to double (fp16, bf16, fp32 and
- * OCP FP8 E4M3 all embed exactly in binary64), the dot product is summed in
+ * OCP FP8 E4M3/E5M2 all embed exactly in binary64; A and B may differ in type), the dot product is summed in
  * double in increasing k, the epilogue is evaluated in double, and results
  * are rounded once, round-to-nearest-even, to the output format.  The sum
  * of |a*b| is returned too: it scales the comparison bound.
@@ -44,7 +45,7 @@
 #endif
 
 /* Type codes of this oracle (its own numbering). */
-enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2, OR_E4M3 = 3 };
+enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2, OR_E4M3 = 3, OR_E5M2 = 4 };
 
 /* ---------------------------------------------------------------- decoders */
 
@@ -88,6 +89,21 @@ static double decode_e4m3(uint32_t b) {
   return s ? -v : v;
 }
 
+/* OCP 8-bit floating point, E5M2 variant: 1 sign, 5 exponent (bias 15),
+ * 2 mantissa bits; IEEE-like: exponent 31 is infinity (mantissa 0) or NaN;
+ * subnormals m/4 * 2^(1-15). */
+static double decode_e5m2(uint32_t b) {
+  int s = (b >> 7) & 1, e = (b >> 2) & 0x1F, f = b & 0x3;
+  double v;
+  if (e == 0)
+    v = ldexp((double)f, -16);               /* subnormal: f/4 * 2^-14 */
+  else if (e == 31)
+    v = f ? NAN : INFINITY;
+  else
+    v = ldexp(1.0 + f / 4.0, e - 15);
+  return s ? -v : v;
+}
+
 static double decode_f32(uint32_t w) {
   float f;
   memcpy(&f, &w, 4);
@@ -100,13 +116,14 @@ static int elem_bytes(int dt) {
     case OR_F16: return 2;
     case OR_BF16: return 2;
     case OR_E4M3: return 1;
+    case OR_E5M2: return 1;
   }
   return 0;
 }
 
 /* Decoded value of every 16-bit and 8-bit code, filled once from the
  * decoders above (a cache of the same function, nothing more). */
-static double tab_f16[65536], tab_bf16[65536], tab_e4m3[256];
+static double tab_f16[65536], tab_bf16[65536], tab_e4m3[256], tab_e5m2[256];
 static int tabs_ready = 0;
 
 static void build_tables(void) {
@@ -119,7 +136,10 @@ static void build_tables(void) {
         tab_f16[c] = decode_f16(c);
         tab_bf16[c] = decode_bf16(c);
       }
-      for (uint32_t c = 0; c < 256; ++c) tab_e4m3[c] = decode_e4m3(c);
+      for (uint32_t c = 0; c < 256; ++c) {
+        tab_e4m3[c] = decode_e4m3(c);
+        tab_e5m2[c] = decode_e5m2(c);
+      }
       tabs_ready = 1;
     }
   }
@@ -132,6 +152,7 @@ static double load_elem(const void* p, int dt, int64_t idx) {
     case OR_F16: return tab_f16[((const uint16_t*)p)[idx]];
     case OR_BF16: return tab_bf16[((const uint16_t*)p)[idx]];
     case OR_E4M3: return tab_e4m3[((const uint8_t*)p)[idx]];
+    case OR_E5M2: return tab_e5m2[((const uint8_t*)p)[idx]];
   }
   return NAN;
 }
@@ -142,6 +163,7 @@ double oracle_decode(int dt, uint32_t code) {
     case OR_F16: return decode_f16(code & 0xFFFF);
     case OR_BF16: return decode_bf16(code & 0xFFFF);
     case OR_E4M3: return decode_e4m3(code & 0xFF);
+    case OR_E5M2: return decode_e5m2(code & 0xFF);
   }
   return NAN;
 }
@@ -209,9 +231,9 @@ typedef struct {
   const void* A; int64_t lda; int a_mn_major;
   const void* B; int64_t ldb; int b_mn_major;
   const void* C; const void* X;
-  int ab_dt, c_dt, x_dt, cd_m_major;
+  int a_dt, b_dt, c_dt, x_dt, cd_m_major;
   double alpha, beta, xf;
-  int use_c, use_x;
+  int use_c, use_x, relu;
 } oracle_problem;
 
 static int64_t a_index(const oracle_problem* p, int64_t m, int64_t k, int64_t l) {
@@ -229,13 +251,16 @@ static void entry(const oracle_problem* p, int64_t m, int64_t n, int64_t l,
                   const double* arow, double* d, double* y, double* s) {
   double acc = 0.0, sabs = 0.0;
   for (int64_t k = 0; k < p->K; ++k) {
-    double a = arow ? arow[k] : load_elem(p->A, p->ab_dt, a_index(p, m, k, l));
-    double b = load_elem(p->B, p->ab_dt, b_index(p, n, k, l));
+    double a = arow ? arow[k] : load_elem(p->A, p->a_dt, a_index(p, m, k, l));
+    double b = load_elem(p->B, p->b_dt, b_index(p, n, k, l));
     acc += a * b;
     sabs += fabs(a * b);
   }
   double dv = p->alpha * acc;
   if (p->use_c) dv += p->beta * load_elem(p->C, p->c_dt, cd_index(p, m, n, l));
+  /* relu variant ("custom_epilogue_dense_gemm.py", epilogue() function):
+   * the rectifier applies to alpha*acc + beta*C, before X is added. */
+  if (p->relu && dv < 0.0) dv = 0.0;
   if (p->use_x) dv += p->xf * load_elem(p->X, p->x_dt, cd_index(p, m, n, l));
   *d = dv;
   *y = acc;
@@ -244,32 +269,34 @@ static void entry(const oracle_problem* p, int64_t m, int64_t n, int64_t l,
 
 static void fill_problem(oracle_problem* p, int64_t M, int64_t N, int64_t K, int64_t L,
                          const void* A, int64_t lda, int a_mn, const void* B, int64_t ldb,
-                         int b_mn, const void* C, const void* X, int ab_dt, int c_dt,
+                         int b_mn, const void* C, const void* X, int a_dt, int b_dt, int c_dt,
                          int x_dt, int cd_m_major, double alpha, double beta, double xf,
-                         int use_c, int use_x) {
+                         int use_c, int use_x, int relu) {
   p->M = M; p->N = N; p->K = K; p->L = L;
   p->A = A; p->lda = lda; p->a_mn_major = a_mn;
   p->B = B; p->ldb = ldb; p->b_mn_major = b_mn;
   p->C = C; p->X = X;
-  p->ab_dt = ab_dt; p->c_dt = c_dt; p->x_dt = x_dt; p->cd_m_major = cd_m_major;
+  p->a_dt = a_dt; p->b_dt = b_dt; p->c_dt = c_dt; p->x_dt = x_dt; p->cd_m_major = cd_m_major;
   p->alpha = alpha; p->beta = beta; p->xf = xf;
   p->use_c = use_c && C != NULL;
   p->use_x = use_x && X != NULL;
+  p->relu = relu;
 }
 
 /* Rows [m0, m1) of every batch, all columns.  D, Y, S are [L][m1-m0][N]
  * (S may be NULL).  Returns 0, or -1 on a bad argument. */
 int oracle_gemm_rows(int64_t M, int64_t N, int64_t K, int64_t L,
                      const void* A, int64_t lda, int a_mn, const void* B, int64_t ldb, int b_mn,
-                     const void* C, const void* X, int ab_dt, int c_dt, int x_dt, int cd_m_major,
-                     double alpha, double beta, double xf, int use_c, int use_x,
-                     int64_t m0, int64_t m1, double* D, double* Y, double* S, int nthreads) {
+                     const void* C, const void* X, int a_dt, int b_dt, int c_dt, int x_dt,
+                     int cd_m_major, double alpha, double beta, double xf, int use_c, int use_x,
+                     int relu, int64_t m0, int64_t m1, double* D, double* Y, double* S,
+                     int nthreads) {
   if (M < 0 || N < 0 || K < 0 || L < 0 || m0 < 0 || m1 > M || m0 > m1) return -1;
-  if (elem_bytes(ab_dt) == 0) return -1;
+  if (elem_bytes(a_dt) == 0 || elem_bytes(b_dt) == 0) return -1;
   build_tables();
   oracle_problem p;
-  fill_problem(&p, M, N, K, L, A, lda, a_mn, B, ldb, b_mn, C, X, ab_dt, c_dt, x_dt, cd_m_major,
-               alpha, beta, xf, use_c, use_x);
+  fill_problem(&p, M, N, K, L, A, lda, a_mn, B, ldb, b_mn, C, X, a_dt, b_dt, c_dt, x_dt,
+               cd_m_major, alpha, beta, xf, use_c, use_x, relu);
   int64_t rows = m1 - m0;
 #ifdef _OPENMP
   if (nthreads > 0) omp_set_num_threads(nthreads);
@@ -282,7 +309,7 @@ int oracle_gemm_rows(int64_t M, int64_t N, int64_t K, int64_t L,
 #endif
     for (int64_t lm = 0; lm < L * rows; ++lm) {
       int64_t l = lm / rows, m = m0 + lm % rows;
-      for (int64_t k = 0; k < K; ++k) arow[k] = load_elem(A, ab_dt, a_index(&p, m, k, l));
+      for (int64_t k = 0; k < K; ++k) arow[k] = load_elem(A, a_dt, a_index(&p, m, k, l));
       for (int64_t n = 0; n < N; ++n) {
         int64_t o = (l * rows + (m - m0)) * N + n;
         entry(&p, m, n, l, arow, &D[o], &Y[o], S ? &S[o] : NULL);
@@ -296,17 +323,17 @@ int oracle_gemm_rows(int64_t M, int64_t N, int64_t K, int64_t L,
 /* Selected entries (ms[i], ns[i], ls[i]), i < count. */
 int oracle_gemm_entries(int64_t M, int64_t N, int64_t K, int64_t L,
                         const void* A, int64_t lda, int a_mn, const void* B, int64_t ldb, int b_mn,
-                        const void* C, const void* X, int ab_dt, int c_dt, int x_dt,
+                        const void* C, const void* X, int a_dt, int b_dt, int c_dt, int x_dt,
                         int cd_m_major, double alpha, double beta, double xf, int use_c, int use_x,
-                        const int64_t* ms, const int64_t* ns, const int64_t* ls, int64_t count,
-                        double* D, double* Y, double* S, int nthreads) {
-  if (elem_bytes(ab_dt) == 0) return -1;
+                        int relu, const int64_t* ms, const int64_t* ns, const int64_t* ls,
+                        int64_t count, double* D, double* Y, double* S, int nthreads) {
+  if (elem_bytes(a_dt) == 0 || elem_bytes(b_dt) == 0) return -1;
   for (int64_t i = 0; i < count; ++i)
     if (ms[i] < 0 || ms[i] >= M || ns[i] < 0 || ns[i] >= N || ls[i] < 0 || ls[i] >= L) return -1;
   build_tables();
   oracle_problem p;
-  fill_problem(&p, M, N, K, L, A, lda, a_mn, B, ldb, b_mn, C, X, ab_dt, c_dt, x_dt, cd_m_major,
-               alpha, beta, xf, use_c, use_x);
+  fill_problem(&p, M, N, K, L, A, lda, a_mn, B, ldb, b_mn, C, X, a_dt, b_dt, c_dt, x_dt,
+               cd_m_major, alpha, beta, xf, use_c, use_x, relu);
 #ifdef _OPENMP
   if (nthreads > 0) omp_set_num_threads(nthreads);
 #pragma omp parallel for schedule(dynamic, 16)

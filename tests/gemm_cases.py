@@ -61,19 +61,21 @@ class Case:
     seed: int = 0
     lda_pad: int = 0
     ldb_pad: int = 0
+    b: str | None = None      # B's type when it differs from A's (fp8 pairs)
+    relu: bool = False
 
     @staticmethod
     def from_workload(w: W.Workload, **over):
         kw = dict(M=w.M, N=w.N, K=w.K, L=w.L, ab=w.ab, c=w.c, d=w.d, x=w.x, y=w.y,
                   a_mn=w.a_mn_major, b_mn=w.b_mn_major, cd_m=w.cd_m_major, alpha=w.alpha,
-                  beta=w.beta, xf=w.x_factor, dist=w.dist, seed=w.seed)
+                  beta=w.beta, xf=w.x_factor, dist=w.dist, seed=w.seed, b=w.b, relu=w.relu)
         kw.update(over)
         return Case(**kw)
 
     def workload(self) -> W.Workload:
         return W.Workload("case", self.M, self.N, self.K, self.L, self.ab, self.a_mn, self.b_mn,
                           self.c, self.d, self.x, self.y, self.cd_m, self.alpha, self.beta,
-                          self.xf, self.seed, self.dist)
+                          self.xf, self.seed, self.dist, self.b, self.relu)
 
 
 def _pad_ld(t: torch.Tensor, pad: int) -> torch.Tensor:
@@ -121,7 +123,8 @@ def run_gpu(gemm: G.Gemm, prep: Prepared, stream=None, D=None, Y=None, use_x=Tru
     if Y is None and c.y is not None:
         Y = torch.empty(out_shape(c), dtype=W.TORCH_DTYPE[c.y], device=dev)
     dt = G.make_dtypes(c.ab, c.c or "f32", c.d, c.x or "f32", c.y or "f32",
-                       G.GEMM_MN_MAJOR if c.cd_m else G.GEMM_K_MAJOR)
+                       G.GEMM_MN_MAJOR if c.cd_m else G.GEMM_K_MAJOR, b=c.b,
+                       epilogue=G.GEMM_EPI_RELU if c.relu else G.GEMM_EPI_LINEAR)
     gemm.run(c.M, c.N, c.K, c.L, A, A.shape[-1], int(c.a_mn), B, B.shape[-1], int(c.b_mn),
              C, X, D, Y, c.alpha, c.beta, c.xf, dt, stream)
     return D, Y
@@ -134,7 +137,8 @@ def oracle_problem(prep: Prepared, use_x=True) -> oracle.Problem:
                           st(prep.B), prep.B.shape[-1], c.b_mn,
                           st(prep.C) if prep.C is not None else None,
                           st(prep.X) if (prep.X is not None and use_x) else None,
-                          c.ab, c.c or "f32", c.x or "f32", c.cd_m, c.alpha, c.beta, c.xf)
+                          c.ab, c.c or "f32", c.x or "f32", c.cd_m, c.alpha, c.beta, c.xf,
+                          b_dtype=c.b, relu=c.relu)
 
 
 def logical(t: torch.Tensor, cd_m: bool) -> torch.Tensor:

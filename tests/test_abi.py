@@ -110,6 +110,17 @@ def test_check_rejects(lib, kw, code):
     assert G.gemm_check(_p(**kw)) == code
 
 
+def test_check_fp8_pairs_and_epilogue(lib):
+    dt = lambda **kw: G.make_dtypes("e4m3", "f16", "f16", **kw)
+    assert G.gemm_check(_p(dtypes=dt(b="e5m2"))) == G.GEMM_OK
+    assert G.gemm_check(_p(dtypes=G.make_dtypes("e5m2", "f16", "f16", b="e4m3"))) == 0
+    assert G.gemm_check(_p(dtypes=G.make_dtypes("f16", "f16", "f16", b="bf16"))) == \
+        G.GEMM_ERR_UNSUPPORTED_DTYPE                       # only fp8 types may differ
+    assert G.gemm_check(_p(dtypes=dt(b="f16"))) == G.GEMM_ERR_UNSUPPORTED_DTYPE
+    assert G.gemm_check(_p(dtypes=dt(epilogue=G.GEMM_EPI_RELU))) == G.GEMM_OK
+    assert G.gemm_check(_p(dtypes=dt(epilogue=7))) == G.GEMM_ERR_INVALID_ARG
+
+
 def test_check_e4m3_alignment(lib):
     dt = G.make_dtypes("e4m3", "f16", "f16")
     assert G.gemm_check(_p(K=4096, lda=4096, ldb=4096, N=5000, M=3000, dtypes=dt)) == 0
@@ -159,7 +170,8 @@ def test_plan_every_workload(lib, name):
     lda = w.M if w.a_mn_major else w.K
     ldb = w.N if w.b_mn_major else w.K
     dt = G.make_dtypes(w.ab, w.c or "f32", w.d, w.x or "f32", w.y or "f32",
-                       G.GEMM_MN_MAJOR if w.cd_m_major else G.GEMM_K_MAJOR)
+                       G.GEMM_MN_MAJOR if w.cd_m_major else G.GEMM_K_MAJOR, b=w.b,
+                       epilogue=G.GEMM_EPI_RELU if w.relu else G.GEMM_EPI_LINEAR)
     p = _p(M=w.M, N=w.N, K=w.K, L=w.L, lda=lda, ldb=ldb, layoutA=int(w.a_mn_major),
            layoutB=int(w.b_mn_major), alpha=w.alpha, beta=w.beta, x_factor=w.x_factor,
            dtypes=dt, C=C16 if w.c else None)
@@ -167,7 +179,7 @@ def test_plan_every_workload(lib, name):
     st, cfg = G.gemm_plan(p, 152, 232448)
     assert st == G.GEMM_OK
     assert cfg.cta_group in (1, 2) and cfg.tile_n in (128, 256)
-    atom_k = 128 if w.ab == "e4m3" else 64            # K of one 128-byte swizzle atom
+    atom_k = 128 if w.ab in ("e4m3", "e5m2") else 64  # K of one 128-byte swizzle atom
     k_atoms = 1 if (cfg.cta_group, cfg.tile_n) == (1, 256) else 2
     assert cfg.tile_k == atom_k * k_atoms
     assert 2 <= cfg.stages and cfg.smem_bytes <= 232448

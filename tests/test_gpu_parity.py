@@ -161,6 +161,40 @@ def test_layout_equivalence_bitwise(gemm):
                     assert torch.equal(base[0], out[0]) and torch.equal(base[1], out[1])
 
 
+# ------------------------------------------------------------ fp8 pairs, relu epilogue
+
+@pytest.mark.parametrize("variant", [None, (1, 256, 1), (2, 256, 1), (2, 256, 2), (1, 128, 1)])
+@pytest.mark.parametrize("a_dt,b_dt", [("e5m2", "e5m2"), ("e4m3", "e5m2"), ("e5m2", "e4m3")])
+@pytest.mark.parametrize("relu", [False, True])
+def test_fp8_pairs_and_relu(gemm, variant, a_dt, b_dt, relu):
+    """E5M2 inputs, mixed E4M3 x E5M2 pairs (tcgen05 kind::f8f6f4 with two
+    operand formats) and the relu epilogue, on ragged shapes."""
+    if variant:
+        _force(gemm, *variant)
+    else:
+        gemm.set_config(None)
+    case = Case(M=700, N=520, K=400, L=2, ab=a_dt, b=None if b_dt == a_dt else b_dt, c="f16",
+                d="f16", x="bf16", y="f32", alpha=0.25, beta=1.0, xf=0.5, relu=relu,
+                dist="e4m3_pm4", seed=61)
+    prep = prepare(case)
+    D, Y = run_gpu(gemm, prep)
+    _finish(gemm)
+    compare_full(prep, D, Y)
+    gemm.set_config(None)
+
+
+@pytest.mark.parametrize("layouts", [(True, True, True), (False, True, False)])
+def test_fp8_pair_mn_major(gemm, layouts):
+    a_mn, b_mn, cd_m = layouts
+    case = Case(M=512, N=512, K=256, L=1, ab="e5m2", b="e4m3", c="f32", d="bf16", a_mn=a_mn,
+                b_mn=b_mn, cd_m=cd_m, alpha=1.0, beta=-0.5, relu=True, dist="e4m3_pm4", seed=63)
+    gemm.set_config(None)
+    prep = prepare(case)
+    D, Y = run_gpu(gemm, prep)
+    _finish(gemm)
+    compare_full(prep, D, Y)
+
+
 # ------------------------------------------------------------ edge cases
 
 @pytest.mark.parametrize("M,N,K,L", [(8, 8, 16, 1), (1, 8, 16, 1), (129, 136, 72, 1),
@@ -268,7 +302,7 @@ def test_streams_and_repeat_determinism(gemm):
 # ------------------------------------------------------------ full-size workloads
 
 FULL = ["gemm2048_bf16_f32", "efc8192_f16", "gemm8192_bf16", "batched16_bf16_mn",
-        "ragged_e4m3_f16"]
+        "ragged_e4m3_f16", "e5m2_4096_f16", "fp8mix_relu_4096"]
 
 
 @pytest.mark.parametrize("name", FULL)

@@ -26,7 +26,8 @@ def _storage(t):
 
 
 def _problem(A, B, C=None, X=None, *, ab="f16", c="f32", x="f32", a_mn=False, b_mn=False,
-             cd_m=False, alpha=1.0, beta=0.0, xf=0.0, use_c=None, use_x=None, lda=None, ldb=None):
+             cd_m=False, alpha=1.0, beta=0.0, xf=0.0, use_c=None, use_x=None, lda=None, ldb=None,
+             b=None, relu=False):
     """Build an oracle Problem from LOGICAL torch tensors A [L,M,K], B [L,N,K],
     C/X [L,M,N] (storage dtypes), laying them out as requested."""
     L, M, K = A.shape
@@ -42,12 +43,12 @@ def _problem(A, B, C=None, X=None, *, ab="f16", c="f32", x="f32", a_mn=False, b_
     Cs = None if C is None else _storage(W.to_storage(C, cd_m))
     Xs = None if X is None else _storage(W.to_storage(X, cd_m))
     return oracle.Problem(M, N, K, L, _storage(As), As.shape[2], a_mn, _storage(Bs), Bs.shape[2],
-                          b_mn, Cs, Xs, ab, c, x, cd_m, alpha, beta, xf, use_c, use_x)
+                          b_mn, Cs, Xs, ab, c, x, cd_m, alpha, beta, xf, use_c, use_x, b, relu)
 
 
-def _f64(t):
-    if t.dtype == torch.uint8:   # e4m3 codes
-        return t.view(torch.float8_e4m3fn).double()
+def _f64(t, fp8="e4m3"):
+    if t.dtype == torch.uint8:   # fp8 codes
+        return t.view(torch.float8_e4m3fn if fp8 == "e4m3" else torch.float8_e5m2).double()
     return t.double()
 
 
@@ -85,6 +86,28 @@ def test_decode_e4m3_matches_torch_and_ocp_points():
     assert np.isnan(got[0x7F]) and np.isnan(got[0xFF])          # the only NaNs
     assert got[0x38] == 1.0 and got[0x48] == 4.0
     assert np.isnan(got).sum() == 2
+
+
+def test_decode_e5m2_matches_torch_and_ocp_points():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e5m2).double().numpy()
+    got = oracle.decode("e5m2", codes)
+    np.testing.assert_array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    np.testing.assert_array_equal(got[ok], ref[ok])
+    # Points fixed by the OCP FP8 definition (E5M2: bias 15, IEEE-like specials).
+    assert got[0x7B] == 57344.0                                 # largest finite
+    assert got[0x04] == 2.0 ** -14 and got[0x01] == 2.0 ** -16  # smallest normal / subnormal
+    assert got[0x7C] == np.inf and got[0xFC] == -np.inf
+    assert np.isnan(got[[0x7D, 0x7E, 0x7F, 0xFD, 0xFE, 0xFF]]).all() and np.isnan(got).sum() == 6
+    assert got[0x3C] == 1.0 and got[0x44] == 4.0
+
+
+def test_e5m2_code_set_for_pm4_recipe():
+    codes = W.e5m2_codes_in_pm4().numpy()
+    allv = oracle.decode("e5m2", np.arange(256))
+    inside = [c for c in range(256) if np.isfinite(allv[c]) and abs(allv[c]) <= 4.0]
+    assert len(codes) == 138 and sorted(inside) == sorted(codes.tolist())
 
 
 def test_e4m3_code_set_for_pm4_recipe():
@@ -143,8 +166,8 @@ def test_round_f32_matches_numpy():
 # ---------------------------------------------------------------- the GEMM
 
 def _rand(shape, dt, gen, scale=1.0):
-    if dt == "e4m3":
-        tab = W.e4m3_codes_in_pm4()
+    if dt in ("e4m3", "e5m2"):
+        tab = W.e4m3_codes_in_pm4() if dt == "e4m3" else W.e5m2_codes_in_pm4()
         return tab[torch.randint(0, tab.numel(), shape, generator=gen)]
     return (torch.randn(shape, generator=gen) * scale).to(W.TORCH_DTYPE[dt])
 
@@ -325,3 +348,49 @@ def test_entries_and_row_blocks_agree_with_full():
     np.testing.assert_array_equal(Se, S[ls, ms, ns])
     Dr, Yr, _ = oracle.gemm_rows(p, 5, 12)
     np.testing.assert_array_equal(Dr, D[:, 5:12])
+
+
+@pytest.mark.parametrize("a_dt,b_dt", [("e5m2", "e5m2"), ("e4m3", "e5m2"), ("e5m2", "e4m3")])
+def test_fp8_pairs_match_numpy_float64_matmul(a_dt, b_dt):
+    """E5M2 and mixed E4M3 x E5M2 operands: numpy float64 matmul of the exact
+    values (decoded by torch) agrees with the oracle within fp64 error."""
+    g = torch.Generator().manual_seed(91)
+    L, M, N, K = 2, 17, 21, 40
+    A, B = _rand((L, M, K), a_dt, g), _rand((L, N, K), b_dt, g)
+    C = _rand((L, M, N), "f16", g)
+    p = _problem(A, B, C, ab=a_dt, b=b_dt, c="f16", b_mn=True, alpha=0.25, beta=1.0)
+    D, Y, S = oracle.gemm(p)
+    a, b = _f64(A, a_dt).numpy(), _f64(B, b_dt).numpy()
+    acc = np.matmul(a, b.transpose(0, 2, 1))
+    tol = 4 * K * 2.0 ** -53 * np.matmul(np.abs(a), np.abs(b).transpose(0, 2, 1)) + 1e-300
+    assert np.all(np.abs(Y - acc) <= tol)
+    assert np.all(np.abs(D - (0.25 * acc + C.double().numpy())) <= 2 * tol + 1e-12)
+
+
+def test_relu_variant_closed_forms_and_numpy():
+    """relu(alpha*acc + beta*C) + x_factor*X, the rectifier before X is added
+    ("custom_epilogue_dense_gemm.py", epilogue() function)."""
+    g = torch.Generator().manual_seed(93)
+    L, M, N, K = 1, 12, 10, 16
+    A = torch.randn(L, M, K, generator=g).to(torch.float16)
+    B = torch.randn(L, N, K, generator=g).to(torch.float16)
+    C = torch.randn(L, M, N, generator=g).to(torch.float16)
+    X = torch.randn(L, M, N, generator=g).to(torch.float16)
+    c, x = C.double().numpy(), X.double().numpy()
+    # A = 0: D = max(beta*C, 0) + x_factor*X exactly
+    D0, Y0, _ = oracle.gemm(_problem(torch.zeros_like(A), B, C, X, c="f16", x="f16", alpha=1.0,
+                                     beta=-2.0, xf=0.5, relu=True))
+    np.testing.assert_array_equal(D0, np.maximum(-2.0 * c, 0.0) + 0.5 * x)
+    assert np.all(Y0 == 0)
+    # general: numpy float64
+    D, Y, S = oracle.gemm(_problem(A, B, C, X, c="f16", x="f16", alpha=1.5, beta=0.5, xf=-1.0,
+                                   relu=True))
+    acc = np.matmul(A.double().numpy(), B.double().numpy().transpose(0, 2, 1))
+    want = np.maximum(1.5 * acc + 0.5 * c, 0.0) - x
+    assert np.all(np.abs(D - want) <= 8 * K * 2.0 ** -53 * (S + np.abs(c) + np.abs(x)))
+    # the same problem without relu differs exactly where alpha*acc + beta*C < 0
+    Dl, _, _ = oracle.gemm(_problem(A, B, C, X, c="f16", x="f16", alpha=1.5, beta=0.5, xf=-1.0))
+    neg = (1.5 * acc + 0.5 * c) < 0
+    assert neg.any() and (~neg).any()
+    np.testing.assert_array_equal(D[~neg], Dl[~neg])
+    assert np.all(D[neg] == -x[neg])

@@ -26,6 +26,9 @@ MUTANTS = {
                           "return !p->cd_m_major ? (l * p->N + n) * p->M + m : (l * p->M + m) * p->N + n;"),
     "bf16_decoder_mantissa": ("v = ldexp(1.0 + f / 128.0, e - 127);",
                               "v = ldexp(1.0 + f / 256.0, e - 127);"),
+    "e5m2_bias": ("v = ldexp(1.0 + f / 4.0, e - 15);", "v = ldexp(1.0 + f / 4.0, e - 16);"),
+    "relu_after_x": ("  if (p->relu && dv < 0.0) dv = 0.0;\n  if (p->use_x) dv += p->xf",
+                     "  if (p->use_x) dv += p->xf"),
 }
 
 

@@ -41,6 +41,12 @@ class Workload:
     x_factor: float
     seed: int
     dist: str               # see draw()
+    b: str | None = None    # B's type when it differs from A's (fp8 pairs)
+    relu: bool = False      # D = max(alpha*AB + beta*C, 0) + x_factor*X
+
+    @property
+    def b_type(self) -> str:
+        return self.b or self.ab
 
     @property
     def flops(self) -> int:
@@ -65,11 +71,18 @@ WORKLOADS = {
     "ragged_e4m3_f16": Workload("ragged_e4m3_f16", 3000, 5000, 4096, 1, "e4m3", False, False,
                                 "f16", "f16", None, None, False, 0.25, 1.0, 0.0, 4,
                                 "e4m3_pm4"),
+    # Beyond the listed shapes: E5M2 inputs, and a mixed E4M3 x E5M2 pair with
+    # the relu epilogue and an X term.
+    "e5m2_4096_f16": Workload("e5m2_4096_f16", 4096, 4096, 4096, 1, "e5m2", False, False,
+                              "f16", "f16", None, None, False, 0.25, 1.0, 0.0, 6, "e4m3_pm4"),
+    "fp8mix_relu_4096": Workload("fp8mix_relu_4096", 4096, 4096, 4096, 1, "e4m3", False, False,
+                                 "f16", "f16", "f16", None, False, 0.25, 1.0, 0.5, 7,
+                                 "e4m3_pm4", b="e5m2", relu=True),
 }
 
 TORCH_DTYPE = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16,
-               "e4m3": torch.uint8}
-ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "e4m3": 1}
+               "e4m3": torch.uint8, "e5m2": torch.uint8}
+ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "e4m3": 1, "e5m2": 1}
 
 
 def e4m3_codes_in_pm4() -> torch.Tensor:
@@ -86,6 +99,18 @@ def e4m3_codes_in_pm4() -> torch.Tensor:
     return torch.tensor(codes, dtype=torch.uint8)
 
 
+def e5m2_codes_in_pm4() -> torch.Tensor:
+    """The 138 OCP E5M2 bit patterns whose value lies in [-4, 4]: exponent
+    field <= 16 (every value below 4, both zeros, subnormals) or exponent 17
+    with a zero mantissa (exactly 4.0).  Selected by bit pattern alone."""
+    codes = []
+    for c in range(256):
+        e, f = (c >> 2) & 0x1F, c & 0x3
+        if e <= 16 or (e == 17 and f == 0):
+            codes.append(c)
+    return torch.tensor(codes, dtype=torch.uint8)
+
+
 def draw(dist: str, shape, gen: torch.Generator, out_dtype: str) -> torch.Tensor:
     """One seeded draw over a logical shape, rounded to `out_dtype` storage."""
     if dist == "int2":         # integers uniform in [-2, 2]
@@ -96,10 +121,11 @@ def draw(dist: str, shape, gen: torch.Generator, out_dtype: str) -> torch.Tensor
         v = torch.randn(shape, generator=gen, dtype=torch.float32)
     elif dist == "normal002":  # N(0, sigma=0.02)
         v = torch.randn(shape, generator=gen, dtype=torch.float32) * 0.02
-    elif dist == "e4m3_pm4":   # discrete uniform over the 146 E4M3 codes in [-4, 4]
-        table = e4m3_codes_in_pm4()
+    elif dist == "e4m3_pm4":   # discrete uniform over the fp8 codes in [-4, 4]
+        # (146 E4M3 codes or 138 E5M2 codes, by the storage type asked for)
+        table = e4m3_codes_in_pm4() if out_dtype == "e4m3" else e5m2_codes_in_pm4()
         idx = torch.randint(0, table.numel(), shape, generator=gen)
-        assert out_dtype == "e4m3"
+        assert out_dtype in ("e4m3", "e5m2")
         return table[idx]
     else:
         raise ValueError(dist)
@@ -123,7 +149,7 @@ def make_inputs(w: Workload, M=None, N=None, K=None, L=None, seed=None) -> Input
     L = w.L if L is None else L
     gen = torch.Generator("cpu").manual_seed(w.seed if seed is None else seed)
     A = draw(w.dist, (L, M, K), gen, w.ab)
-    B = draw(w.dist, (L, N, K), gen, w.ab)
+    B = draw(w.dist, (L, N, K), gen, w.b_type)
     cdist = {"e4m3_pm4": "uniform1"}.get(w.dist, w.dist)
     C = draw(cdist, (L, M, N), gen, w.c) if w.c else None
     X = draw(cdist, (L, M, N), gen, w.x) if w.x else None
