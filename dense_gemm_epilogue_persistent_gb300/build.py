@@ -22,7 +22,7 @@ BUILD = os.path.join(ROOT, "_build", "gemm_gb300")
 LIB = os.path.join(HERE, "libgemm_gb300.so")
 
 SOURCES = ["gemm_api.cu", "kern_ab16_mc1.cu", "kern_ab16_mc2.cu", "kern_ab8_mc1.cu",
-           "kern_ab8_mc2.cu"]
+           "kern_ab8_mc2.cu", "kern_ab32_mc1.cu", "kern_ab32_mc2.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler",
          "-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC]

@@ -60,7 +60,7 @@ struct gemm_handle {
   gemm_config_t forced_cfg{};
   gemm_config_t last{};
   uint64_t timeout_ns = kDefaultTimeoutNs;
-  VariantState variants[2][2][2][2];   // [ab 16/8][cta_group 1/2][tile_n 128/256][mc 1/2]
+  VariantState variants[3][2][2][2];   // [ab 16/8/32][cta_group 1/2][tile_n 128/256][mc 1/2]
   int clusters_by_size[5] = {0, 0, 0, 0, 0};   // resident clusters of 1, 2, 4 CTAs
   std::mutex mu;
 };
@@ -74,13 +74,16 @@ int dtype_bytes(int dt) {
     case GEMM_BF16: return 2;
     case GEMM_E4M3: return 1;
     case GEMM_E5M2: return 1;
+    case GEMM_TF32: return 4;
   }
   return 0;
 }
 
 bool is_epi_type(int dt) { return dt == GEMM_F32 || dt == GEMM_F16 || dt == GEMM_BF16; }
 bool is_fp8(int dt) { return dt == GEMM_E4M3 || dt == GEMM_E5M2; }
-bool is_ab_type(int dt) { return dt == GEMM_F16 || dt == GEMM_BF16 || is_fp8(dt); }
+bool is_ab_type(int dt) {
+  return dt == GEMM_F16 || dt == GEMM_BF16 || is_fp8(dt) || dt == GEMM_TF32;
+}
 // B's type: the descriptor's b when set (0 = GEMM_F32 means "same as ab").
 int b_type(const gemm_dtypes_t& t) { return t.b == GEMM_F32 ? t.ab : t.b; }
 bool is_layout(int v) { return v == GEMM_K_MAJOR || v == GEMM_MN_MAJOR; }
@@ -107,6 +110,9 @@ gemm_status_t validate(const gemm_problem_t* pp) {
   // takes E4M3 and E5M2 in any pairing).
   if (t.b != GEMM_F32 && !(is_fp8(t.ab) && is_fp8(t.b))) return GEMM_ERR_UNSUPPORTED_DTYPE;
   if (t.epilogue != GEMM_EPI_LINEAR && t.epilogue != GEMM_EPI_RELU) return GEMM_ERR_INVALID_ARG;
+  // tf32 operands are K-major only (cuBLASDx Blackwell card, "Arrangement").
+  if (t.ab == GEMM_TF32 && (p.layoutA != GEMM_K_MAJOR || p.layoutB != GEMM_K_MAJOR))
+    return GEMM_ERR_UNSUPPORTED_DTYPE;
   if (p.M == 0 || p.N == 0 || p.L == 0) return GEMM_OK;   // nothing to compute
 
   // Sizes the kernel indexes with 32-bit tile ids and 64-bit element offsets.
@@ -295,6 +301,7 @@ CUtensorMapDataType tma_type(int dt) {
   switch (dt) {
     case GEMM_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     case GEMM_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    case GEMM_TF32: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;   // raw fp32 words
     default: return CU_TENSOR_MAP_DATA_TYPE_UINT8;   // fp8: bytes, never converted
   }
 }
@@ -355,8 +362,11 @@ bool encode_epi(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int dt, in
 }
 
 uint32_t make_idesc(int a_type, int b_type_, int cg, int bn, bool a_mn, bool b_mn) {
-  // kind::f16: format 0 = fp16, 1 = bf16.  kind::f8f6f4: 0 = e4m3, 1 = e5m2.
-  auto fmt = [](int t) { return (t == GEMM_BF16 || t == GEMM_E5M2) ? 1u : 0u; };
+  // kind::f16 / kind::tf32: format 0 = fp16, 1 = bf16, 2 = tf32.
+  // kind::f8f6f4: 0 = e4m3, 1 = e5m2.
+  auto fmt = [](int t) {
+    return t == GEMM_TF32 ? 2u : (t == GEMM_BF16 || t == GEMM_E5M2) ? 1u : 0u;
+  };
   uint32_t d = 0;
   d |= 1u << 4;                                   // accumulator (D) format: fp32
   d |= fmt(a_type) << 7;                          // A format
@@ -548,7 +558,7 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
   const int csize = cfg.cta_group * cfg.cluster_m;
   const void* kern = gb300::kernel_for(ab_bytes, cfg.cta_group, cfg.tile_n, cfg.cluster_m);
   if (!kern) return GEMM_ERR_UNSUPPORTED_CONFIG;
-  VariantState& vs = h->variants[ab_bytes == 2 ? 0 : 1][cfg.cta_group - 1]
+  VariantState& vs = h->variants[ab_bytes == 2 ? 0 : ab_bytes == 1 ? 1 : 2][cfg.cta_group - 1]
                                 [cfg.tile_n == 256 ? 1 : 0][cfg.cluster_m - 1];
 
   cudaLaunchConfig_t lc{};

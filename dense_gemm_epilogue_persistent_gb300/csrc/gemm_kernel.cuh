@@ -103,7 +103,8 @@ struct Geometry {
   static constexpr int B_ATOM = BN_CTA * 128;    // bytes of one K-major B atom
   static constexpr int A_STAGE = A_ATOM * KA;    // bytes
   static constexpr int B_STAGE = B_ATOM * KA;    // bytes
-  static constexpr int UMMA_K = 32 / AB_BYTES;   // K per tcgen05.mma (32 bytes)
+  static constexpr int UMMA_K = 32 / AB_BYTES;   // K per tcgen05.mma (32 bytes: 8 tf32,
+                                                 // 16 fp16/bf16, 32 fp8)
   static constexpr int K_STEPS = BK / UMMA_K;    // instructions per stage
   static constexpr int STEPS_PER_ATOM = ATOM_K / UMMA_K;   // 4
   static constexpr int ATOM_MN = 128 / AB_BYTES; // MN extent of one MN-major swizzle atom
@@ -263,7 +264,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmY,
                        const __grid_constant__ KernelParams p) {
   using G = Geometry<CG, BN, AB_BYTES, MC>;
-  constexpr int KIND = (AB_BYTES == 1) ? 1 : 0;
+  constexpr int KIND = (AB_BYTES == 1) ? 1 : (AB_BYTES == 4 ? 2 : 0);
   constexpr bool MULTI = G::CLUSTER > 1;
 
   extern __shared__ uint8_t smem_raw[];

@@ -251,27 +251,22 @@ __device__ __forceinline__ void tc_fence_after_sync() {
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, one instruction.  KIND: 0 = kind::f16
-// (fp16/bf16 inputs), 1 = kind::f8f6f4 (8-bit float inputs).
+// (fp16/bf16 inputs), 1 = kind::f8f6f4 (8-bit float inputs), 2 = kind::tf32.
+#define GB300_UMMA(CGS, KINDS)                                                              \
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"                        \
+               "tcgen05.mma.cta_group::" CGS ".kind::" KINDS " [%0], %1, %2, %3, p;\n\t}"   \
+               :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate))
 template <int CG, int KIND>
 __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                      uint32_t idesc, uint32_t accumulate) {
-  if constexpr (CG == 1 && KIND == 0)
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-                 :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
-  else if constexpr (CG == 1 && KIND == 1)
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
-                 :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
-  else if constexpr (CG == 2 && KIND == 0)
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-                 :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
-  else
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
-                 :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+  if constexpr (CG == 1 && KIND == 0) GB300_UMMA("1", "f16");
+  else if constexpr (CG == 1 && KIND == 1) GB300_UMMA("1", "f8f6f4");
+  else if constexpr (CG == 1 && KIND == 2) GB300_UMMA("1", "tf32");
+  else if constexpr (CG == 2 && KIND == 0) GB300_UMMA("2", "f16");
+  else if constexpr (CG == 2 && KIND == 1) GB300_UMMA("2", "f8f6f4");
+  else GB300_UMMA("2", "tf32");
 }
+#undef GB300_UMMA
 
 // Arrive (once) on `bar` when every tcgen05.mma this thread issued so far has
 // completed.  MULTI: the arrival goes to the barrier at the same offset in

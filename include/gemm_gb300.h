@@ -57,8 +57,11 @@ typedef enum {
   GEMM_ERR_UNSUPPORTED_CONFIG = 7  /* a forced kernel configuration cannot run this problem */
 } gemm_status_t;
 
+/* GEMM_TF32: fp32 storage read by the tensor core at tf32 precision (10-bit
+ * mantissa; A and B must be K-major).  Values whose low 13 mantissa bits are
+ * not zero are not exact inputs: the tensor core does not see those bits. */
 typedef enum {
-  GEMM_F32 = 0, GEMM_F16 = 1, GEMM_BF16 = 2, GEMM_E4M3 = 3, GEMM_E5M2 = 4
+  GEMM_F32 = 0, GEMM_F16 = 1, GEMM_BF16 = 2, GEMM_E4M3 = 3, GEMM_E5M2 = 4, GEMM_TF32 = 5
 } gemm_dtype_t;
 
 /* Epilogue variants ("custom_epilogue_dense_gemm.py": the docstring's linear
@@ -71,7 +74,7 @@ typedef enum {
 typedef enum { GEMM_K_MAJOR = 0, GEMM_MN_MAJOR = 1 } gemm_layout_t;
 
 /* Per-call descriptor of types and epilogue.
- *   ab: A's type, F16, BF16, E4M3 or E5M2 (and B's, unless b is set).
+ *   ab: A's type, F16, BF16, E4M3, E5M2 or TF32 (and B's, unless b is set).
  *   c, x: F32, F16 or BF16 (inputs).  d, y: F32, F16 or BF16 (outputs).
  *   cdxy_major: the one major order of C, D, X and Y.
  *   b: B's type when it differs from A's -- only fp8 pairs (E4M3 x E5M2 in

@@ -29,9 +29,9 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-DTYPES = {"f32": 0, "f16": 1, "bf16": 2, "e4m3": 3, "e5m2": 4}
+DTYPES = {"f32": 0, "f16": 1, "bf16": 2, "e4m3": 3, "e5m2": 4, "tf32": 5}
 STORAGE = {"f32": np.float32, "f16": np.uint16, "bf16": np.uint16, "e4m3": np.uint8,
-           "e5m2": np.uint8}
+           "e5m2": np.uint8, "tf32": np.float32}
 
 
 def build(force: bool = False) -> str:

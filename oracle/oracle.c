@@ -45,7 +45,8 @@
 #endif
 
 /* Type codes of this oracle (its own numbering). */
-enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2, OR_E4M3 = 3, OR_E5M2 = 4 };
+/* OR_TF32: fp32 storage holding values representable in tf32; decoded like fp32. */
+enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2, OR_E4M3 = 3, OR_E5M2 = 4, OR_TF32 = 5 };
 
 /* ---------------------------------------------------------------- decoders */
 
@@ -113,6 +114,7 @@ static double decode_f32(uint32_t w) {
 static int elem_bytes(int dt) {
   switch (dt) {
     case OR_F32: return 4;
+    case OR_TF32: return 4;
     case OR_F16: return 2;
     case OR_BF16: return 2;
     case OR_E4M3: return 1;
@@ -148,7 +150,8 @@ static void build_tables(void) {
 /* Decode element `idx` of a buffer of type `dt`. */
 static double load_elem(const void* p, int dt, int64_t idx) {
   switch (dt) {
-    case OR_F32: { uint32_t w; memcpy(&w, (const char*)p + 4 * idx, 4); return decode_f32(w); }
+    case OR_F32:
+    case OR_TF32: { uint32_t w; memcpy(&w, (const char*)p + 4 * idx, 4); return decode_f32(w); }
     case OR_F16: return tab_f16[((const uint16_t*)p)[idx]];
     case OR_BF16: return tab_bf16[((const uint16_t*)p)[idx]];
     case OR_E4M3: return tab_e4m3[((const uint8_t*)p)[idx]];
@@ -159,7 +162,8 @@ static double load_elem(const void* p, int dt, int64_t idx) {
 
 double oracle_decode(int dt, uint32_t code) {
   switch (dt) {
-    case OR_F32: return decode_f32(code);
+    case OR_F32:
+    case OR_TF32: return decode_f32(code);
     case OR_F16: return decode_f16(code & 0xFFFF);
     case OR_BF16: return decode_bf16(code & 0xFFFF);
     case OR_E4M3: return decode_e4m3(code & 0xFF);

@@ -121,6 +121,15 @@ def test_check_fp8_pairs_and_epilogue(lib):
     assert G.gemm_check(_p(dtypes=dt(epilogue=7))) == G.GEMM_ERR_INVALID_ARG
 
 
+def test_check_tf32_k_major_only(lib):
+    dt = G.make_dtypes("tf32", "f32", "f32")
+    assert G.gemm_check(_p(dtypes=dt)) == G.GEMM_OK
+    assert G.gemm_check(_p(dtypes=dt, layoutA=G.GEMM_MN_MAJOR)) == G.GEMM_ERR_UNSUPPORTED_DTYPE
+    assert G.gemm_check(_p(dtypes=dt, layoutB=G.GEMM_MN_MAJOR)) == G.GEMM_ERR_UNSUPPORTED_DTYPE
+    assert G.gemm_check(_p(dtypes=dt, lda=260, ldb=260)) == G.GEMM_OK    # 1040-byte rows
+    assert G.gemm_check(_p(dtypes=dt, lda=258)) == G.GEMM_ERR_MISALIGNED
+
+
 def test_check_e4m3_alignment(lib):
     dt = G.make_dtypes("e4m3", "f16", "f16")
     assert G.gemm_check(_p(K=4096, lda=4096, ldb=4096, N=5000, M=3000, dtypes=dt)) == 0
@@ -179,7 +188,7 @@ def test_plan_every_workload(lib, name):
     st, cfg = G.gemm_plan(p, 152, 232448)
     assert st == G.GEMM_OK
     assert cfg.cta_group in (1, 2) and cfg.tile_n in (128, 256)
-    atom_k = 128 if w.ab in ("e4m3", "e5m2") else 64  # K of one 128-byte swizzle atom
+    atom_k = 128 // W.ELEM_BYTES[w.ab]                 # K of one 128-byte swizzle atom
     k_atoms = 1 if (cfg.cta_group, cfg.tile_n) == (1, 256) else 2
     assert cfg.tile_k == atom_k * k_atoms
     assert 2 <= cfg.stages and cfg.smem_bytes <= 232448

@@ -195,6 +195,35 @@ def test_fp8_pair_mn_major(gemm, layouts):
     compare_full(prep, D, Y)
 
 
+# ------------------------------------------------------------ tf32 inputs
+
+@pytest.mark.parametrize("variant", [None, (1, 256, 1), (2, 256, 1), (2, 256, 2), (1, 128, 1),
+                                     (2, 128, 1)])
+def test_tf32(gemm, variant):
+    """tf32 operands (fp32 storage of tf32 values, K-major, tcgen05 kind::tf32)."""
+    if variant:
+        _force(gemm, *variant)
+    else:
+        gemm.set_config(None)
+    case = Case(M=600, N=456, K=200, L=2, ab="tf32", c="f32", d="f32", x="f16", y="bf16",
+                alpha=1.5, beta=-1.0, xf=0.25, dist="normal1", seed=65)
+    prep = prepare(case)
+    D, Y = run_gpu(gemm, prep)
+    _finish(gemm)
+    compare_full(prep, D, Y)
+    gemm.set_config(None)
+
+
+def test_tf32_integers_exact(gemm):
+    case = Case(M=256, N=384, K=512, L=1, ab="tf32", c="f32", d="f32", y="f32", alpha=1.0,
+                beta=1.0, dist="int2", seed=67)
+    gemm.set_config(None)
+    prep = prepare(case)
+    D, Y = run_gpu(gemm, prep)
+    _finish(gemm)
+    compare_full(prep, D, Y, exact=True)
+
+
 # ------------------------------------------------------------ edge cases
 
 @pytest.mark.parametrize("M,N,K,L", [(8, 8, 16, 1), (1, 8, 16, 1), (129, 136, 72, 1),
@@ -302,7 +331,7 @@ def test_streams_and_repeat_determinism(gemm):
 # ------------------------------------------------------------ full-size workloads
 
 FULL = ["gemm2048_bf16_f32", "efc8192_f16", "gemm8192_bf16", "batched16_bf16_mn",
-        "ragged_e4m3_f16", "e5m2_4096_f16", "fp8mix_relu_4096"]
+        "ragged_e4m3_f16", "e5m2_4096_f16", "fp8mix_relu_4096", "tf32_4096_f32"]
 
 
 @pytest.mark.parametrize("name", FULL)

@@ -394,3 +394,19 @@ def test_relu_variant_closed_forms_and_numpy():
     assert neg.any() and (~neg).any()
     np.testing.assert_array_equal(D[~neg], Dl[~neg])
     assert np.all(D[neg] == -x[neg])
+
+
+def test_tf32_storage_decodes_as_fp32_and_generator_rounds_to_tf32():
+    g = torch.Generator().manual_seed(95)
+    v = torch.randn(4096, generator=g) * 10.0 ** torch.randint(-20, 20, (4096,), generator=g)
+    r = W.round_to_tf32(v)
+    bits = r.view(torch.int32)
+    assert torch.all((bits & 0x1FFF) == 0)                     # 10 fraction bits left
+    # nearest: within half a tf32 spacing, ties (constructed) to even
+    e = torch.floor(torch.log2(v.abs().double()))
+    half = torch.exp2(e - 11)
+    assert torch.all((r.double() - v.double()).abs() <= half)
+    ties = torch.tensor([1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11], dtype=torch.float32)
+    assert W.round_to_tf32(ties).tolist() == [1.0, 1.0 + 2.0 ** -9]
+    codes = bits.numpy().view(np.uint32)[:64]
+    np.testing.assert_array_equal(oracle.decode("tf32", codes), oracle.decode("f32", codes))

@@ -78,11 +78,23 @@ WORKLOADS = {
     "fp8mix_relu_4096": Workload("fp8mix_relu_4096", 4096, 4096, 4096, 1, "e4m3", False, False,
                                  "f16", "f16", "f16", None, False, 0.25, 1.0, 0.5, 7,
                                  "e4m3_pm4", b="e5m2", relu=True),
+    # tf32 inputs (fp32 storage of tf32 values), fp32 C and D
+    "tf32_4096_f32": Workload("tf32_4096_f32", 4096, 4096, 4096, 1, "tf32", False, False,
+                              "f32", "f32", None, None, False, 1.0, 1.0, 0.0, 8, "normal1"),
 }
 
 TORCH_DTYPE = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16,
-               "e4m3": torch.uint8, "e5m2": torch.uint8}
-ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "e4m3": 1, "e5m2": 1}
+               "e4m3": torch.uint8, "e5m2": torch.uint8, "tf32": torch.float32}
+ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "e4m3": 1, "e5m2": 1, "tf32": 4}
+
+
+def round_to_tf32(v: torch.Tensor) -> torch.Tensor:
+    """Round fp32 values to the nearest tf32 value (10 fraction bits, ties to
+    even), kept in fp32 storage: the tf32 inputs' storage type."""
+    bits = v.contiguous().view(torch.int32)
+    lsb = (bits >> 13) & 1
+    bits = (bits + 0xFFF + lsb) & ~0x1FFF
+    return bits.view(torch.float32)
 
 
 def e4m3_codes_in_pm4() -> torch.Tensor:
@@ -129,6 +141,8 @@ def draw(dist: str, shape, gen: torch.Generator, out_dtype: str) -> torch.Tensor
         return table[idx]
     else:
         raise ValueError(dist)
+    if out_dtype == "tf32":
+        return round_to_tf32(v)
     return v.to(TORCH_DTYPE[out_dtype])
 
 
