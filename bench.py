@@ -63,11 +63,16 @@ def load_peaks():
     return dict(FALLBACK_PEAKS, bf16_tflops_sustained=1700.0)
 
 
+# Dense tensor rate of each input type relative to bf16 (GB300 nominal:
+# fp8 4.5, bf16/fp16 2.25, tf32 1.1 PFLOP/s).
+PEAK_RATIO = {"bf16": 1.0, "f16": 1.0, "e4m3": 2.0, "e5m2": 2.0, "tf32": 1.1 / 2.25}
+
+
 def tensor_peak(peaks, ab: str, sustained=False):
-    """Dense tensor peak for the input type: fp16 runs at the bf16 rate; fp8
-    at twice it (nominal ratio 4.5 / 2.25 PFLOP/s)."""
+    """Dense tensor peak for the input type: the measured bf16 figure times
+    the nominal rate ratio of the type."""
     base = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
-    return base * (2.0 if ab in ("e4m3", "e5m2") else 1.0)
+    return base * PEAK_RATIO[ab]
 
 
 DEVICE_SOURCES = ("gemm_kernel.cuh", "ptx.cuh", "kernels.h")
@@ -480,7 +485,8 @@ def main():
     peak = tensor_peak(peaks, w.ab, sustained=sustained)
     burst = tensor_peak(peaks, w.ab, sustained=False)
     achieved = flops / (kernel_ms / 1e3) / 1e12
-    ratio_note = " x2 (fp8/bf16 nominal ratio)" if w.ab in ("e4m3", "e5m2") else ""
+    ratio_note = (f" x{PEAK_RATIO[w.ab]:.3g} ({w.ab}/bf16 nominal rate ratio)"
+                  if PEAK_RATIO[w.ab] != 1.0 else "")
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": recorded_traffic(w.name, cfg),
                 "algorithmic_flops_per_launch": flops,
