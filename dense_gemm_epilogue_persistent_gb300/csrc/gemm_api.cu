@@ -35,7 +35,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 
 constexpr uint64_t kDefaultTimeoutNs = 4000000000ull;
 constexpr int kMaxStages = 12;
-constexpr int kMaxEpiSlots = 4;
+constexpr int kMaxEpiSlots = 6;
 // Default L2 priorities: evict-first for every TMA copy (A/B loads, C/X loads,
 // D/Y stores).  Interleaved sustained sweeps on GB300 found it best or tied
 // on all five benchmark shapes (fp8 3000x5000x4096: +11% over evict-normal).
@@ -259,11 +259,22 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
     while (n < kMaxStages && total_smem(cg, bn, ab_bytes, n + 1, slots, slot) <= smem_optin) ++n;
     return n;
   };
-  int slots = forced && forced->epi_slots ? forced->epi_slots : (max_stages_for(3) >= 4 ? 3 : 2);
-  if (slots < 2 || slots > kMaxEpiSlots) return GEMM_ERR_UNSUPPORTED_CONFIG;
-  const int max_stages = max_stages_for(slots);
+  // The deepest A/B ring that still leaves two epilogue slots, then every
+  // further slot that fits: more slots let C/X loads run further ahead, which
+  // keeps the epilogue ahead of fast main loops (8-bit inputs, short K).
+  const int max_stages = max_stages_for(2);
   int stages = forced && forced->stages ? forced->stages : max_stages;
   if (stages < 2 || stages > max_stages) return GEMM_ERR_UNSUPPORTED_CONFIG;
+  int slots = 2;
+  while (slots < kMaxEpiSlots &&
+         total_smem(cg, bn, ab_bytes, stages, slots + 1, slot) <= smem_optin)
+    ++slots;
+  if (forced && forced->epi_slots) {
+    slots = forced->epi_slots;
+    if (slots < 2 || slots > kMaxEpiSlots ||
+        total_smem(cg, bn, ab_bytes, stages, slots, slot) > smem_optin)
+      return GEMM_ERR_UNSUPPORTED_CONFIG;
+  }
 
   const int64_t tiles_m = cdiv(std::max<int64_t>(p.M, 1), 128 * cg * mc);
   const int64_t tiles_n = cdiv(std::max<int64_t>(p.N, 1), bn);

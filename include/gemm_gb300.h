@@ -99,7 +99,7 @@ typedef struct {
  *   cluster_m   CTA groups per thread-block cluster, stacked along M, that share
  *               their B tile through TMA multicast: 1 or 2 (0 = automatic).  The
  *               cluster holds cta_group * cluster_m CTAs.
- *   epi_slots   (also an input) epilogue slots, 2..4 (0 = automatic).
+ *   epi_slots   (also an input) epilogue slots, 2..6 (0 = automatic).
  *   l2_hints    (also an input) L2 eviction priority of the TMA copies, 2 bits
  *               each (0 normal, 1 evict-last, 2 evict-first): bits 0-1 A/B
  *               loads, 2-3 C/X loads, 4-5 D/Y stores.  As an input it applies
