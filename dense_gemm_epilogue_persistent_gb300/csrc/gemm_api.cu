@@ -192,25 +192,41 @@ bool variant_supports(const gemm_problem_t& p, int cg, int bn, int mc) {
   return true;
 }
 
-// Relative cost of running `tiles` tiles of one variant on `sm_count` SMs:
-// waves of tiles times the time of one tile, in units of one k-block of a CTA
-// pair's 256 x 256 tile.  Fitted to sweeps of the five benchmark shapes on
-// GB300 (8192^3, 2048^3, 16 x 1024^2 x 4096, 3000 x 5000 x 4096 fp8):
-//   per k-block  2x256: 1.0   1x256: 1.13   2x128: 1.3   1x128: 0.93
-//   (128-wide tiles halve the MMA work per k-block but not the operand
-//   traffic, so L2->SM bandwidth, not the tensor pipe, sets their pace; a CTA
-//   pair halves the B traffic of each SM)
-//   fixed per tile (pipeline fill, epilogue tail): pair 17, single CTA 10.
-//   Two pairs sharing B through multicast (4-CTA cluster): 0.955 per pair-tile
-//   k-block, but fewer clusters fit the GPCs (36 of 38 on GB300), which the
-//   wave count sees through `clusters` (resident clusters of that size).
-double plan_cost(int64_t tiles, int64_t k_blocks, int cg, int mc, int bn, int64_t clusters) {
+// Relative cost of running `tiles` tiles of one variant: waves of tiles times
+// the time of one tile, in units of one 128-byte-K-atom k-block of a 128 x 256
+// per-SM tile (512 tensor cycles).  A tile takes the longer of its main loop
+// and its epilogue.  Fitted to interleaved sweeps on GB300 of the benchmark
+// shapes (8192^3, 2048^3, 16 x 1024^2 x 4096, 4096^3 fp8/tf32, 3000 x 5000 x 4096):
+//   main loop per k-block  2x256: 1.0   1x256: 1.13   2x128: 1.3   1x128: 0.93;
+//     two CTA pairs sharing B by multicast: 0.985 (fewer 4-CTA clusters fit the
+//     GPCs -- 36 of 38 on GB300 -- which the wave count sees through `clusters`);
+//   fixed per tile (pipeline fill, epilogue tail): pair 17, single CTA 10;
+//   epilogue: tile_n/32 chunks; a chunk that waits for C/X loads costs about
+//     9 units (the load latency under load) spread over the slots - 1 chunks of
+//     lookahead, a store-only chunk about 1.5.
+double plan_cost(int64_t tiles, int64_t k_blocks, int cg, int mc, int bn, int64_t clusters,
+                 bool epi_loads, int epi_slots) {
   const double waves = (double)cdiv(tiles, std::max<int64_t>(1, clusters));
   double per_kb;
-  if (bn == 256) per_kb = cg == 2 ? (mc == 2 ? 0.955 : 1.0) : 1.13;
+  if (bn == 256) per_kb = cg == 2 ? (mc == 2 ? 0.985 : 1.0) : 1.13;
   else per_kb = cg == 2 ? 1.3 : 0.93;
   const double fixed = cg == 2 ? 17.0 : 10.0;
-  return waves * ((double)k_blocks * per_kb + fixed);
+  const double main_loop = (double)k_blocks * per_kb + fixed;
+  const double chunk = epi_loads ? 9.0 / std::max(1, epi_slots - 1) : 1.5;
+  const double epilogue = (double)(bn / gb300::kEpiChunk) * chunk;
+  return waves * std::max(main_loop, epilogue);
+}
+
+// Epilogue slots the planner gives a variant: the deepest ring that leaves two
+// slots, then every further slot that fits (at most kMaxEpiSlots).
+int auto_slots(int cg, int bn, int ab_bytes, int slot, int smem_optin) {
+  int stages = 0;
+  while (stages < kMaxStages && total_smem(cg, bn, ab_bytes, stages + 1, 2, slot) <= smem_optin)
+    ++stages;
+  int slots = 2;
+  while (slots < kMaxEpiSlots && total_smem(cg, bn, ab_bytes, stages, slots + 1, slot) <= smem_optin)
+    ++slots;
+  return slots;
 }
 
 // Resident clusters of `csize` CTAs: the device's measured occupancy when
@@ -244,7 +260,9 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
         const int64_t tiles = cdiv(std::max<int64_t>(p.M, 1), 128 * a * m) *
                               cdiv(std::max<int64_t>(p.N, 1), b) * std::max<int64_t>(p.L, 1);
         const double c = plan_cost(tiles, cdiv(p.K, 128 / ab_bytes), a, m, b,
-                                   resident_clusters(sm_count, clusters_by_size, a * m));
+                                   resident_clusters(sm_count, clusters_by_size, a * m),
+                                   reads_c(p) || reads_x(p),
+                                   auto_slots(a, b, ab_bytes, epi_slot_bytes(p), smem_optin));
         if (c < best - 1e-9) { best = c; cg = a; bn = b; mc = m; }
       }
   if (!cg) return GEMM_ERR_UNSUPPORTED_CONFIG;
