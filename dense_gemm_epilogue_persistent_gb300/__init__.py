@@ -52,7 +52,7 @@ class gemm_config_t(ctypes.Structure):
                 ("grid_ctas", ctypes.c_int), ("epi_slots", ctypes.c_int),
                 ("epi_slot_bytes", ctypes.c_int), ("cluster_m", ctypes.c_int),
                 ("l2_hints", ctypes.c_int), ("epi_wait_ns", ctypes.c_int),
-                ("inject_stall", ctypes.c_int)]
+                ("inject_stall", ctypes.c_int), ("tail_split", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

@@ -204,9 +204,14 @@ bool variant_supports(const gemm_problem_t& p, int cg, int bn, int mc) {
 //   epilogue: tile_n/32 chunks; a chunk that waits for C/X loads costs about
 //     9 units (the load latency under load) spread over the slots - 1 chunks of
 //     lookahead, a store-only chunk about 1.5.
+//   a last wave split into half-width items (tail_split) costs ~0.6 of a wave
+//     (half the MMA work, but the same A traffic and stage overheads).
 double plan_cost(int64_t tiles, int64_t k_blocks, int cg, int mc, int bn, int64_t clusters,
-                 bool epi_loads, int epi_slots) {
-  const double waves = (double)cdiv(tiles, std::max<int64_t>(1, clusters));
+                 bool epi_loads, int epi_slots, bool can_split) {
+  clusters = std::max<int64_t>(1, clusters);
+  const int64_t full = tiles / clusters, rem = tiles % clusters;
+  const double waves =
+      (double)full + (rem == 0 ? 0.0 : (can_split && 2 * rem <= clusters ? 0.6 : 1.0));
   double per_kb;
   if (bn == 256) per_kb = cg == 2 ? (mc == 2 ? 0.985 : 1.0) : 1.13;
   else per_kb = cg == 2 ? 1.3 : 0.93;
@@ -215,6 +220,15 @@ double plan_cost(int64_t tiles, int64_t k_blocks, int cg, int mc, int bn, int64_
   const double chunk = epi_loads ? 9.0 / std::max(1, epi_slots - 1) : 1.5;
   const double epilogue = (double)(bn / gb300::kEpiChunk) * chunk;
   return waves * std::max(main_loop, epilogue);
+}
+
+// Whether the last wave of a variant may run as half-width items: CTA groups
+// without multicast (a cluster's groups share B), and B staged in whole
+// 128-byte atoms at half width.
+bool can_split_tail(const gemm_problem_t& p, int cg, int bn, int mc) {
+  if (mc != 1) return false;
+  const int atom = 128 / dtype_bytes(p.dtypes.ab);
+  return p.layoutB == GEMM_K_MAJOR || (bn / cg / 2) % atom == 0;
 }
 
 // Epilogue slots the planner gives a variant: the deepest ring that leaves two
@@ -262,7 +276,9 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
         const double c = plan_cost(tiles, cdiv(p.K, 128 / ab_bytes), a, m, b,
                                    resident_clusters(sm_count, clusters_by_size, a * m),
                                    reads_c(p) || reads_x(p),
-                                   auto_slots(a, b, ab_bytes, epi_slot_bytes(p), smem_optin));
+                                   auto_slots(a, b, ab_bytes, epi_slot_bytes(p), smem_optin),
+                                   can_split_tail(p, a, b, m) &&
+                                       !(forced && forced->tail_split == 1));
         if (c < best - 1e-9) { best = c; cg = a; bn = b; mc = m; }
       }
   if (!cg) return GEMM_ERR_UNSUPPORTED_CONFIG;
@@ -321,7 +337,13 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
                           smem_optin / 2 + 1024);
   c.tiles = tiles;
   const int64_t units = resident_clusters(sm_count, clusters_by_size, cg * mc);
-  c.grid_ctas = (int)(std::min<int64_t>(tiles, units) * cg * mc);
+  int64_t split = 0;
+  if (can_split_tail(p, cg, bn, mc) && !(forced && forced->tail_split == 1)) {
+    const int64_t rem = tiles % units;
+    if (rem > 0 && 2 * rem <= units) split = rem;
+  }
+  c.tail_split = (int)split;
+  c.grid_ctas = (int)(std::min<int64_t>(tiles + split, units) * cg * mc);
   *out = c;
   return GEMM_OK;
 }
@@ -539,6 +561,7 @@ GEMM_API gemm_status_t gemm_set_config(gemm_handle_t h, const gemm_config_t* cfg
       (cfg->tile_n && cfg->tile_n != 128 && cfg->tile_n != 256) || cfg->stages < 0 ||
       (cfg->cluster_m && cfg->cluster_m != 1 && cfg->cluster_m != 2) ||
       cfg->epi_slots < 0 || cfg->epi_slots > kMaxEpiSlots || cfg->epi_wait_ns < 0 ||
+      cfg->tail_split < 0 || cfg->tail_split > 1 ||
       cfg->epi_wait_ns > 1000001 ||
       cfg->stages > kMaxStages || cfg->group_m < 0)
     return GEMM_ERR_INVALID_ARG;
@@ -617,7 +640,7 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
     vs.smem_set = cfg.smem_bytes;
     vs.max_clusters = nclusters;
   }
-  const int64_t clusters = std::min<int64_t>(cfg.tiles, vs.max_clusters);
+  const int64_t clusters = std::min<int64_t>(cfg.tiles + cfg.tail_split, vs.max_clusters);
   cfg.grid_ctas = (int)(clusters * csize);
   lc.gridDim = dim3((unsigned)cfg.grid_ctas);
 
@@ -654,6 +677,10 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
   kp.a_mn_major = a_mn;
   kp.b_mn_major = b_mn;
   kp.idesc = make_idesc(dtypes->ab, b_type(*dtypes), cfg.cta_group, cfg.tile_n, a_mn, b_mn);
+  kp.idesc_half = make_idesc(dtypes->ab, b_type(*dtypes), cfg.cta_group, cfg.tile_n / 2, a_mn,
+                             b_mn);
+  kp.split_start = (int)(cfg.tiles - cfg.tail_split);
+  kp.num_items = (int)(cfg.tiles + cfg.tail_split);
   kp.l2_hints = (uint32_t)cfg.l2_hints;
   kp.epi_wait_ns = (uint32_t)cfg.epi_wait_ns;
   kp.inject_stall = cfg.inject_stall;

@@ -76,6 +76,9 @@ struct KernelParams {
   int stages;                // A/B ring depth
   int a_mn_major, b_mn_major;
   uint32_t idesc;            // tcgen05 instruction descriptor
+  int split_start;           // tiles from here on run as two half-width items (num_tiles: none)
+  int num_items;             // split_start + 2 * (num_tiles - split_start)
+  uint32_t idesc_half;       // instruction descriptor of a half-width item (N / 2)
   uint32_t epi_wait_ns;      // suspend-time hint of the epilogue's accumulator wait (0: none)
   int inject_stall;          // test only: the MMA warp first waits on a barrier nobody arrives at
   uint32_t l2_hints;         // L2 eviction priority (0 normal, 1 last, 2 first):
@@ -162,6 +165,20 @@ __device__ __forceinline__ void tile_coords(int t, const KernelParams& p, int& t
   const int rr = r - g * span;
   tm = first_m + rr % gm;
   tn = rr / gm;
+}
+
+// Work item -> tile and half.  Items below split_start are whole tiles; the
+// rest are the two half-width (tile_n / 2) halves of the last tiles, so that
+// the final, partial wave of tiles runs as a wave of half tiles.  half = -1
+// for a whole tile, else 0 or 1.
+__device__ __forceinline__ int item_tile(int it, const KernelParams& p, int& half) {
+  if (it < p.split_start) {
+    half = -1;
+    return it;
+  }
+  const int r = it - p.split_start;
+  half = r & 1;
+  return p.split_start + (r >> 1);
 }
 
 // ------------------------------------------------------------------ epilogue smem
@@ -344,11 +361,18 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+      for (int it = cluster_id; ok && it < p.num_items; it += num_clusters) {
+        int half;
+        const int t = item_tile(it, p, half);
         int tm, tn, tl;
         tile_coords(t, p, tm, tn, tl);
+        // A half-width item covers columns [half * BN/2, +BN/2) of its tile: its
+        // CTAs load full B boxes from that origin and the MMA reads their first
+        // half.
+        const int item_n = half < 0 ? BN : BN / 2;
         const int m0 = tm * G::CM + (int)grp * (G::BM * CG) + (int)rank * G::BM;
-        const int n0 = tn * BN + (int)rank * G::BN_CTA + (int)grp * G::BN_PART;
+        const int n0 = tn * BN + (half > 0 ? BN / 2 : 0) + (int)rank * (item_n / CG) +
+                       (int)grp * (item_n / CG / MC);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!wait_phase(empty0 + 8u * s, ph ^ 1u, w, kWaitProducer)) { ok = false; break; }
           const uint32_t fb = full0 + 8u * s;
@@ -397,10 +421,11 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       int s = 0, acc = 0;
       uint32_t ph = 0, aph = 0;
       bool ok = !p.inject_stall || wait_phase(never_bar, 0u, w, kWaitInjected);
-      for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+      for (int it = cluster_id; ok && it < p.num_items; it += num_clusters) {
         if (!wait_phase(tempty0 + 8u * acc, aph ^ 1u, w, kWaitMmaAcc)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        const uint32_t idesc = it < p.split_start ? p.idesc : p.idesc_half;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!wait_phase(full0 + 8u * s, ph, w, kWaitMmaFull)) { ok = false; break; }
           tc_fence_after_sync();
@@ -420,7 +445,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             const uint64_t bd = p.b_mn_major
                 ? smem_desc_sw128(sb + k * G::UMMA_K * 128, G::ATOM_BYTES, 1024)
                 : smem_desc_sw128(sb + ka * G::B_ATOM + kk * 32, 16, 1024);
-            umma<CG, KIND>(d_tmem, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
+            umma<CG, KIND>(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
           }
           umma_commit<CG, MULTI>(empty0 + 8u * s, all_mask);   // slot drained: tell every loader
           if (++s == S) { s = 0; ph ^= 1u; }
@@ -441,17 +466,31 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     const uint64_t pol_in = make_l2_policy((p.l2_hints >> 2) & 3u);
     const uint64_t pol_out = make_l2_policy((p.l2_hints >> 4) & 3u);
 
-    // Epilogue chunk c of this CTA's stream: tile ordinal c / CHUNKS, columns
-    // 32*(c % CHUNKS).. of that tile.  TMA coordinates are (column, row, batch)
-    // for row-major C/D/X/Y and (row, column, batch) for column-major ones.
+    // Epilogue chunk c of this CTA's stream: this CTA's whole-tile items come
+    // first (CHUNKS chunks each), then its half-width items (CHUNKS / 2 each).
+    // TMA coordinates are (column, row, batch) for row-major C/D/X/Y and (row,
+    // column, batch) for column-major ones.
+    const int n_whole = cluster_id < p.split_start
+                            ? (p.split_start - cluster_id + num_clusters - 1) / num_clusters
+                            : 0;
     auto chunk_origin = [&](int c, int& row0, int& col0, int& tl) -> bool {
-      const int ord = c / G::CHUNKS;
-      const int t = cluster_id + ord * num_clusters;
-      if (t >= p.num_tiles) return false;
+      int ord, j;
+      if (c < n_whole * G::CHUNKS) {
+        ord = c / G::CHUNKS;
+        j = c - ord * G::CHUNKS;
+      } else {
+        const int c2 = c - n_whole * G::CHUNKS;
+        ord = n_whole + c2 / (G::CHUNKS / 2);
+        j = c2 % (G::CHUNKS / 2);
+      }
+      const int it = cluster_id + ord * num_clusters;
+      if (it >= p.num_items) return false;
+      int half;
+      const int t = item_tile(it, p, half);
       int tm, tn;
       tile_coords(t, p, tm, tn, tl);
       row0 = tm * G::CM + (int)grp * (G::BM * CG) + (int)rank * G::BM;
-      col0 = tn * BN + (c - ord * G::CHUNKS) * kEpiChunk;
+      col0 = tn * BN + (half > 0 ? BN / 2 : 0) + j * kEpiChunk;
       return true;
     };
     auto issue_loads = [&](int c) {         // epilogue leader only
@@ -479,9 +518,13 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     uint32_t aph = 0;
     int gc = 0;                             // chunk counter of this CTA's stream
     bool ok = true;
-    for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+    for (int it = cluster_id; ok && it < p.num_items; it += num_clusters) {
+      int half;
+      const int t = item_tile(it, p, half);
       int tm, tn, tl;
       tile_coords(t, p, tm, tn, tl);
+      const int nchunks = half < 0 ? G::CHUNKS : G::CHUNKS / 2;
+      const int ncol0 = tn * BN + (half > 0 ? BN / 2 : 0);
       const bool ready = wait_phase(tfull0 + 8u * acc, aph, w, kWaitEpilogue, p.epi_wait_ns);
       __syncwarp();
       ok = named_barrier_and(kEpiBarrier, 128, ready);
@@ -490,11 +533,11 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       const int row0 = tm * G::CM + (int)grp * (G::BM * CG) + (int)rank * G::BM;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll 1
-      for (int j = 0; j < G::CHUNKS; ++j, ++gc) {
+      for (int j = 0; j < nchunks; ++j, ++gc) {
         uint32_t raw_acc[32];
         tmem_load_32cols(tbase + 32u * j, raw_acc);
         tmem_wait_ld();
-        if (j == G::CHUNKS - 1) {
+        if (j == nchunks - 1) {
           // The whole accumulator stage has been read: hand it back to the MMA warp.
           tc_fence_before_sync();
           __syncwarp();
@@ -533,7 +576,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         fence_proxy_async_smem();
         named_barrier_sync(kEpiBarrier, 128);
         if (epi_leader) {
-          const int col0 = tn * BN + j * kEpiChunk;
+          const int col0 = ncol0 + j * kEpiChunk;
           const int x0 = e.cd_m_major ? row0 : col0, x1 = e.cd_m_major ? col0 : row0;
           const uint32_t s_addr = epi0 + (uint32_t)slot_idx * slot_bytes;
           tma_store_3d(&tmD, s_addr, x0, x1, tl, pol_out);

@@ -107,6 +107,10 @@ typedef struct {
  *   epi_wait_ns (also an input) suspend-time hint, in ns, of the epilogue's
  *               wait for a finished accumulator; as an input, value + 1
  *               (0 = automatic, 1 = no hint).
+ *   tail_split  tiles of the last, partial wave run as two half-width (tile_n/2)
+ *               items each, so that wave takes about half as long; reports how
+ *               many tiles were split.  As an input: 0 = automatic (split when the
+ *               partial wave fills at most half the clusters), 1 = never.
  *   inject_stall  (input, tests of the watchdog only) non-zero: the MMA warp
  *               first waits on a barrier nothing ever arrives at, so every launch
  *               ends through the watchdog with GEMM_ERR_DEVICE_TIMEOUT (role 6 in
@@ -138,6 +142,7 @@ typedef struct {
   int l2_hints;
   int epi_wait_ns;
   int inject_stall;
+  int tail_split;
 } gemm_config_t;
 
 /* Every argument of one gemm_run call, for the host-only planning calls. */

@@ -214,3 +214,22 @@ def test_plan_forced_and_rejected(lib):
     assert st == G.GEMM_ERR_UNSUPPORTED_CONFIG
     st, cfg = G.gemm_plan(p8, 152, 232448)
     assert st == 0 and (cfg.tile_n // cfg.cta_group) % 128 == 0
+
+
+def test_plan_tail_split(lib):
+    """The last, partial wave runs as half-width items when it fills at most
+    half of the clusters."""
+    p = _p(M=8192, N=8192, K=8192, lda=8192, ldb=8192, dtypes=G.make_dtypes("f16", "f16", "f16"))
+    st, cfg = G.gemm_plan(p, 152, 232448, G.gemm_config_t(cta_group=2, tile_n=256, cluster_m=1))
+    assert st == 0 and cfg.tiles == 1024 and cfg.tail_split == 1024 % 76 == 36
+    assert cfg.grid_ctas == 152
+    st, cfg = G.gemm_plan(p, 152, 232448, G.gemm_config_t(cta_group=2, tile_n=256, cluster_m=1,
+                                                          tail_split=1))
+    assert st == 0 and cfg.tail_split == 0
+    # a partial wave more than half full is not split
+    p2 = _p(M=8192, N=6656, K=512, lda=512, ldb=512, dtypes=G.make_dtypes("f16", "f16", "f16"))
+    st, cfg = G.gemm_plan(p2, 152, 232448, G.gemm_config_t(cta_group=2, tile_n=256, cluster_m=1))
+    assert st == 0 and cfg.tiles == 32 * 26 and cfg.tiles % 76 > 38 and cfg.tail_split == 0
+    # multicast clusters share B across their groups: never split
+    st, cfg = G.gemm_plan(p, 152, 232448, G.gemm_config_t(cta_group=2, tile_n=256, cluster_m=2))
+    assert st == 0 and cfg.tail_split == 0

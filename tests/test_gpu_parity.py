@@ -161,6 +161,44 @@ def test_layout_equivalence_bitwise(gemm):
                     assert torch.equal(base[0], out[0]) and torch.equal(base[1], out[1])
 
 
+# ------------------------------------------------------------ split last wave
+
+@pytest.mark.parametrize("variant,shape", [
+    ((2, 256, 1), (2560, 2560, 192)),      # 100 tiles on 76 pairs: 24 split
+    ((1, 256, 1), (2048, 2560, 128)),      # 160 tiles on 152 CTAs: 8 split
+    ((1, 128, 1), (2048, 1280, 256)),
+    ((2, 128, 1), (2048, 1408, 128)),
+    ((2, 256, 1), (2500, 2550, 200)),      # ragged
+    ((1, 256, 1), (2000, 2560, 136)),
+])
+def test_split_last_wave(gemm, variant, shape):
+    """Tiles of the last, partial wave run as two half-width items each."""
+    M, N, K = shape
+    _force(gemm, *variant)
+    case = Case(M=M, N=N, K=K, L=1, ab="f16", c="f16", d="f16", x="bf16", y="f16", alpha=1.0,
+                beta=-0.5, xf=2.0, seed=M + N)
+    prep = prepare(case)
+    D, Y = run_gpu(gemm, prep)
+    _finish(gemm)
+    cfg = gemm.last_config()
+    assert cfg.tail_split > 0
+    compare_full(prep, D, Y)
+    gemm.set_config(None)
+
+
+@pytest.mark.parametrize("ab,b_mn", [("bf16", True), ("e4m3", False), ("tf32", False)])
+def test_split_last_wave_types_and_layouts(gemm, ab, b_mn):
+    _force(gemm, 2 if ab == "bf16" else 1, 256, 1)
+    case = Case(M=2048, N=2560, K=256, L=1, ab=ab, c="f32", d="f32", y="bf16", b_mn=b_mn,
+                alpha=0.5, beta=1.0, dist="e4m3_pm4" if ab == "e4m3" else "normal1", seed=71)
+    prep = prepare(case)
+    D, Y = run_gpu(gemm, prep)
+    _finish(gemm)
+    assert gemm.last_config().tail_split > 0
+    compare_full(prep, D, Y)
+    gemm.set_config(None)
+
+
 # ------------------------------------------------------------ fp8 pairs, relu epilogue
 
 @pytest.mark.parametrize("variant", [None, (1, 256, 1), (2, 256, 1), (2, 256, 2), (1, 128, 1)])
