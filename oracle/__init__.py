@@ -60,11 +60,11 @@ def _load():
             lib.oracle_round.restype = None
             lib.oracle_round.argtypes = [i32, vp, i64, vp]
             common = [i64, i64, i64, i64, vp, i64, i32, vp, i64, i32, vp, vp, i32, i32, i32, i32,
-                      i32, f64, f64, f64, i32, i32, i32]
+                      i32, f64, f64, f64, i32, i32, i32, i64]
             lib.oracle_gemm_rows.restype = i32
-            lib.oracle_gemm_rows.argtypes = common + [i64, i64, vp, vp, vp, i32]
+            lib.oracle_gemm_rows.argtypes = common + [i64, i64, vp, vp, vp, vp, i32]
             lib.oracle_gemm_entries.restype = i32
-            lib.oracle_gemm_entries.argtypes = common + [vp, vp, vp, i64, vp, vp, vp, i32]
+            lib.oracle_gemm_entries.argtypes = common + [vp, vp, vp, i64, vp, vp, vp, vp, i32]
             lib.oracle_max_threads.restype = i32
             lib.oracle_max_threads.argtypes = []
             _lib = lib
@@ -100,12 +100,16 @@ class Problem:
     use_c / use_x: whether beta*C / x_factor*X take part (C, X may be None).
     b_dtype: B's type when it differs from A's (fp8 pairs); None = ab_dtype.
     relu: D = max(alpha*acc + beta*C, 0) + x_factor*X.
+    acc_chunk: > 0 makes gemm_rows / gemm_entries also return P, the sum over
+        the chunk boundaries (every acc_chunk k, and k = K) of the magnitude of
+        the exact running sum: the scale of the error a half-precision
+        accumulator, rounded once per chunk, may add.  P is not part of the result.
     """
 
     def __init__(self, M, N, K, L, A, lda, a_mn_major, B, ldb, b_mn_major, C, X,
                  ab_dtype, c_dtype="f32", x_dtype="f32", cd_m_major=False,
                  alpha=1.0, beta=0.0, x_factor=0.0, use_c=None, use_x=None, b_dtype=None,
-                 relu=False):
+                 relu=False, acc_chunk=0):
         self.M, self.N, self.K, self.L = int(M), int(N), int(K), int(L)
         self.A = None if A is None else np.ascontiguousarray(A)
         self.B = None if B is None else np.ascontiguousarray(B)
@@ -116,6 +120,7 @@ class Problem:
         self.ab_dtype, self.c_dtype, self.x_dtype = ab_dtype, c_dtype, x_dtype
         self.b_dtype = ab_dtype if b_dtype is None else b_dtype
         self.relu = bool(relu)
+        self.acc_chunk = int(acc_chunk)
         self.cd_m_major = bool(cd_m_major)
         self.alpha, self.beta, self.x_factor = float(alpha), float(beta), float(x_factor)
         self.use_c = (self.C is not None and self.beta != 0.0) if use_c is None else bool(use_c)
@@ -127,33 +132,37 @@ class Problem:
                 ptr(self.B), self.ldb, int(self.b_mn_major), ptr(self.C), ptr(self.X),
                 DTYPES[self.ab_dtype], DTYPES[self.b_dtype], DTYPES[self.c_dtype],
                 DTYPES[self.x_dtype], int(self.cd_m_major), self.alpha, self.beta, self.x_factor,
-                int(self.use_c), int(self.use_x), int(self.relu)]
+                int(self.use_c), int(self.use_x), int(self.relu), self.acc_chunk]
 
 
 def gemm_rows(p: Problem, m0: int = 0, m1: int | None = None, nthreads: int = 0):
     """Exact (fp64) D, Y and sum|a*b| for rows [m0, m1) of every batch.
 
-    Returns three float64 arrays of shape [L, m1-m0, N]."""
+    Returns three float64 arrays of shape [L, m1-m0, N] -- four (P last) when
+    p.acc_chunk > 0."""
     lib = _load()
     m1 = p.M if m1 is None else int(m1)
     shape = (p.L, m1 - m0, p.N)
     D = np.empty(shape, np.float64)
     Y = np.empty(shape, np.float64)
     S = np.empty(shape, np.float64)
+    P = np.empty(shape, np.float64) if p.acc_chunk > 0 else None
     rc = lib.oracle_gemm_rows(*p._common(), int(m0), m1, D.ctypes.data, Y.ctypes.data,
-                              S.ctypes.data, int(nthreads))
+                              S.ctypes.data, None if P is None else P.ctypes.data, int(nthreads))
     if rc != 0:
         raise ValueError("oracle_gemm_rows: bad arguments")
-    return D, Y, S
+    return (D, Y, S) if P is None else (D, Y, S, P)
 
 
 def gemm(p: Problem, nthreads: int = 0):
-    """Exact D, Y and sum|a*b| for the whole problem, each [L, M, N] float64."""
+    """Exact D, Y and sum|a*b| (and P, see Problem) for the whole problem, each
+    [L, M, N] float64."""
     return gemm_rows(p, 0, p.M, nthreads)
 
 
 def gemm_entries(p: Problem, ms, ns, ls, nthreads: int = 0):
-    """Exact D, Y and sum|a*b| at the listed (m, n, l) entries (1-D arrays)."""
+    """Exact D, Y and sum|a*b| (and P, see Problem) at the listed (m, n, l)
+    entries (1-D arrays)."""
     lib = _load()
     ms = np.ascontiguousarray(ms, dtype=np.int64)
     ns = np.ascontiguousarray(ns, dtype=np.int64)
@@ -162,8 +171,10 @@ def gemm_entries(p: Problem, ms, ns, ls, nthreads: int = 0):
     D = np.empty(n, np.float64)
     Y = np.empty(n, np.float64)
     S = np.empty(n, np.float64)
+    P = np.empty(n, np.float64) if p.acc_chunk > 0 else None
     rc = lib.oracle_gemm_entries(*p._common(), ms.ctypes.data, ns.ctypes.data, ls.ctypes.data,
-                                 n, D.ctypes.data, Y.ctypes.data, S.ctypes.data, int(nthreads))
+                                 n, D.ctypes.data, Y.ctypes.data, S.ctypes.data,
+                                 None if P is None else P.ctypes.data, int(nthreads))
     if rc != 0:
         raise ValueError("oracle_gemm_entries: bad arguments")
-    return D, Y, S
+    return (D, Y, S) if P is None else (D, Y, S, P)

@@ -26,7 +26,9 @@
  * OCP FP8 E4M3/E5M2 all embed exactly in binary64; A and B may differ in type), the dot product is summed in
  * double in increasing k, the epilogue is evaluated in double, and results
  * are rounded once, round-to-nearest-even, to the output format.  The sum
- * of |a*b| is returned too: it scales the comparison bound.
+ * of |a*b| is returned too: it scales the comparison bound; so, on request,
+ * does the sum of the running sums' magnitudes at fixed chunk boundaries
+ * (the bound of a half-precision accumulator, see entry()).
  *
  * Layout conventions (element strides; ld = leading dimension):
  *   A K-major : A(m,k,l) at (l*M + m)*lda + k        (lda >= K)
@@ -238,6 +240,7 @@ typedef struct {
   int a_dt, b_dt, c_dt, x_dt, cd_m_major;
   double alpha, beta, xf;
   int use_c, use_x, relu;
+  int64_t acc_chunk;  /* > 0: also report sum_j |partial sum after chunk j| (see entry) */
 } oracle_problem;
 
 static int64_t a_index(const oracle_problem* p, int64_t m, int64_t k, int64_t l) {
@@ -250,15 +253,26 @@ static int64_t cd_index(const oracle_problem* p, int64_t m, int64_t n, int64_t l
   return p->cd_m_major ? (l * p->N + n) * p->M + m : (l * p->M + m) * p->N + n;
 }
 
-/* One output entry, straight from the definition. */
+/* One output entry, straight from the definition.
+ *
+ * With acc_chunk = c > 0 it also returns, in *pp, the sum over the chunk
+ * boundaries k = c, 2c, ... and k = K (the last, possibly shorter, chunk) of
+ * the magnitude of the exact running sum |sum_{k' < k} a*b|.  A half-precision
+ * accumulator is rounded once per tensor-core instruction, i.e. at these
+ * boundaries (the cuBLASDx Blackwell page: a `half` accumulator for `half`
+ * and fp8 inputs, one instruction consuming 16 K of 16-bit or 32 K of 8-bit
+ * inputs), and each such rounding errs by at most half an fp16 ulp of the
+ * running sum: this sum scales that part of the comparison bound.  It is not
+ * part of the result. */
 static void entry(const oracle_problem* p, int64_t m, int64_t n, int64_t l,
-                  const double* arow, double* d, double* y, double* s) {
-  double acc = 0.0, sabs = 0.0;
+                  const double* arow, double* d, double* y, double* s, double* pp) {
+  double acc = 0.0, sabs = 0.0, pabs = 0.0;
   for (int64_t k = 0; k < p->K; ++k) {
     double a = arow ? arow[k] : load_elem(p->A, p->a_dt, a_index(p, m, k, l));
     double b = load_elem(p->B, p->b_dt, b_index(p, n, k, l));
     acc += a * b;
     sabs += fabs(a * b);
+    if (p->acc_chunk > 0 && ((k + 1) % p->acc_chunk == 0 || k + 1 == p->K)) pabs += fabs(acc);
   }
   double dv = p->alpha * acc;
   if (p->use_c) dv += p->beta * load_elem(p->C, p->c_dt, cd_index(p, m, n, l));
@@ -269,13 +283,14 @@ static void entry(const oracle_problem* p, int64_t m, int64_t n, int64_t l,
   *d = dv;
   *y = acc;
   if (s) *s = sabs;
+  if (pp) *pp = pabs;
 }
 
 static void fill_problem(oracle_problem* p, int64_t M, int64_t N, int64_t K, int64_t L,
                          const void* A, int64_t lda, int a_mn, const void* B, int64_t ldb,
                          int b_mn, const void* C, const void* X, int a_dt, int b_dt, int c_dt,
                          int x_dt, int cd_m_major, double alpha, double beta, double xf,
-                         int use_c, int use_x, int relu) {
+                         int use_c, int use_x, int relu, int64_t acc_chunk) {
   p->M = M; p->N = N; p->K = K; p->L = L;
   p->A = A; p->lda = lda; p->a_mn_major = a_mn;
   p->B = B; p->ldb = ldb; p->b_mn_major = b_mn;
@@ -285,22 +300,25 @@ static void fill_problem(oracle_problem* p, int64_t M, int64_t N, int64_t K, int
   p->use_c = use_c && C != NULL;
   p->use_x = use_x && X != NULL;
   p->relu = relu;
+  p->acc_chunk = acc_chunk;
 }
 
-/* Rows [m0, m1) of every batch, all columns.  D, Y, S are [L][m1-m0][N]
- * (S may be NULL).  Returns 0, or -1 on a bad argument. */
+/* Rows [m0, m1) of every batch, all columns.  D, Y, S, P are [L][m1-m0][N]
+ * (S and P may be NULL; P is filled when acc_chunk > 0).  Returns 0, or -1
+ * on a bad argument. */
 int oracle_gemm_rows(int64_t M, int64_t N, int64_t K, int64_t L,
                      const void* A, int64_t lda, int a_mn, const void* B, int64_t ldb, int b_mn,
                      const void* C, const void* X, int a_dt, int b_dt, int c_dt, int x_dt,
                      int cd_m_major, double alpha, double beta, double xf, int use_c, int use_x,
-                     int relu, int64_t m0, int64_t m1, double* D, double* Y, double* S,
-                     int nthreads) {
+                     int relu, int64_t acc_chunk, int64_t m0, int64_t m1, double* D, double* Y,
+                     double* S, double* P, int nthreads) {
   if (M < 0 || N < 0 || K < 0 || L < 0 || m0 < 0 || m1 > M || m0 > m1) return -1;
+  if (acc_chunk < 0) return -1;
   if (elem_bytes(a_dt) == 0 || elem_bytes(b_dt) == 0) return -1;
   build_tables();
   oracle_problem p;
   fill_problem(&p, M, N, K, L, A, lda, a_mn, B, ldb, b_mn, C, X, a_dt, b_dt, c_dt, x_dt,
-               cd_m_major, alpha, beta, xf, use_c, use_x, relu);
+               cd_m_major, alpha, beta, xf, use_c, use_x, relu, acc_chunk);
   int64_t rows = m1 - m0;
 #ifdef _OPENMP
   if (nthreads > 0) omp_set_num_threads(nthreads);
@@ -316,7 +334,8 @@ int oracle_gemm_rows(int64_t M, int64_t N, int64_t K, int64_t L,
       for (int64_t k = 0; k < K; ++k) arow[k] = load_elem(A, a_dt, a_index(&p, m, k, l));
       for (int64_t n = 0; n < N; ++n) {
         int64_t o = (l * rows + (m - m0)) * N + n;
-        entry(&p, m, n, l, arow, &D[o], &Y[o], S ? &S[o] : NULL);
+        entry(&p, m, n, l, arow, &D[o], &Y[o], S ? &S[o] : NULL,
+              P && acc_chunk > 0 ? &P[o] : NULL);
       }
     }
     free(arow);
@@ -329,21 +348,24 @@ int oracle_gemm_entries(int64_t M, int64_t N, int64_t K, int64_t L,
                         const void* A, int64_t lda, int a_mn, const void* B, int64_t ldb, int b_mn,
                         const void* C, const void* X, int a_dt, int b_dt, int c_dt, int x_dt,
                         int cd_m_major, double alpha, double beta, double xf, int use_c, int use_x,
-                        int relu, const int64_t* ms, const int64_t* ns, const int64_t* ls,
-                        int64_t count, double* D, double* Y, double* S, int nthreads) {
+                        int relu, int64_t acc_chunk, const int64_t* ms, const int64_t* ns,
+                        const int64_t* ls, int64_t count, double* D, double* Y, double* S,
+                        double* P, int nthreads) {
   if (elem_bytes(a_dt) == 0 || elem_bytes(b_dt) == 0) return -1;
+  if (acc_chunk < 0) return -1;
   for (int64_t i = 0; i < count; ++i)
     if (ms[i] < 0 || ms[i] >= M || ns[i] < 0 || ns[i] >= N || ls[i] < 0 || ls[i] >= L) return -1;
   build_tables();
   oracle_problem p;
   fill_problem(&p, M, N, K, L, A, lda, a_mn, B, ldb, b_mn, C, X, a_dt, b_dt, c_dt, x_dt,
-               cd_m_major, alpha, beta, xf, use_c, use_x, relu);
+               cd_m_major, alpha, beta, xf, use_c, use_x, relu, acc_chunk);
 #ifdef _OPENMP
   if (nthreads > 0) omp_set_num_threads(nthreads);
 #pragma omp parallel for schedule(dynamic, 16)
 #endif
   for (int64_t i = 0; i < count; ++i)
-    entry(&p, ms[i], ns[i], ls[i], NULL, &D[i], &Y[i], S ? &S[i] : NULL);
+    entry(&p, ms[i], ns[i], ls[i], NULL, &D[i], &Y[i], S ? &S[i] : NULL,
+          P && acc_chunk > 0 ? &P[i] : NULL);
   return 0;
 }
 

@@ -27,7 +27,7 @@ def _storage(t):
 
 def _problem(A, B, C=None, X=None, *, ab="f16", c="f32", x="f32", a_mn=False, b_mn=False,
              cd_m=False, alpha=1.0, beta=0.0, xf=0.0, use_c=None, use_x=None, lda=None, ldb=None,
-             b=None, relu=False):
+             b=None, relu=False, acc_chunk=0):
     """Build an oracle Problem from LOGICAL torch tensors A [L,M,K], B [L,N,K],
     C/X [L,M,N] (storage dtypes), laying them out as requested."""
     L, M, K = A.shape
@@ -43,7 +43,8 @@ def _problem(A, B, C=None, X=None, *, ab="f16", c="f32", x="f32", a_mn=False, b_
     Cs = None if C is None else _storage(W.to_storage(C, cd_m))
     Xs = None if X is None else _storage(W.to_storage(X, cd_m))
     return oracle.Problem(M, N, K, L, _storage(As), As.shape[2], a_mn, _storage(Bs), Bs.shape[2],
-                          b_mn, Cs, Xs, ab, c, x, cd_m, alpha, beta, xf, use_c, use_x, b, relu)
+                          b_mn, Cs, Xs, ab, c, x, cd_m, alpha, beta, xf, use_c, use_x, b, relu,
+                          acc_chunk)
 
 
 def _f64(t, fp8="e4m3"):
@@ -410,3 +411,63 @@ def test_tf32_storage_decodes_as_fp32_and_generator_rounds_to_tf32():
     assert W.round_to_tf32(ties).tolist() == [1.0, 1.0 + 2.0 ** -9]
     codes = bits.numpy().view(np.uint32)[:64]
     np.testing.assert_array_equal(oracle.decode("tf32", codes), oracle.decode("f32", codes))
+
+
+# ---------------------------------------------------------------- half-precision accumulator term
+
+def test_partial_sum_term_brute_force_fractions():
+    """P = sum over the chunk boundaries (every 16 k and k = K) of |exact
+    running sum|, checked against exact rational arithmetic on a K that is
+    not a multiple of the chunk (50 = 3*16 + 2), for two chunk sizes."""
+    g = torch.Generator().manual_seed(37)
+    A = torch.randn(1, 4, 50, generator=g).to(torch.float16)
+    B = torch.randn(1, 3, 50, generator=g).to(torch.float16)
+    a = [[Fraction(float(v)) for v in row] for row in A[0].float()]
+    b = [[Fraction(float(v)) for v in row] for row in B[0].float()]
+    for chunk, bounds in ((16, (16, 32, 48, 50)), (32, (32, 50))):
+        D, Y, S, P = oracle.gemm(_problem(A, B, ab="f16", alpha=1.0, acc_chunk=chunk))
+        for m in range(4):
+            for n in range(3):
+                exact = sum(abs(sum(a[m][k] * b[n][k] for k in range(e))) for e in bounds)
+                assert abs(Fraction(P[0, m, n]) - exact) <= Fraction(1e-12) * (1 + exact)
+
+
+def test_partial_sum_term_closed_forms():
+    """All-ones A and B: the running sum after k terms is k, so P is the sum
+    of the boundaries themselves (16+32+48+64 = 160 for K = 64, chunk 16;
+    32+64+70 = 166 for K = 70, chunk 32).  Signs alternating along k make
+    every even running sum 0: with chunk 2, P = 0 exactly; with chunk 3 the
+    boundaries 3, 6, ... alternate |1| and |0|."""
+    for K, chunk, want in ((64, 16, 160.0), (70, 32, 166.0), (1, 16, 1.0)):
+        A = torch.ones(1, 2, K, dtype=torch.float16)
+        B = torch.ones(1, 2, K, dtype=torch.float16)
+        _, Y, _, P = oracle.gemm(_problem(A, B, ab="f16", alpha=1.0, acc_chunk=chunk))
+        assert np.all(P == want) and np.all(Y == K)
+    K = 12
+    alt = torch.tensor([(-1.0) ** k for k in range(K)], dtype=torch.float16)
+    A = alt.expand(1, 2, K).contiguous()
+    B = torch.ones(1, 2, K, dtype=torch.float16)
+    _, _, _, P2 = oracle.gemm(_problem(A, B, ab="f16", alpha=1.0, acc_chunk=2))
+    _, _, _, P3 = oracle.gemm(_problem(A, B, ab="f16", alpha=1.0, acc_chunk=3))
+    assert np.all(P2 == 0.0)
+    assert np.all(P3 == 2.0)       # boundaries 3, 6, 9, 12: |1|, |0|, |1|, |0|
+
+
+def test_partial_sum_term_layouts_entries_and_off():
+    """P does not depend on layouts, entries and row blocks agree with the
+    full problem, acc_chunk = 0 returns the three-array result, and a
+    negative chunk is rejected."""
+    g = torch.Generator().manual_seed(41)
+    A = torch.randn(2, 9, 40, generator=g).to(torch.bfloat16)
+    B = torch.randn(2, 7, 40, generator=g).to(torch.bfloat16)
+    base = oracle.gemm(_problem(A, B, ab="bf16", alpha=1.0, acc_chunk=16))
+    assert len(base) == 4 and np.all(base[3] >= np.abs(base[1]))
+    alt = _problem(A, B, ab="bf16", a_mn=True, b_mn=True, alpha=1.0, acc_chunk=16)
+    np.testing.assert_array_equal(oracle.gemm(alt)[3], base[3])
+    ms, ns, ls = np.array([0, 8, 4]), np.array([6, 0, 3]), np.array([1, 0, 1])
+    pe = oracle.gemm_entries(alt, ms, ns, ls)[3]
+    np.testing.assert_array_equal(pe, base[3][ls, ms, ns])
+    np.testing.assert_array_equal(oracle.gemm_rows(alt, 2, 5)[3], base[3][:, 2:5])
+    assert len(oracle.gemm(_problem(A, B, ab="bf16", alpha=1.0))) == 3
+    with pytest.raises(ValueError):
+        oracle.gemm(_problem(A, B, ab="bf16", alpha=1.0, acc_chunk=-1))

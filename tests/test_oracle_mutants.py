@@ -27,6 +27,8 @@ MUTANTS = {
     "bf16_decoder_mantissa": ("v = ldexp(1.0 + f / 128.0, e - 127);",
                               "v = ldexp(1.0 + f / 256.0, e - 127);"),
     "e5m2_bias": ("v = ldexp(1.0 + f / 4.0, e - 15);", "v = ldexp(1.0 + f / 4.0, e - 16);"),
+    "partial_boundary_shift": ("((k + 1) % p->acc_chunk == 0 || k + 1 == p->K)",
+                               "(k % p->acc_chunk == 0 || k + 1 == p->K)"),
     "relu_after_x": ("  if (p->relu && dv < 0.0) dv = 0.0;\n  if (p->use_x) dv += p->xf",
                      "  if (p->use_x) dv += p->xf"),
 }
