@@ -268,7 +268,8 @@ class Bound:
         self.Y = torch.empty(shape, dtype=W.TORCH_DTYPE[w.y], device=dev) if w.y else None
         self.dt = G.make_dtypes(w.ab, w.c or "f32", w.d, w.x or "f32", w.y or "f32",
                                 G.GEMM_MN_MAJOR if w.cd_m_major else G.GEMM_K_MAJOR, b=w.b,
-                                epilogue=G.GEMM_EPI_RELU if w.relu else G.GEMM_EPI_LINEAR)
+                                epilogue=G.GEMM_EPI_RELU if w.relu else G.GEMM_EPI_LINEAR,
+                                acc=w.acc)
         self.G, self.g = G, g
 
     def launch(self, stream, A=None, B=None, C=None, X=None, D=None, Y=None):
@@ -526,7 +527,7 @@ def main():
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": warm, "ms_per_step": max_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": w.ab + (f"/{w.b}" if w.b else "") + " in, f32 accumulate",
+            "dtype": w.ab + (f"/{w.b}" if w.b else "") + f" in, {w.acc} accumulate",
             "data": "synthetic",
             "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "L": w.L,
                        "ab": w.ab, "c": w.c, "d": w.d, "x": w.x, "y": w.y,

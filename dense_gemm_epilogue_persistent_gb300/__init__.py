@@ -41,7 +41,7 @@ DTYPE_CODES = {"f32": GEMM_F32, "f16": GEMM_F16, "bf16": GEMM_BF16, "e4m3": GEMM
 class gemm_dtypes_t(ctypes.Structure):
     _fields_ = [("ab", ctypes.c_int), ("c", ctypes.c_int), ("d", ctypes.c_int),
                 ("x", ctypes.c_int), ("y", ctypes.c_int), ("cdxy_major", ctypes.c_int),
-                ("b", ctypes.c_int), ("epilogue", ctypes.c_int)]
+                ("b", ctypes.c_int), ("epilogue", ctypes.c_int), ("acc", ctypes.c_int)]
 
 
 class gemm_config_t(ctypes.Structure):
@@ -135,11 +135,12 @@ def _stream(s) -> int | None:
 
 
 def make_dtypes(ab, c="f32", d="f32", x="f32", y="f32", cdxy_major=GEMM_K_MAJOR, b=None,
-                epilogue=GEMM_EPI_LINEAR) -> gemm_dtypes_t:
-    """b: B's type when it differs from A's (fp8 pairs); epilogue: GEMM_EPI_*."""
+                epilogue=GEMM_EPI_LINEAR, acc="f32") -> gemm_dtypes_t:
+    """b: B's type when it differs from A's (fp8 pairs); epilogue: GEMM_EPI_*;
+    acc: the tensor-core accumulator type, "f32" or "f16"."""
     code = lambda v: DTYPE_CODES[v] if isinstance(v, str) else int(v)
     return gemm_dtypes_t(code(ab), code(c), code(d), code(x), code(y), int(cdxy_major),
-                         GEMM_F32 if b is None or b == ab else code(b), int(epilogue))
+                         GEMM_F32 if b is None or b == ab else code(b), int(epilogue), code(acc))
 
 
 # ------------------------------------------------------------------ C entry points

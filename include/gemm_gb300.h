@@ -79,12 +79,21 @@ typedef enum { GEMM_K_MAJOR = 0, GEMM_MN_MAJOR = 1 } gemm_layout_t;
  *   cdxy_major: the one major order of C, D, X and Y.
  *   b: B's type when it differs from A's -- only fp8 pairs (E4M3 x E5M2 in
  *      either order, which tcgen05 kind::f8f6f4 takes); 0 (GEMM_F32) = same as ab.
- *   epilogue: GEMM_EPI_LINEAR (0) or GEMM_EPI_RELU. */
+ *   epilogue: GEMM_EPI_LINEAR (0) or GEMM_EPI_RELU.
+ *   acc: the tensor-core accumulator, GEMM_F32 (0, the default) or GEMM_F16.
+ *      F16 is taken for F16, E4M3 and E5M2 inputs only (the cuBLASDx
+ *      Blackwell page: half inputs with a half or float accumulator, fp8 with
+ *      half or float, bfloat16 and tf32 with float); otherwise the call
+ *      returns GEMM_ERR_UNSUPPORTED_DTYPE.  An F16 accumulator is rounded to
+ *      fp16 once per tensor-core instruction (every 16 K of 16-bit inputs,
+ *      32 K of 8-bit) and overflows to infinity past 65504; Y is that fp16
+ *      value and the epilogue still runs in fp32. */
 typedef struct {
   gemm_dtype_t ab, c, d, x, y;
   gemm_layout_t cdxy_major;
   gemm_dtype_t b;
   gemm_epilogue_t epilogue;
+  gemm_dtype_t acc;
 } gemm_dtypes_t;
 
 /* Kernel configuration.  Chosen automatically per problem shape unless the

@@ -7,6 +7,16 @@ Comparison bound (the target's statement of parity):
   Y the same with alpha = 1 and no C or X term; bit-exact equality with the
   once-rounded oracle value on integer-valued inputs whose products and sums
   are exactly representable.
+
+fp16 accumulator (rounded to fp16 once per tensor-core instruction, i.e.
+after every chunk of 16 K for 16-bit inputs, 32 K for 8-bit): the
+accumulator's error is at most
+  E = (2^-11 * P + 2^-10 * sum_k |a*b|) / (1 - n * 2^-11),
+P the oracle's sum over the n chunk boundaries of |exact running sum|; the
+2^-11 * P term is half an fp16 ulp (relative) per rounding, the 2^-10 term
+the fp32 path's own bound for the products inside an instruction, and the
+divisor absorbs the rounding of already-rounded errors.  D's bound takes
+|alpha| * E in place of 2^-10 * |alpha| * sum|ab|; Y's is E.
 """
 from __future__ import annotations
 
@@ -20,6 +30,7 @@ import workloads as W
 import dense_gemm_epilogue_persistent_gb300 as G
 
 TOL_REL = 2.0 ** -10
+U16 = 2.0 ** -11                               # unit roundoff of fp16
 ULP = {"f16": (10, -14), "bf16": (7, -126)}   # fraction bits, min normal exponent
 
 
@@ -63,19 +74,28 @@ class Case:
     ldb_pad: int = 0
     b: str | None = None      # B's type when it differs from A's (fp8 pairs)
     relu: bool = False
+    acc: str = "f32"          # tensor-core accumulator
 
     @staticmethod
     def from_workload(w: W.Workload, **over):
         kw = dict(M=w.M, N=w.N, K=w.K, L=w.L, ab=w.ab, c=w.c, d=w.d, x=w.x, y=w.y,
                   a_mn=w.a_mn_major, b_mn=w.b_mn_major, cd_m=w.cd_m_major, alpha=w.alpha,
-                  beta=w.beta, xf=w.x_factor, dist=w.dist, seed=w.seed, b=w.b, relu=w.relu)
+                  beta=w.beta, xf=w.x_factor, dist=w.dist, seed=w.seed, b=w.b, relu=w.relu,
+                  acc=w.acc)
         kw.update(over)
         return Case(**kw)
 
     def workload(self) -> W.Workload:
         return W.Workload("case", self.M, self.N, self.K, self.L, self.ab, self.a_mn, self.b_mn,
                           self.c, self.d, self.x, self.y, self.cd_m, self.alpha, self.beta,
-                          self.xf, self.seed, self.dist, self.b, self.relu)
+                          self.xf, self.seed, self.dist, self.b, self.relu, self.acc)
+
+    @property
+    def acc_chunk(self) -> int:
+        """K per tensor-core instruction when the accumulator is fp16, else 0."""
+        if self.acc != "f16":
+            return 0
+        return 32 if W.ELEM_BYTES[self.ab] == 1 else 16
 
 
 def _pad_ld(t: torch.Tensor, pad: int) -> torch.Tensor:
@@ -124,7 +144,7 @@ def run_gpu(gemm: G.Gemm, prep: Prepared, stream=None, D=None, Y=None, use_x=Tru
         Y = torch.empty(out_shape(c), dtype=W.TORCH_DTYPE[c.y], device=dev)
     dt = G.make_dtypes(c.ab, c.c or "f32", c.d, c.x or "f32", c.y or "f32",
                        G.GEMM_MN_MAJOR if c.cd_m else G.GEMM_K_MAJOR, b=c.b,
-                       epilogue=G.GEMM_EPI_RELU if c.relu else G.GEMM_EPI_LINEAR)
+                       epilogue=G.GEMM_EPI_RELU if c.relu else G.GEMM_EPI_LINEAR, acc=c.acc)
     gemm.run(c.M, c.N, c.K, c.L, A, A.shape[-1], int(c.a_mn), B, B.shape[-1], int(c.b_mn),
              C, X, D, Y, c.alpha, c.beta, c.xf, dt, stream)
     return D, Y
@@ -138,7 +158,7 @@ def oracle_problem(prep: Prepared, use_x=True) -> oracle.Problem:
                           st(prep.C) if prep.C is not None else None,
                           st(prep.X) if (prep.X is not None and use_x) else None,
                           c.ab, c.c or "f32", c.x or "f32", c.cd_m, c.alpha, c.beta, c.xf,
-                          b_dtype=c.b, relu=c.relu)
+                          b_dtype=c.b, relu=c.relu, acc_chunk=c.acc_chunk)
 
 
 def logical(t: torch.Tensor, cd_m: bool) -> torch.Tensor:
@@ -146,8 +166,17 @@ def logical(t: torch.Tensor, cd_m: bool) -> torch.Tensor:
     return W.from_storage(t.cpu(), cd_m)
 
 
-def bound_D(case: Case, S, Cv, Xv, ref):
-    b = TOL_REL * (abs(case.alpha) * S)
+def bound_acc(case: Case, S, P=None):
+    """Bound on the accumulator's error (see the module docstring)."""
+    if case.acc_chunk == 0:
+        return TOL_REL * S
+    n = -(-case.K // case.acc_chunk)
+    assert n * U16 < 0.5, "K too long for the fp16-accumulator bound"
+    return (U16 * P + TOL_REL * S) / (1.0 - n * U16)
+
+
+def bound_D(case: Case, S, Cv, Xv, ref, P=None):
+    b = abs(case.alpha) * bound_acc(case, S, P)
     if Cv is not None and case.beta != 0:
         b = b + TOL_REL * np.abs(case.beta * Cv)
     if Xv is not None and case.xf != 0:
@@ -169,7 +198,8 @@ def assert_within(name, got, ref, bound):
 def compare_full(prep: Prepared, D_dev, Y_dev, exact=False, use_x=True):
     """Element-by-element comparison of every output against the oracle."""
     c = prep.case
-    D_ref, Y_ref, S = oracle.gemm(oracle_problem(prep, use_x))
+    D_ref, Y_ref, S, *rest = oracle.gemm(oracle_problem(prep, use_x))
+    P = rest[0] if rest else None
     D = to_f64(logical(D_dev, c.cd_m))
     if exact:
         want = oracle.round_to(c.d, D_ref)
@@ -178,7 +208,7 @@ def compare_full(prep: Prepared, D_dev, Y_dev, exact=False, use_x=True):
     else:
         Cv = to_f64(prep.inp.C) if prep.inp.C is not None else None
         Xv = to_f64(prep.inp.X) if (prep.inp.X is not None and use_x) else None
-        assert_within("D", D, D_ref, bound_D(c, S, Cv, Xv, D_ref))
+        assert_within("D", D, D_ref, bound_D(c, S, Cv, Xv, D_ref, P))
     if Y_dev is not None:
         Y = to_f64(logical(Y_dev, c.cd_m))
         if exact:
@@ -186,7 +216,7 @@ def compare_full(prep: Prepared, D_dev, Y_dev, exact=False, use_x=True):
             want = want.astype(np.float64) if c.y == "f32" else oracle.decode(c.y, want).reshape(Y.shape)
             np.testing.assert_array_equal(Y, want)
         else:
-            assert_within("Y", Y, Y_ref, TOL_REL * S + ulp_at(c.y, Y_ref))
+            assert_within("Y", Y, Y_ref, bound_acc(c, S, P) + ulp_at(c.y, Y_ref))
     return D_ref, Y_ref
 
 
@@ -208,13 +238,14 @@ def compare_sampled(prep: Prepared, D_dev, Y_dev, tile_m: int, tile_n: int, seed
                 ms = np.concatenate([ms, np.arange(c.M)])
                 ns = np.concatenate([ns, np.full(c.M, col)])
                 ls = np.concatenate([ls, np.full(c.M, l)])
-    D_ref, Y_ref, S = oracle.gemm_entries(p, ms, ns, ls)
+    D_ref, Y_ref, S, *rest = oracle.gemm_entries(p, ms, ns, ls)
+    P = rest[0] if rest else None
     Dl = logical(D_dev, c.cd_m)
     D = to_f64(Dl[ls, ms, ns])
     Cv = to_f64(prep.inp.C[ls, ms, ns]) if prep.inp.C is not None else None
     Xv = to_f64(prep.inp.X[ls, ms, ns]) if prep.inp.X is not None else None
-    assert_within("D", D, D_ref, bound_D(c, S, Cv, Xv, D_ref))
+    assert_within("D", D, D_ref, bound_D(c, S, Cv, Xv, D_ref, P))
     if Y_dev is not None:
         Y = to_f64(logical(Y_dev, c.cd_m)[ls, ms, ns])
-        assert_within("Y", Y, Y_ref, TOL_REL * S + ulp_at(c.y, Y_ref))
+        assert_within("Y", Y, Y_ref, bound_acc(c, S, P) + ulp_at(c.y, Y_ref))
     return len(ms)

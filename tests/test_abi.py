@@ -121,6 +121,21 @@ def test_check_fp8_pairs_and_epilogue(lib):
     assert G.gemm_check(_p(dtypes=dt(epilogue=7))) == G.GEMM_ERR_INVALID_ARG
 
 
+def test_check_accumulator_types(lib):
+    """fp16 accumulation is taken for fp16 and fp8 inputs only (the cuBLASDx
+    Blackwell page's precision list); the accumulator is fp32 or fp16."""
+    for ab, b in (("f16", None), ("e4m3", None), ("e5m2", None), ("e4m3", "e5m2")):
+        dt = G.make_dtypes(ab, "f16", "f16", b=b, acc="f16")
+        assert G.gemm_check(_p(dtypes=dt)) == G.GEMM_OK, (ab, b)
+    for ab, c in (("bf16", "f16"), ("tf32", "f32")):
+        dt = G.make_dtypes(ab, c, c, acc="f16")
+        assert G.gemm_check(_p(dtypes=dt)) == G.GEMM_ERR_UNSUPPORTED_DTYPE, ab
+    for acc in ("bf16", "e4m3", "tf32", 9):
+        dt = G.make_dtypes("f16", "f16", "f16", acc=acc)
+        assert G.gemm_check(_p(dtypes=dt)) == G.GEMM_ERR_UNSUPPORTED_DTYPE, acc
+    assert G.gemm_check(_p(dtypes=G.make_dtypes("f16", "f16", "f16", acc="f32"))) == G.GEMM_OK
+
+
 def test_check_tf32_k_major_only(lib):
     dt = G.make_dtypes("tf32", "f32", "f32")
     assert G.gemm_check(_p(dtypes=dt)) == G.GEMM_OK

@@ -262,6 +262,84 @@ def test_tf32_integers_exact(gemm):
     compare_full(prep, D, Y, exact=True)
 
 
+# ------------------------------------------------------------ fp16 accumulator
+
+def _int_fp8_inputs(case):
+    """Integer inputs in [-2, 2] stored as fp8 codes (exact in E4M3 and E5M2),
+    with integer C: every running sum stays an integer below 2048."""
+    g = torch.Generator().manual_seed(case.seed)
+    fp8 = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+    A = torch.randint(-2, 3, (case.L, case.M, case.K), generator=g).float()
+    B = torch.randint(-2, 3, (case.L, case.N, case.K), generator=g).float()
+    C = torch.randint(-2, 3, (case.L, case.M, case.N), generator=g).float()
+    return W.Inputs(A.to(fp8[case.ab]).view(torch.uint8),
+                    B.to(fp8[case.b or case.ab]).view(torch.uint8), C, None)
+
+
+@pytest.mark.parametrize("variant", VARIANTS + [None])
+@pytest.mark.parametrize("ab", ["f16", "e4m3"])
+def test_f16_accumulator_integers_exact(gemm, variant, ab):
+    """fp16 accumulation, integer inputs in [-2, 2], K = 400: every running
+    sum is an integer of magnitude <= 1600 < 2048, exact in fp16 whatever the
+    rounding points, so Y and D (f32, alpha 1.5, beta -0.5) are bit-exact."""
+    if variant:
+        _force(gemm, *variant)
+    else:
+        gemm.set_config(None)
+    case = Case(M=300, N=264, K=400, L=2, ab=ab, c="f32", d="f32", y="f32", alpha=1.5,
+                beta=-0.5, dist="int2", seed=71, acc="f16")
+    prep = prepare(case, _int_fp8_inputs(case) if ab != "f16" else None)
+    D, Y = run_gpu(gemm, prep)
+    _finish(gemm)
+    compare_full(prep, D, Y, exact=True)
+    gemm.set_config(None)
+
+
+@pytest.mark.parametrize("variant", [None, (1, 128, 1), (1, 256, 2), (2, 128, 1), (2, 256, 1)])
+@pytest.mark.parametrize("ab,b", [("f16", None), ("e4m3", None), ("e5m2", "e4m3")])
+def test_f16_accumulator_bound_and_precision(gemm, variant, ab, b):
+    """fp16 accumulation on real-valued ragged problems: D and Y within the
+    fp16-accumulator bound, and Y (stored as f32) holds fp16 values only --
+    the accumulator really is fp16 (an fp32 accumulator would not round
+    there).  The same problem with an fp32 accumulator is closer to the
+    exact result on average."""
+    if variant:
+        _force(gemm, *variant)
+    else:
+        gemm.set_config(None)
+    dist = "normal1" if ab == "f16" else "e4m3_pm4"
+    case = Case(M=520, N=392, K=1008, L=2, ab=ab, b=b, c="f16", d="f16", x="bf16", y="f32",
+                alpha=0.75, beta=1.0, xf=-0.5, dist=dist, seed=73, acc="f16")
+    prep = prepare(case)
+    D, Y = run_gpu(gemm, prep)
+    _finish(gemm)
+    _, Y_ref = compare_full(prep, D, Y)
+    y = Y.cpu()
+    assert torch.equal(y, y.half().float())
+    prep32 = prepare(Case(**{**case.__dict__, "acc": "f32"}), prep.inp)
+    _, Y32 = run_gpu(gemm, prep32)
+    _finish(gemm)
+    err16 = np.abs(to_f64(logical(Y, False)) - Y_ref).mean()
+    err32 = np.abs(to_f64(logical(Y32, False)) - Y_ref).mean()
+    assert err32 < err16
+    gemm.set_config(None)
+
+
+def test_f16_accumulator_split_last_wave(gemm):
+    """fp16 accumulation through the half-width items of a split last wave
+    (100 pair tiles on 76 pairs: 24 split; the half-width instruction
+    descriptor carries the fp16 accumulator format too)."""
+    _force(gemm, 2, 256, 1)
+    case = Case(M=2560, N=2560, K=192, L=1, ab="f16", c="f16", d="f16", y="f16", alpha=1.0,
+                beta=1.0, dist="normal1", seed=75, acc="f16")
+    prep = prepare(case)
+    D, Y = run_gpu(gemm, prep)
+    _finish(gemm)
+    assert gemm.last_config().tail_split > 0
+    compare_full(prep, D, Y)
+    gemm.set_config(None)
+
+
 # ------------------------------------------------------------ edge cases
 
 @pytest.mark.parametrize("M,N,K,L", [(8, 8, 16, 1), (1, 8, 16, 1), (129, 136, 72, 1),
@@ -369,7 +447,8 @@ def test_streams_and_repeat_determinism(gemm):
 # ------------------------------------------------------------ full-size workloads
 
 FULL = ["gemm2048_bf16_f32", "efc8192_f16", "gemm8192_bf16", "batched16_bf16_mn",
-        "ragged_e4m3_f16", "e5m2_4096_f16", "fp8mix_relu_4096", "tf32_4096_f32"]
+        "ragged_e4m3_f16", "e5m2_4096_f16", "fp8mix_relu_4096", "tf32_4096_f32",
+        "f16acc_4096_f16", "e4m3_f16acc_4096"]
 
 
 @pytest.mark.parametrize("name", FULL)

@@ -43,6 +43,7 @@ class Workload:
     dist: str               # see draw()
     b: str | None = None    # B's type when it differs from A's (fp8 pairs)
     relu: bool = False      # D = max(alpha*AB + beta*C, 0) + x_factor*X
+    acc: str = "f32"        # tensor-core accumulator: "f32" or "f16"
 
     @property
     def b_type(self) -> str:
@@ -81,6 +82,13 @@ WORKLOADS = {
     # tf32 inputs (fp32 storage of tf32 values), fp32 C and D
     "tf32_4096_f32": Workload("tf32_4096_f32", 4096, 4096, 4096, 1, "tf32", False, False,
                               "f32", "f32", None, None, False, 1.0, 1.0, 0.0, 8, "normal1"),
+    # fp16 accumulation: fp16 inputs with the custom epilogue, and E4M3 inputs
+    "f16acc_4096_f16": Workload("f16acc_4096_f16", 4096, 4096, 4096, 1, "f16", False, False,
+                                "f16", "f16", "f16", "f16", False, 2.0, 1.0, 3.0, 9, "normal1",
+                                acc="f16"),
+    "e4m3_f16acc_4096": Workload("e4m3_f16acc_4096", 4096, 4096, 4096, 1, "e4m3", False, False,
+                                 "f16", "f16", None, None, False, 0.25, 1.0, 0.0, 10, "e4m3_pm4",
+                                 acc="f16"),
 }
 
 TORCH_DTYPE = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16,
