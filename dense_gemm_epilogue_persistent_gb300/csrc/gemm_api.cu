@@ -110,6 +110,11 @@ gemm_status_t validate(const gemm_problem_t* pp) {
   // takes E4M3 and E5M2 in any pairing).
   if (t.b != GEMM_F32 && !(is_fp8(t.ab) && is_fp8(t.b))) return GEMM_ERR_UNSUPPORTED_DTYPE;
   if (t.epilogue != GEMM_EPI_LINEAR && t.epilogue != GEMM_EPI_RELU) return GEMM_ERR_INVALID_ARG;
+  // Accumulator: fp32, or fp16 for fp16 and fp8 inputs (cuBLASDx Blackwell
+  // card, "Precision": half with a half or float accumulator, bfloat16 and
+  // tf32 with float only, fp8 with half or float).
+  if (t.acc != GEMM_F32 && t.acc != GEMM_F16) return GEMM_ERR_UNSUPPORTED_DTYPE;
+  if (t.acc == GEMM_F16 && t.ab != GEMM_F16 && !is_fp8(t.ab)) return GEMM_ERR_UNSUPPORTED_DTYPE;
   // tf32 operands are K-major only (cuBLASDx Blackwell card, "Arrangement").
   if (t.ab == GEMM_TF32 && (p.layoutA != GEMM_K_MAJOR || p.layoutB != GEMM_K_MAJOR))
     return GEMM_ERR_UNSUPPORTED_DTYPE;
@@ -412,14 +417,14 @@ bool encode_epi(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int dt, in
   return r == CUDA_SUCCESS;
 }
 
-uint32_t make_idesc(int a_type, int b_type_, int cg, int bn, bool a_mn, bool b_mn) {
+uint32_t make_idesc(int a_type, int b_type_, bool acc_f16, int cg, int bn, bool a_mn, bool b_mn) {
   // kind::f16 / kind::tf32: format 0 = fp16, 1 = bf16, 2 = tf32.
   // kind::f8f6f4: 0 = e4m3, 1 = e5m2.
   auto fmt = [](int t) {
     return t == GEMM_TF32 ? 2u : (t == GEMM_BF16 || t == GEMM_E5M2) ? 1u : 0u;
   };
   uint32_t d = 0;
-  d |= 1u << 4;                                   // accumulator (D) format: fp32
+  d |= (acc_f16 ? 0u : 1u) << 4;                  // accumulator (D) format: 0 fp16, 1 fp32
   d |= fmt(a_type) << 7;                          // A format
   d |= fmt(b_type_) << 10;                        // B format
   d |= (a_mn ? 1u : 0u) << 15;                    // A MN-major
@@ -676,9 +681,11 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
   kp.stages = cfg.stages;
   kp.a_mn_major = a_mn;
   kp.b_mn_major = b_mn;
-  kp.idesc = make_idesc(dtypes->ab, b_type(*dtypes), cfg.cta_group, cfg.tile_n, a_mn, b_mn);
-  kp.idesc_half = make_idesc(dtypes->ab, b_type(*dtypes), cfg.cta_group, cfg.tile_n / 2, a_mn,
-                             b_mn);
+  const bool acc_f16 = dtypes->acc == GEMM_F16;
+  kp.idesc = make_idesc(dtypes->ab, b_type(*dtypes), acc_f16, cfg.cta_group, cfg.tile_n, a_mn,
+                        b_mn);
+  kp.idesc_half = make_idesc(dtypes->ab, b_type(*dtypes), acc_f16, cfg.cta_group, cfg.tile_n / 2,
+                             a_mn, b_mn);
   kp.split_start = (int)(cfg.tiles - cfg.tail_split);
   kp.num_items = (int)(cfg.tiles + cfg.tail_split);
   kp.l2_hints = (uint32_t)cfg.l2_hints;
@@ -698,6 +705,7 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
   kp.epi.beta = beta;
   kp.epi.x_factor = x_factor;
   kp.epi.relu = dtypes->epilogue == GEMM_EPI_RELU;
+  kp.epi.acc_f16 = acc_f16;
   kp.epi.slots = cfg.epi_slots;
   {
     const int sub = 128 * gb300::kEpiChunk;

@@ -62,6 +62,7 @@ struct EpiParams {
   int read_c, read_x, write_y;
   float alpha, beta, x_factor;
   int relu;                  // D = max(alpha*acc + beta*C, 0) + x_factor*X
+  int acc_f16;               // accumulator is fp16: one per 32-bit TMEM column, low half
   int slots;                 // epilogue shared-memory slots (>= 2)
   uint32_t cd_bytes;         // bytes of a slot's C/D region
   uint32_t xy_bytes;         // bytes of a slot's X/Y region (0: neither X nor Y)
@@ -92,6 +93,7 @@ constexpr int kThreads = 192;
 constexpr int kAccStages = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kEpiChunk = 32;          // columns per epilogue chunk
+constexpr int kPrefetchChunks = 4;     // C/X chunks prefetched into L2 beyond the slot loads
 constexpr int kEpiLeader = 64;         // thread that issues the epilogue's TMA
 constexpr uint32_t kEpiBarrier = 1;    // named barrier of the 128 epilogue threads
 
@@ -183,13 +185,21 @@ __device__ __forceinline__ int item_tile(int it, const KernelParams& p, int& hal
 
 // ------------------------------------------------------------------ epilogue smem
 
-__device__ __forceinline__ float bits16_to_f32(uint32_t b, int dt) {
-  return dt == DT_BF16 ? __uint_as_float(b << 16) : __half2float(__ushort_as_half((uint16_t)b));
+// Two fp32 values -> one 32-bit word of two 16-bit values (first in the low
+// half), rounded to nearest even.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
-
-__device__ __forceinline__ uint32_t f32_to_bits16(float v, int dt) {
-  return dt == DT_BF16 ? (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v))
-                       : (uint32_t)__half_as_ushort(__float2half_rn(v));
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t w) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
 // Epilogue sub-tiles hold 128 rows x 32 columns of one tensor, as TMA lays them out:
@@ -198,7 +208,8 @@ __device__ __forceinline__ uint32_t f32_to_bits16(float v, int dt) {
 //     64-byte swizzle: chunk j ^ ((r >> 1) & 3));
 //   column-major tensors: [column][128 rows], unswizzled.
 // Thread r touches only row r; the swizzles make each 8-row group of a warp hit
-// distinct banks.
+// distinct banks.  The type and layout branches are uniform and sit outside the
+// element loops, and 16-bit values convert two at a time.
 __device__ __forceinline__ void smem_read_row(const uint8_t* sub, int dt, int m_major, int r,
                                               float (&v)[kEpiChunk]) {
   if (!m_major) {
@@ -209,15 +220,24 @@ __device__ __forceinline__ void smem_read_row(const uint8_t* sub, int dt, int m_
         v[4 * j] = q.x; v[4 * j + 1] = q.y; v[4 * j + 2] = q.z; v[4 * j + 3] = q.w;
       }
     } else {
+      uint32_t w[16];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const uint4 q =
             *reinterpret_cast<const uint4*>(sub + r * 64 + ((j ^ ((r >> 1) & 3)) << 4));
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        w[4 * j] = q.x; w[4 * j + 1] = q.y; w[4 * j + 2] = q.z; w[4 * j + 3] = q.w;
+      }
+      if (dt == DT_BF16) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          v[8 * j + 2 * i] = bits16_to_f32(w[i] & 0xFFFFu, dt);
-          v[8 * j + 2 * i + 1] = bits16_to_f32(w[i] >> 16, dt);
+        for (int i = 0; i < 16; ++i) {
+          const float2 f = unpack_bf16x2(w[i]);
+          v[2 * i] = f.x; v[2 * i + 1] = f.y;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 f = unpack_f16x2(w[i]);
+          v[2 * i] = f.x; v[2 * i + 1] = f.y;
         }
       }
     }
@@ -227,40 +247,62 @@ __device__ __forceinline__ void smem_read_row(const uint8_t* sub, int dt, int m_
       for (int c = 0; c < kEpiChunk; ++c)
         v[c] = *reinterpret_cast<const float*>(sub + (c * 128 + r) * 4);
     } else {
+      uint32_t w[16];
 #pragma unroll
-      for (int c = 0; c < kEpiChunk; ++c)
-        v[c] = bits16_to_f32(*reinterpret_cast<const uint16_t*>(sub + (c * 128 + r) * 2), dt);
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t lo = *reinterpret_cast<const uint16_t*>(sub + (2 * i * 128 + r) * 2);
+        const uint32_t hi = *reinterpret_cast<const uint16_t*>(sub + ((2 * i + 1) * 128 + r) * 2);
+        w[i] = lo | (hi << 16);
+      }
+      if (dt == DT_BF16) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 f = unpack_bf16x2(w[i]);
+          v[2 * i] = f.x; v[2 * i + 1] = f.y;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 f = unpack_f16x2(w[i]);
+          v[2 * i] = f.x; v[2 * i + 1] = f.y;
+        }
+      }
     }
   }
 }
 
 __device__ __forceinline__ void smem_write_row(uint8_t* sub, int dt, int m_major, int r,
                                                const float (&v)[kEpiChunk]) {
-  if (!m_major) {
-    if (dt == DT_F32) {
+  if (dt == DT_F32) {
+    if (!m_major) {
 #pragma unroll
       for (int j = 0; j < 8; ++j)
         *reinterpret_cast<float4*>(sub + r * 128 + ((j ^ (r & 7)) << 4)) =
             make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
     } else {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint4 q;
-        q.x = f32_to_bits16(v[8 * j + 0], dt) | (f32_to_bits16(v[8 * j + 1], dt) << 16);
-        q.y = f32_to_bits16(v[8 * j + 2], dt) | (f32_to_bits16(v[8 * j + 3], dt) << 16);
-        q.z = f32_to_bits16(v[8 * j + 4], dt) | (f32_to_bits16(v[8 * j + 5], dt) << 16);
-        q.w = f32_to_bits16(v[8 * j + 6], dt) | (f32_to_bits16(v[8 * j + 7], dt) << 16);
-        *reinterpret_cast<uint4*>(sub + r * 64 + ((j ^ ((r >> 1) & 3)) << 4)) = q;
-      }
-    }
-  } else {
-    if (dt == DT_F32) {
-#pragma unroll
       for (int c = 0; c < kEpiChunk; ++c) *reinterpret_cast<float*>(sub + (c * 128 + r) * 4) = v[c];
-    } else {
+    }
+    return;
+  }
+  uint32_t w[16];
+  if (dt == DT_BF16) {
 #pragma unroll
-      for (int c = 0; c < kEpiChunk; ++c)
-        *reinterpret_cast<uint16_t*>(sub + (c * 128 + r) * 2) = (uint16_t)f32_to_bits16(v[c], dt);
+    for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = pack_f16x2(v[2 * i], v[2 * i + 1]);
+  }
+  if (!m_major) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      *reinterpret_cast<uint4*>(sub + r * 64 + ((j ^ ((r >> 1) & 3)) << 4)) =
+          make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      *reinterpret_cast<uint16_t*>(sub + (2 * i * 128 + r) * 2) = (uint16_t)(w[i] & 0xFFFFu);
+      *reinterpret_cast<uint16_t*>(sub + ((2 * i + 1) * 128 + r) * 2) = (uint16_t)(w[i] >> 16);
     }
   }
 }
@@ -466,42 +508,60 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     const uint64_t pol_in = make_l2_policy((p.l2_hints >> 2) & 3u);
     const uint64_t pol_out = make_l2_policy((p.l2_hints >> 4) & 3u);
 
-    // Epilogue chunk c of this CTA's stream: this CTA's whole-tile items come
-    // first (CHUNKS chunks each), then its half-width items (CHUNKS / 2 each).
-    // TMA coordinates are (column, row, batch) for row-major C/D/X/Y and (row,
-    // column, batch) for column-major ones.
-    const int n_whole = cluster_id < p.split_start
-                            ? (p.split_start - cluster_id + num_clusters - 1) / num_clusters
-                            : 0;
-    auto chunk_origin = [&](int c, int& row0, int& col0, int& tl) -> bool {
-      int ord, j;
-      if (c < n_whole * G::CHUNKS) {
-        ord = c / G::CHUNKS;
-        j = c - ord * G::CHUNKS;
-      } else {
-        const int c2 = c - n_whole * G::CHUNKS;
-        ord = n_whole + c2 / (G::CHUNKS / 2);
-        j = c2 % (G::CHUNKS / 2);
-      }
-      const int it = cluster_id + ord * num_clusters;
-      if (it >= p.num_items) return false;
+    // The epilogue leader walks this CTA's stream of chunks (CHUNKS per whole
+    // tile, CHUNKS / 2 per half-width item, in item order) with two cursors:
+    // `ld` issues the TMA loads of C/X into the slots, E - 1 chunks ahead of
+    // the chunk being processed, and `pf` prefetches into L2 the chunks
+    // kPrefetchChunks beyond that.  A cursor computes an item's coordinates
+    // once, when it enters the item.  TMA coordinates are (column, row, batch)
+    // for row-major C/D/X/Y and (row, column, batch) for column-major ones.
+    struct Cursor { int it, j, nch, row0, col0, tl; };
+    auto cursor_enter = [&](Cursor& cc) {
+      if (cc.it >= p.num_items) return;
       int half;
-      const int t = item_tile(it, p, half);
+      const int t = item_tile(cc.it, p, half);
       int tm, tn;
-      tile_coords(t, p, tm, tn, tl);
-      row0 = tm * G::CM + (int)grp * (G::BM * CG) + (int)rank * G::BM;
-      col0 = tn * BN + (half > 0 ? BN / 2 : 0) + j * kEpiChunk;
-      return true;
+      tile_coords(t, p, tm, tn, cc.tl);
+      cc.nch = half < 0 ? G::CHUNKS : G::CHUNKS / 2;
+      cc.row0 = tm * G::CM + (int)grp * (G::BM * CG) + (int)rank * G::BM;
+      cc.col0 = tn * BN + (half > 0 ? BN / 2 : 0);
     };
-    auto issue_loads = [&](int c) {         // epilogue leader only
-      int row0, col0, tl;
-      if (!chunk_origin(c, row0, col0, tl)) return;
-      const uint32_t slot = epi0 + (uint32_t)(c % E) * slot_bytes;
-      const uint32_t bar = cfull0 + 8u * (uint32_t)(c % E);
-      const int x0 = e.cd_m_major ? row0 : col0, x1 = e.cd_m_major ? col0 : row0;
-      mbar_arrive_expect_tx(bar, load_tx);
-      if (e.read_c) tma_load_3d(slot, &tmC, bar, x0, x1, tl, pol_in);
-      if (e.read_x) tma_load_3d(slot + e.cd_bytes, &tmX, bar, x0, x1, tl, pol_in);
+    auto cursor_next = [&](Cursor& cc) {
+      if (cc.it < p.num_items && ++cc.j == cc.nch) {
+        cc.j = 0;
+        cc.it += num_clusters;
+        cursor_enter(cc);
+      }
+    };
+    auto cursor_xy = [&](const Cursor& cc, int& x0, int& x1) {
+      const int col = cc.col0 + cc.j * kEpiChunk;
+      x0 = e.cd_m_major ? cc.row0 : col;
+      x1 = e.cd_m_major ? col : cc.row0;
+    };
+    Cursor ld{cluster_id, 0, 0, 0, 0, 0};
+    Cursor pf{cluster_id, 0, 0, 0, 0, 0};
+    int ld_slot = 0;
+    auto issue_loads = [&]() {              // epilogue leader only
+      if (ld.it < p.num_items) {
+        int x0, x1;
+        cursor_xy(ld, x0, x1);
+        const uint32_t slot = epi0 + (uint32_t)ld_slot * slot_bytes;
+        const uint32_t bar = cfull0 + 8u * (uint32_t)ld_slot;
+        mbar_arrive_expect_tx(bar, load_tx);
+        if (e.read_c) tma_load_3d(slot, &tmC, bar, x0, x1, ld.tl, pol_in);
+        if (e.read_x) tma_load_3d(slot + e.cd_bytes, &tmX, bar, x0, x1, ld.tl, pol_in);
+      }
+      if (++ld_slot == E) ld_slot = 0;
+      cursor_next(ld);
+    };
+    auto issue_prefetch = [&]() {           // epilogue leader only
+      if (pf.it < p.num_items) {
+        int x0, x1;
+        cursor_xy(pf, x0, x1);
+        if (e.read_c) tma_prefetch_l2_3d(&tmC, x0, x1, pf.tl);
+        if (e.read_x) tma_prefetch_l2_3d(&tmX, x0, x1, pf.tl);
+      }
+      cursor_next(pf);
     };
 
     if (epi_leader) {
@@ -510,7 +570,13 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       if (loads) {
         if (e.read_c) prefetch_tensormap(&tmC);
         if (e.read_x) prefetch_tensormap(&tmX);
-        for (int c = 0; c < E - 1; ++c) issue_loads(c);
+        cursor_enter(ld);
+        cursor_enter(pf);
+        for (int c = 0; c < E - 1; ++c) {
+          issue_loads();
+          cursor_next(pf);
+        }
+        for (int c = 0; c < kPrefetchChunks; ++c) issue_prefetch();
       }
     }
 
@@ -537,6 +603,16 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         uint32_t raw_acc[32];
         tmem_load_32cols(tbase + 32u * j, raw_acc);
         tmem_wait_ld();
+        // Normalise the accumulator to fp32 bit patterns once per chunk (uniform
+        // branches), so the per-element epilogue below is the same for every case.
+        if (p.k_blocks == 0) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) raw_acc[i] = 0u;     // K = 0: nothing was accumulated
+        } else if (e.acc_f16) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            raw_acc[i] = __float_as_uint(__half2float(__ushort_as_half((uint16_t)raw_acc[i])));
+        }
         if (j == nchunks - 1) {
           // The whole accumulator stage has been read: hand it back to the MMA warp.
           tc_fence_before_sync();
@@ -552,27 +628,50 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         float cv[kEpiChunk], xv[kEpiChunk];
         bool got = true;
         if (loads) got = wait_phase(cfull0 + 8u * slot_idx, (uint32_t)(gc / E) & 1u, w, kWaitEpiLoad);
-        if (got && e.read_c) smem_read_row(slot, e.c_dt, e.cd_m_major, r, cv);
+        if (got && e.read_c) {
+          smem_read_row(slot, e.c_dt, e.cd_m_major, r, cv);
+        } else {
+#pragma unroll
+          for (int i = 0; i < kEpiChunk; ++i) cv[i] = 0.f;
+        }
         if (got && e.read_x) smem_read_row(slot + e.cd_bytes, e.x_dt, e.cd_m_major, r, xv);
         // Every thread has read the slot (and agrees whether to go on) before any
         // thread overwrites it with D and Y.
         __syncwarp();
         ok = named_barrier_and(kEpiBarrier, 128, got);
         if (!ok) break;
-        float dv[kEpiChunk], yv[kEpiChunk];
+        // D from the accumulator, C (zero when not read) and X; the branches
+        // are uniform and outside the element loops.
+        float dv[kEpiChunk];
+        const float al = e.alpha, be = e.beta, xf = e.x_factor;
+        if (e.read_x) {
+          if (e.relu) {
 #pragma unroll
-        for (int i = 0; i < kEpiChunk; ++i) {
-          const float a = p.k_blocks > 0 ? __uint_as_float(raw_acc[i]) : 0.f;
-          const float c = e.read_c ? cv[i] : 0.f;
-          const float x = e.read_x ? xv[i] : 0.f;
-          yv[i] = a;
-          if (e.relu)
-            dv[i] = fmaf(e.x_factor, x, fmaxf(fmaf(e.alpha, a, e.beta * c), 0.f));
-          else
-            dv[i] = fmaf(e.alpha, a, fmaf(e.beta, c, e.x_factor * x));
+            for (int i = 0; i < kEpiChunk; ++i)
+              dv[i] = fmaf(xf, xv[i], fmaxf(fmaf(al, __uint_as_float(raw_acc[i]), be * cv[i]), 0.f));
+          } else {
+#pragma unroll
+            for (int i = 0; i < kEpiChunk; ++i)
+              dv[i] = fmaf(al, __uint_as_float(raw_acc[i]), fmaf(be, cv[i], xf * xv[i]));
+          }
+        } else {
+          if (e.relu) {
+#pragma unroll
+            for (int i = 0; i < kEpiChunk; ++i)
+              dv[i] = fmaxf(fmaf(al, __uint_as_float(raw_acc[i]), be * cv[i]), 0.f);
+          } else {
+#pragma unroll
+            for (int i = 0; i < kEpiChunk; ++i)
+              dv[i] = fmaf(al, __uint_as_float(raw_acc[i]), be * cv[i]);
+          }
         }
         smem_write_row(slot, e.d_dt, e.cd_m_major, r, dv);
-        if (e.write_y) smem_write_row(slot + e.cd_bytes, e.y_dt, e.cd_m_major, r, yv);
+        if (e.write_y) {
+          float yv[kEpiChunk];
+#pragma unroll
+          for (int i = 0; i < kEpiChunk; ++i) yv[i] = __uint_as_float(raw_acc[i]);
+          smem_write_row(slot + e.cd_bytes, e.y_dt, e.cd_m_major, r, yv);
+        }
         fence_proxy_async_smem();
         named_barrier_sync(kEpiBarrier, 128);
         if (epi_leader) {
@@ -586,7 +685,10 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           // slot of chunk gc-1) is free once at most one store group -- this
           // chunk's -- still reads shared memory.
           bulk_wait_group_read<1>();
-          if (loads) issue_loads(gc + E - 1);
+          if (loads) {
+            issue_loads();
+            issue_prefetch();
+          }
         }
         __syncwarp();                       // the leader's warp reconverges
       }
