@@ -25,8 +25,10 @@
 //               tile is processed in 32-column chunks through a ring of `slots`
 //               shared-memory slots: C and X sub-tiles are TMA-loaded `slots-1`
 //               chunks ahead (across tile boundaries, so the next tile's C/X arrive
-//               during its main loop); each thread reads its row, computes in fp32,
-//               writes D and Y back into the slot, and one thread TMA-stores them.
+//               during its main loop) by one thread, and prefetched into L2 further
+//               ahead when only two slots fit; each thread reads its row, computes
+//               in fp32, writes D and Y back into the slot, and a thread of another
+//               warp TMA-stores them.
 // Every cluster walks the same static persistent tile sequence
 // t = cluster_id, cluster_id + num_clusters, ...; with two accumulator stages the
 // epilogue of tile i overlaps the main loop of tile i+1.
@@ -94,7 +96,8 @@ constexpr int kAccStages = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kEpiChunk = 32;          // columns per epilogue chunk
 constexpr int kPrefetchChunks = 4;     // C/X chunks prefetched into L2 beyond the slot loads
-constexpr int kEpiLeader = 64;         // thread that issues the epilogue's TMA
+constexpr int kEpiLeader = 64;         // thread that issues the epilogue's TMA stores
+constexpr int kEpiLoader = 96;         // thread that issues the epilogue's TMA loads
 constexpr uint32_t kEpiBarrier = 1;    // named barrier of the 128 epilogue threads
 
 template <int CG, int BN, int AB_BYTES, int MC>
@@ -503,12 +506,17 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     const int q = warp & 3;                 // TMEM lane quarter this warp may read
     const int r = q * 32 + lane;            // this thread's row within the CTA's 128
     const bool epi_leader = threadIdx.x == kEpiLeader;
+    const bool epi_loader = threadIdx.x == kEpiLoader;
+    // L2 prefetch runs ahead of the slot loads only when shared memory holds
+    // just two slots (loads one chunk ahead); with more slots the loads
+    // already run far enough ahead and the extra TMA issue would cost more.
+    const int n_prefetch = E == 2 ? kPrefetchChunks : 0;
     const bool loads = e.read_c || e.read_x;
     const uint32_t load_tx = (e.read_c ? sub_bytes(e.c_dt) : 0u) + (e.read_x ? sub_bytes(e.x_dt) : 0u);
     const uint64_t pol_in = make_l2_policy((p.l2_hints >> 2) & 3u);
     const uint64_t pol_out = make_l2_policy((p.l2_hints >> 4) & 3u);
 
-    // The epilogue leader walks this CTA's stream of chunks (CHUNKS per whole
+    // The epilogue loader walks this CTA's stream of chunks (CHUNKS per whole
     // tile, CHUNKS / 2 per half-width item, in item order) with two cursors:
     // `ld` issues the TMA loads of C/X into the slots, E - 1 chunks ahead of
     // the chunk being processed, and `pf` prefetches into L2 the chunks
@@ -541,7 +549,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     Cursor ld{cluster_id, 0, 0, 0, 0, 0};
     Cursor pf{cluster_id, 0, 0, 0, 0, 0};
     int ld_slot = 0;
-    auto issue_loads = [&]() {              // epilogue leader only
+    auto issue_loads = [&]() {              // epilogue loader only
       if (ld.it < p.num_items) {
         int x0, x1;
         cursor_xy(ld, x0, x1);
@@ -554,7 +562,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       if (++ld_slot == E) ld_slot = 0;
       cursor_next(ld);
     };
-    auto issue_prefetch = [&]() {           // epilogue leader only
+    auto issue_prefetch = [&]() {           // epilogue loader only
       if (pf.it < p.num_items) {
         int x0, x1;
         cursor_xy(pf, x0, x1);
@@ -567,17 +575,17 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     if (epi_leader) {
       prefetch_tensormap(&tmD);
       if (e.write_y) prefetch_tensormap(&tmY);
-      if (loads) {
-        if (e.read_c) prefetch_tensormap(&tmC);
-        if (e.read_x) prefetch_tensormap(&tmX);
-        cursor_enter(ld);
-        cursor_enter(pf);
-        for (int c = 0; c < E - 1; ++c) {
-          issue_loads();
-          cursor_next(pf);
-        }
-        for (int c = 0; c < kPrefetchChunks; ++c) issue_prefetch();
+    }
+    if (epi_loader && loads) {
+      if (e.read_c) prefetch_tensormap(&tmC);
+      if (e.read_x) prefetch_tensormap(&tmX);
+      cursor_enter(ld);
+      cursor_enter(pf);
+      for (int c = 0; c < E - 1; ++c) {
+        issue_loads();
+        cursor_next(pf);
       }
+      for (int c = 0; c < n_prefetch; ++c) issue_prefetch();
     }
 
     int acc = 0;
@@ -673,6 +681,10 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           smem_write_row(slot + e.cd_bytes, e.y_dt, e.cd_m_major, r, yv);
         }
         fence_proxy_async_smem();
+        // The store of chunk gc-1 has finished reading its slot -- the slot that
+        // chunk gc+E-1 is loaded into, and that chunk gc+1 writes into -- before
+        // anyone passes the barrier below.
+        if (epi_leader) bulk_wait_group_read<0>();
         named_barrier_sync(kEpiBarrier, 128);
         if (epi_leader) {
           const int col0 = ncol0 + j * kEpiChunk;
@@ -681,16 +693,13 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           tma_store_3d(&tmD, s_addr, x0, x1, tl, pol_out);
           if (e.write_y) tma_store_3d(&tmY, s_addr + e.cd_bytes, x0, x1, tl, pol_out);
           bulk_commit_group();
-          // The slot of chunk gc+1 (and, with loads, of chunk gc+E-1, i.e. the
-          // slot of chunk gc-1) is free once at most one store group -- this
-          // chunk's -- still reads shared memory.
-          bulk_wait_group_read<1>();
-          if (loads) {
-            issue_loads();
-            issue_prefetch();
-          }
+        } else if (epi_loader && loads) {
+          // Meanwhile, in another warp: C/X of chunk gc+E-1, and an L2 prefetch
+          // further ahead.
+          issue_loads();
+          if (n_prefetch) issue_prefetch();
         }
-        __syncwarp();                       // the leader's warp reconverges
+        __syncwarp();                       // the issuing threads' warps reconverge
       }
       if (++acc == kAccStages) { acc = 0; aph ^= 1u; }
     }
