@@ -619,7 +619,7 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
                                 [cfg.tile_n == 256 ? 1 : 0][cfg.cluster_m - 1];
 
   cudaLaunchConfig_t lc{};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   lc.blockDim = dim3(gb300::kThreads);
   lc.dynamicSmemBytes = (size_t)cfg.smem_bytes;
   lc.stream = reinterpret_cast<cudaStream_t>(stream);
@@ -648,6 +648,12 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
   const int64_t clusters = std::min<int64_t>(cfg.tiles + cfg.tail_split, vs.max_clusters);
   cfg.grid_ctas = (int)(clusters * csize);
   lc.gridDim = dim3((unsigned)cfg.grid_ctas);
+  // Programmatic dependent launch: this grid may be scheduled while the
+  // previous kernel of the stream finishes; the kernel waits for that kernel
+  // (griddepcontrol.wait) before it touches global memory.
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  lc.numAttrs = 2;
 
   const bool a_mn = layoutA == GEMM_MN_MAJOR, b_mn = layoutB == GEMM_MN_MAJOR;
   CUtensorMap tmA, tmB;

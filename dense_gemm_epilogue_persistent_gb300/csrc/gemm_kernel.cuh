@@ -329,6 +329,10 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   constexpr int KIND = (AB_BYTES == 1) ? 1 : (AB_BYTES == 4 ? 2 : 0);
   constexpr bool MULTI = G::CLUSTER > 1;
 
+  // The next GEMM of the stream may start its prologue on SMs this grid leaves
+  // idle; it touches global memory only after its own dependency wait below.
+  grid_launch_dependents();
+
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzle atoms (identical in both CTAs of a pair:
   // same kernel, same layout).
@@ -383,6 +387,14 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     mbar_init(never_bar, 1);
     *abort_ptr = 0u;
     fence_barrier_init();
+    if (p.k_blocks > 0) {                    // A and B are encoded only when K > 0
+      prefetch_tensormap(&tmA);
+      prefetch_tensormap(&tmB);
+    }
+    prefetch_tensormap(&tmD);
+    if (p.epi.write_y) prefetch_tensormap(&tmY);
+    if (p.epi.read_c) prefetch_tensormap(&tmC);
+    if (p.epi.read_x) prefetch_tensormap(&tmX);
   }
   if (warp == 1) {
     tmem_alloc<CG>(holder, kTmemCols);
@@ -393,14 +405,16 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   if constexpr (MULTI) cluster_sync_all();
   tc_fence_after_sync();
   const uint32_t tmem_base = *holder_ptr;
+  // Everything above touched only this CTA's shared and tensor memory and the
+  // kernel parameters.  From here on global memory is read and written: wait
+  // for the previous grid of the stream (programmatic dependent launch).
+  grid_dependency_wait();
 
   const Watch w{abort_ptr, p.status, p.timeout_ns};
 
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer
     if (lane == 0) {
-      prefetch_tensormap(&tmA);
-      prefetch_tensormap(&tmB);
       const uint64_t pol = make_l2_policy(p.l2_hints & 3u);
       const uint32_t tx_bytes = (uint32_t)(CG * (G::A_STAGE + G::B_STAGE));
       int s = 0;
@@ -572,13 +586,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       cursor_next(pf);
     };
 
-    if (epi_leader) {
-      prefetch_tensormap(&tmD);
-      if (e.write_y) prefetch_tensormap(&tmY);
-    }
     if (epi_loader && loads) {
-      if (e.read_c) prefetch_tensormap(&tmC);
-      if (e.read_x) prefetch_tensormap(&tmX);
       cursor_enter(ld);
       cursor_enter(pf);
       for (int c = 0; c < E - 1; ++c) {

@@ -211,6 +211,18 @@ __device__ __forceinline__ void bulk_wait_group_read() {
   asm volatile("cp.async.bulk.wait_group.read %0;" :: "n"(N) : "memory");
 }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel of
+// the stream (if launched with programmatic stream serialization) be
+// scheduled once every CTA of this grid has issued it or exited;
+// dependency_wait blocks until the previous grid of the stream has completed
+// and its memory operations are visible (at once if there is no such grid).
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Wait until every committed bulk group has fully completed.
 __device__ __forceinline__ void bulk_wait_group_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");

@@ -432,6 +432,45 @@ def test_lda_ldb_padding(gemm):
     compare_full(prep, D, None)
 
 
+def test_dependent_launch_chain(gemm):
+    """Back-to-back dependent GEMMs on one stream, no host syncs (the kernel is
+    launched with programmatic stream serialization and waits on the previous
+    grid before touching global memory): D1 = A1 B1^T feeds GEMM 2 as A
+    (read after write), and GEMM 3 overwrites GEMM 2's B (write after read).
+    Integer inputs keep every value exact, so each iteration's D2 must equal
+    the oracle bit for bit."""
+    gemm.set_config(None)
+    g = torch.Generator().manual_seed(91)
+    M, K, N, N2 = 256, 64, 128, 192
+    ri = lambda *sh: torch.randint(-2, 3, sh, generator=g).to(torch.float16)
+    A1, B1, B2 = ri(1, M, K), ri(1, N, K), ri(1, N2, N)
+    dev = torch.device("cuda")
+    A1d, B1d, B2_orig = A1.to(dev), B1.to(dev), B2.to(dev)
+    B2d = torch.empty_like(B2_orig)
+    D1 = torch.empty(1, M, N, dtype=torch.float16, device=dev)
+    A3 = torch.ones(1, N2, K, dtype=torch.float16, device=dev)
+    dt16 = G.make_dtypes("f16", "f32", "f16")
+    dt32 = G.make_dtypes("f16", "f32", "f32")
+    outs = []
+    for it in range(12):
+        B2d.copy_(B2_orig)
+        gemm.run(M, N, K, 1, A1d, K, 0, B1d, K, 0, None, None, D1, None, 1.0, 0.0, 0.0, dt16)
+        D2 = torch.empty(1, M, N2, dtype=torch.float32, device=dev)
+        gemm.run(M, N2, N, 1, D1, N, 0, B2d, N, 0, None, None, D2, None, 1.0, 0.0, 0.0, dt32)
+        # overwrite GEMM 2's B with (A3 B1^T), a different integer matrix
+        gemm.run(N2, N, K, 1, A3, K, 0, B1d, K, 0, None, None, B2d, None, 1.0, 0.0, 0.0, dt16)
+        outs.append(D2)
+    _finish(gemm)
+    st = W.storage_view_np
+    p1 = oracle.Problem(M, N, K, 1, st(A1), K, False, st(B1), K, False, None, None, "f16", alpha=1.0)
+    D1_ref = oracle.round_to("f16", oracle.gemm(p1)[0])        # exact integers in fp16 storage
+    p2 = oracle.Problem(M, N2, N, 1, D1_ref, N, False, st(B2), N, False, None, None, "f16",
+                        alpha=1.0)
+    want = oracle.gemm(p2)[0].astype(np.float32)
+    for D2 in outs:
+        np.testing.assert_array_equal(D2.cpu().numpy(), want)
+
+
 def test_streams_and_repeat_determinism(gemm):
     case = SMALL["efc_f16"]
     prep = prepare(case)
