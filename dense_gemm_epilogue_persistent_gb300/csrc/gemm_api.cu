@@ -44,9 +44,31 @@ constexpr int kDefaultEpiWaitNs = 0;
 constexpr int kSmemSlack = 1024 + 16;   // base alignment + abort flag + watchdog-test barrier
 
 struct VariantState {
-  int smem_set = 0;          // dynamic smem attribute last set
-  int max_clusters = 0;      // occupancy for that smem size
+  bool smem_attr_set = false;  // max dynamic smem attribute raised to the opt-in limit
+  int occ_smem = 0;            // dynamic smem size of the last occupancy query
+  int max_clusters = 0;        // resident clusters at that size
 };
+
+// Everything a launch needs, prepared once per distinct call.  A call whose
+// arguments (every field of the problem, byte for byte) and forced
+// configuration equal a cached entry's launches from it without planning or
+// encoding tensor maps again.
+struct LaunchKey {
+  gemm_problem_t problem;
+  uint64_t config_gen;       // bumped by gemm_set_config
+};
+
+struct LaunchEntry {
+  bool valid = false;
+  LaunchKey key;
+  gemm_config_t cfg{};
+  const void* kern = nullptr;
+  int cluster_ctas = 0;
+  CUtensorMap maps[6];       // A, B, C, X, D, Y
+  KernelParams kp{};
+};
+
+constexpr int kLaunchCacheEntries = 4;
 
 }  // namespace
 
@@ -62,6 +84,9 @@ struct gemm_handle {
   uint64_t timeout_ns = kDefaultTimeoutNs;
   VariantState variants[3][2][2][2];   // [ab 16/8/32][cta_group 1/2][tile_n 128/256][mc 1/2]
   int clusters_by_size[5] = {0, 0, 0, 0, 0};   // resident clusters of 1, 2, 4 CTAs
+  uint64_t config_gen = 0;
+  LaunchEntry cache[kLaunchCacheEntries];
+  int cache_next = 0;
   std::mutex mu;
 };
 
@@ -434,6 +459,138 @@ uint32_t make_idesc(int a_type, int b_type_, bool acc_f16, int cg, int bn, bool 
   return d;
 }
 
+// Plan the launch of problem `p` on handle `h` (which the caller holds
+// locked) and fill `ent`: configuration, kernel, grid, tensor maps and kernel
+// parameters (the status word and timeout are set at each launch).
+gemm_status_t prepare_launch(gemm_handle* h, const gemm_problem_t& p, LaunchEntry& ent) {
+  const int64_t M = p.M, N = p.N, K = p.K, L = p.L;
+  const void *A = p.A, *B = p.B, *C = p.C, *X = p.X;
+  void *D = p.D, *Y = p.Y;
+  const int64_t lda = p.lda, ldb = p.ldb;
+  const gemm_layout_t layoutA = p.layoutA, layoutB = p.layoutB;
+  const float alpha = p.alpha, beta = p.beta, x_factor = p.x_factor;
+  const gemm_dtypes_t* dtypes = &p.dtypes;
+  gemm_config_t cfg{};
+  const gemm_status_t st = plan(&p, h->sm_count, h->smem_optin, h->forced ? &h->forced_cfg : nullptr, &cfg,
+            h->clusters_by_size);
+  if (st != GEMM_OK) return st;
+
+  const int ab_bytes = dtype_bytes(dtypes->ab);
+  const int csize = cfg.cta_group * cfg.cluster_m;
+  const void* kern = gb300::kernel_for(ab_bytes, cfg.cta_group, cfg.tile_n, cfg.cluster_m);
+  if (!kern) return GEMM_ERR_UNSUPPORTED_CONFIG;
+  VariantState& vs = h->variants[ab_bytes == 2 ? 0 : ab_bytes == 1 ? 1 : 2][cfg.cta_group - 1]
+                                [cfg.tile_n == 256 ? 1 : 0][cfg.cluster_m - 1];
+
+  cudaLaunchConfig_t lc{};
+  cudaLaunchAttribute attr[1];
+  lc.blockDim = dim3(gb300::kThreads);
+  lc.dynamicSmemBytes = (size_t)cfg.smem_bytes;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)csize;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+
+  // The attribute is raised once to the device's opt-in limit, so that every
+  // prepared launch of this kernel (cached ones included) may use any size.
+  if (!vs.smem_attr_set) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             h->smem_optin) != cudaSuccess) {
+      cudaGetLastError();
+      return GEMM_ERR_CUDA;
+    }
+    vs.smem_attr_set = true;
+  }
+  if (vs.occ_smem != cfg.smem_bytes) {
+    int nclusters = 0;
+    lc.gridDim = dim3((unsigned)(csize * h->sm_count));
+    if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &lc) != cudaSuccess || nclusters <= 0) {
+      cudaGetLastError();
+      return GEMM_ERR_CUDA;
+    }
+    vs.occ_smem = cfg.smem_bytes;
+    vs.max_clusters = nclusters;
+  }
+  const int64_t clusters = std::min<int64_t>(cfg.tiles + cfg.tail_split, vs.max_clusters);
+  cfg.grid_ctas = (int)(clusters * csize);
+
+  const bool a_mn = layoutA == GEMM_MN_MAJOR, b_mn = layoutB == GEMM_MN_MAJOR;
+  CUtensorMap tmA, tmB;
+  std::memset(&tmA, 0, sizeof(tmA));
+  std::memset(&tmB, 0, sizeof(tmB));
+  if (K > 0) {
+    if (!encode_operand(h->encode, &tmA, A, dtypes->ab, M, K, L, lda, a_mn, 128, cfg.tile_k) ||
+        !encode_operand(h->encode, &tmB, B, dtypes->ab, N, K, L, ldb, b_mn,
+                        cfg.tile_n / cfg.cta_group / cfg.cluster_m, cfg.tile_k))
+      return GEMM_ERR_CUDA;
+  }
+
+  const bool cd_m = dtypes->cdxy_major == GEMM_MN_MAJOR;
+  CUtensorMap tmC, tmX, tmD, tmY;
+  std::memset(&tmC, 0, sizeof(tmC));
+  std::memset(&tmX, 0, sizeof(tmX));
+  std::memset(&tmY, 0, sizeof(tmY));
+  if (!encode_epi(h->encode, &tmD, D, dtypes->d, M, N, L, cd_m) ||
+      (reads_c(p) && !encode_epi(h->encode, &tmC, C, dtypes->c, M, N, L, cd_m)) ||
+      (reads_x(p) && !encode_epi(h->encode, &tmX, X, dtypes->x, M, N, L, cd_m)) ||
+      (Y && !encode_epi(h->encode, &tmY, Y, dtypes->y, M, N, L, cd_m)))
+    return GEMM_ERR_CUDA;
+
+  KernelParams kp{};
+  kp.M = (int)M; kp.N = (int)N; kp.K = (int)K; kp.L = (int)L;
+  kp.tiles_m = (int)cdiv(M, (int64_t)cfg.tile_m * cfg.cluster_m);
+  kp.tiles_n = (int)cdiv(N, cfg.tile_n);
+  kp.num_tiles = (int)cfg.tiles;
+  kp.k_blocks = (int)cdiv(K, cfg.tile_k);
+  kp.group_m = cfg.group_m;
+  kp.stages = cfg.stages;
+  kp.a_mn_major = a_mn;
+  kp.b_mn_major = b_mn;
+  const bool acc_f16 = dtypes->acc == GEMM_F16;
+  kp.idesc = make_idesc(dtypes->ab, b_type(*dtypes), acc_f16, cfg.cta_group, cfg.tile_n, a_mn,
+                        b_mn);
+  kp.idesc_half = make_idesc(dtypes->ab, b_type(*dtypes), acc_f16, cfg.cta_group, cfg.tile_n / 2,
+                             a_mn, b_mn);
+  kp.split_start = (int)(cfg.tiles - cfg.tail_split);
+  kp.num_items = (int)(cfg.tiles + cfg.tail_split);
+  kp.l2_hints = (uint32_t)cfg.l2_hints;
+  kp.epi_wait_ns = (uint32_t)cfg.epi_wait_ns;
+  kp.inject_stall = cfg.inject_stall;
+  kp.status = h->d_status;
+  kp.timeout_ns = h->timeout_ns;
+  kp.epi.c_dt = dtypes->c;
+  kp.epi.d_dt = dtypes->d;
+  kp.epi.x_dt = dtypes->x;
+  kp.epi.y_dt = dtypes->y;
+  kp.epi.cd_m_major = cd_m;
+  kp.epi.read_c = reads_c(p);
+  kp.epi.read_x = reads_x(p);
+  kp.epi.write_y = Y != nullptr;
+  kp.epi.alpha = alpha;
+  kp.epi.beta = beta;
+  kp.epi.x_factor = x_factor;
+  kp.epi.relu = dtypes->epilogue == GEMM_EPI_RELU;
+  kp.epi.acc_f16 = acc_f16;
+  kp.epi.slots = cfg.epi_slots;
+  {
+    const int sub = 128 * gb300::kEpiChunk;
+    int cd = dtype_bytes(dtypes->d);
+    if (reads_c(p)) cd = std::max(cd, dtype_bytes(dtypes->c));
+    kp.epi.cd_bytes = (uint32_t)(sub * cd);
+    kp.epi.xy_bytes = (uint32_t)(cfg.epi_slot_bytes - sub * cd);
+  }
+
+  ent.cfg = cfg;
+  ent.kern = kern;
+  ent.cluster_ctas = csize;
+  ent.maps[0] = tmA; ent.maps[1] = tmB; ent.maps[2] = tmC;
+  ent.maps[3] = tmX; ent.maps[4] = tmD; ent.maps[5] = tmY;
+  ent.kp = kp;
+  return GEMM_OK;
+}
+
 }  // namespace
 
 // ====================================================================== C ABI
@@ -560,6 +717,7 @@ GEMM_API gemm_status_t gemm_set_config(gemm_handle_t h, const gemm_config_t* cfg
   std::lock_guard<std::mutex> g(h->mu);
   if (!cfg) {
     h->forced = false;
+    ++h->config_gen;
     return GEMM_OK;
   }
   if ((cfg->cta_group && cfg->cta_group != 1 && cfg->cta_group != 2) ||
@@ -572,6 +730,7 @@ GEMM_API gemm_status_t gemm_set_config(gemm_handle_t h, const gemm_config_t* cfg
     return GEMM_ERR_INVALID_ARG;
   h->forced = true;
   h->forced_cfg = *cfg;
+  ++h->config_gen;
   return GEMM_OK;
 }
 
@@ -606,127 +765,59 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
   }
 
   std::lock_guard<std::mutex> guard(h->mu);
-  gemm_config_t cfg{};
-  st = plan(&p, h->sm_count, h->smem_optin, h->forced ? &h->forced_cfg : nullptr, &cfg,
-            h->clusters_by_size);
-  if (st != GEMM_OK) return st;
-
-  const int ab_bytes = dtype_bytes(dtypes->ab);
-  const int csize = cfg.cta_group * cfg.cluster_m;
-  const void* kern = gb300::kernel_for(ab_bytes, cfg.cta_group, cfg.tile_n, cfg.cluster_m);
-  if (!kern) return GEMM_ERR_UNSUPPORTED_CONFIG;
-  VariantState& vs = h->variants[ab_bytes == 2 ? 0 : ab_bytes == 1 ? 1 : 2][cfg.cta_group - 1]
-                                [cfg.tile_n == 256 ? 1 : 0][cfg.cluster_m - 1];
+  LaunchKey key;
+  std::memset(&key, 0, sizeof(key));           // padding included: keys compare bytewise
+  key.problem.M = M; key.problem.N = N; key.problem.K = K; key.problem.L = L;
+  key.problem.A = A; key.problem.lda = lda; key.problem.layoutA = layoutA;
+  key.problem.B = B; key.problem.ldb = ldb; key.problem.layoutB = layoutB;
+  key.problem.C = C; key.problem.X = X; key.problem.D = D; key.problem.Y = Y;
+  key.problem.alpha = alpha; key.problem.beta = beta; key.problem.x_factor = x_factor;
+  key.problem.dtypes.ab = dtypes->ab; key.problem.dtypes.c = dtypes->c;
+  key.problem.dtypes.d = dtypes->d; key.problem.dtypes.x = dtypes->x;
+  key.problem.dtypes.y = dtypes->y; key.problem.dtypes.cdxy_major = dtypes->cdxy_major;
+  key.problem.dtypes.b = dtypes->b; key.problem.dtypes.epilogue = dtypes->epilogue;
+  key.problem.dtypes.acc = dtypes->acc;
+  key.config_gen = h->config_gen;
+  LaunchEntry* ent = nullptr;
+  for (LaunchEntry& c : h->cache)
+    if (c.valid && std::memcmp(&c.key, &key, sizeof(key)) == 0) { ent = &c; break; }
+  if (!ent) {
+    LaunchEntry& slot = h->cache[h->cache_next];
+    slot.valid = false;
+    st = prepare_launch(h, p, slot);
+    if (st != GEMM_OK) return st;
+    slot.key = key;
+    slot.valid = true;
+    h->cache_next = (h->cache_next + 1) % kLaunchCacheEntries;
+    ent = &slot;
+  }
 
   cudaLaunchConfig_t lc{};
   cudaLaunchAttribute attr[2];
+  lc.gridDim = dim3((unsigned)ent->cfg.grid_ctas);
   lc.blockDim = dim3(gb300::kThreads);
-  lc.dynamicSmemBytes = (size_t)cfg.smem_bytes;
+  lc.dynamicSmemBytes = (size_t)ent->cfg.smem_bytes;
   lc.stream = reinterpret_cast<cudaStream_t>(stream);
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)csize;
+  attr[0].val.clusterDim.x = (unsigned)ent->cluster_ctas;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  lc.attrs = attr;
-  lc.numAttrs = 1;
-
-  if (vs.smem_set != cfg.smem_bytes) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             cfg.smem_bytes) != cudaSuccess) {
-      cudaGetLastError();
-      return GEMM_ERR_CUDA;
-    }
-    int nclusters = 0;
-    lc.gridDim = dim3((unsigned)(csize * h->sm_count));
-    if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &lc) != cudaSuccess || nclusters <= 0) {
-      cudaGetLastError();
-      return GEMM_ERR_CUDA;
-    }
-    vs.smem_set = cfg.smem_bytes;
-    vs.max_clusters = nclusters;
-  }
-  const int64_t clusters = std::min<int64_t>(cfg.tiles + cfg.tail_split, vs.max_clusters);
-  cfg.grid_ctas = (int)(clusters * csize);
-  lc.gridDim = dim3((unsigned)cfg.grid_ctas);
   // Programmatic dependent launch: this grid may be scheduled while the
   // previous kernel of the stream finishes; the kernel waits for that kernel
   // (griddepcontrol.wait) before it touches global memory.
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
   lc.numAttrs = 2;
-
-  const bool a_mn = layoutA == GEMM_MN_MAJOR, b_mn = layoutB == GEMM_MN_MAJOR;
-  CUtensorMap tmA, tmB;
-  std::memset(&tmA, 0, sizeof(tmA));
-  std::memset(&tmB, 0, sizeof(tmB));
-  if (K > 0) {
-    if (!encode_operand(h->encode, &tmA, A, dtypes->ab, M, K, L, lda, a_mn, 128, cfg.tile_k) ||
-        !encode_operand(h->encode, &tmB, B, dtypes->ab, N, K, L, ldb, b_mn,
-                        cfg.tile_n / cfg.cta_group / cfg.cluster_m, cfg.tile_k))
-      return GEMM_ERR_CUDA;
-  }
-
-  const bool cd_m = dtypes->cdxy_major == GEMM_MN_MAJOR;
-  CUtensorMap tmC, tmX, tmD, tmY;
-  std::memset(&tmC, 0, sizeof(tmC));
-  std::memset(&tmX, 0, sizeof(tmX));
-  std::memset(&tmY, 0, sizeof(tmY));
-  if (!encode_epi(h->encode, &tmD, D, dtypes->d, M, N, L, cd_m) ||
-      (reads_c(p) && !encode_epi(h->encode, &tmC, C, dtypes->c, M, N, L, cd_m)) ||
-      (reads_x(p) && !encode_epi(h->encode, &tmX, X, dtypes->x, M, N, L, cd_m)) ||
-      (Y && !encode_epi(h->encode, &tmY, Y, dtypes->y, M, N, L, cd_m)))
-    return GEMM_ERR_CUDA;
-
-  KernelParams kp{};
-  kp.M = (int)M; kp.N = (int)N; kp.K = (int)K; kp.L = (int)L;
-  kp.tiles_m = (int)cdiv(M, (int64_t)cfg.tile_m * cfg.cluster_m);
-  kp.tiles_n = (int)cdiv(N, cfg.tile_n);
-  kp.num_tiles = (int)cfg.tiles;
-  kp.k_blocks = (int)cdiv(K, cfg.tile_k);
-  kp.group_m = cfg.group_m;
-  kp.stages = cfg.stages;
-  kp.a_mn_major = a_mn;
-  kp.b_mn_major = b_mn;
-  const bool acc_f16 = dtypes->acc == GEMM_F16;
-  kp.idesc = make_idesc(dtypes->ab, b_type(*dtypes), acc_f16, cfg.cta_group, cfg.tile_n, a_mn,
-                        b_mn);
-  kp.idesc_half = make_idesc(dtypes->ab, b_type(*dtypes), acc_f16, cfg.cta_group, cfg.tile_n / 2,
-                             a_mn, b_mn);
-  kp.split_start = (int)(cfg.tiles - cfg.tail_split);
-  kp.num_items = (int)(cfg.tiles + cfg.tail_split);
-  kp.l2_hints = (uint32_t)cfg.l2_hints;
-  kp.epi_wait_ns = (uint32_t)cfg.epi_wait_ns;
-  kp.inject_stall = cfg.inject_stall;
-  kp.status = h->d_status;
-  kp.timeout_ns = h->timeout_ns;
-  kp.epi.c_dt = dtypes->c;
-  kp.epi.d_dt = dtypes->d;
-  kp.epi.x_dt = dtypes->x;
-  kp.epi.y_dt = dtypes->y;
-  kp.epi.cd_m_major = cd_m;
-  kp.epi.read_c = reads_c(p);
-  kp.epi.read_x = reads_x(p);
-  kp.epi.write_y = Y != nullptr;
-  kp.epi.alpha = alpha;
-  kp.epi.beta = beta;
-  kp.epi.x_factor = x_factor;
-  kp.epi.relu = dtypes->epilogue == GEMM_EPI_RELU;
-  kp.epi.acc_f16 = acc_f16;
-  kp.epi.slots = cfg.epi_slots;
-  {
-    const int sub = 128 * gb300::kEpiChunk;
-    int cd = dtype_bytes(dtypes->d);
-    if (reads_c(p)) cd = std::max(cd, dtype_bytes(dtypes->c));
-    kp.epi.cd_bytes = (uint32_t)(sub * cd);
-    kp.epi.xy_bytes = (uint32_t)(cfg.epi_slot_bytes - sub * cd);
-  }
-
-  void* args[7] = {&tmA, &tmB, &tmC, &tmX, &tmD, &tmY, &kp};
-  if (cudaLaunchKernelExC(&lc, kern, args) != cudaSuccess) {
+  ent->kp.status = h->d_status;
+  ent->kp.timeout_ns = h->timeout_ns;
+  void* args[7] = {&ent->maps[0], &ent->maps[1], &ent->maps[2], &ent->maps[3], &ent->maps[4],
+                   &ent->maps[5], &ent->kp};
+  if (cudaLaunchKernelExC(&lc, ent->kern, args) != cudaSuccess) {
     cudaGetLastError();
     return GEMM_ERR_CUDA;
   }
-  h->last = cfg;
+  h->last = ent->cfg;
   return GEMM_OK;
 }
 

@@ -471,6 +471,48 @@ def test_dependent_launch_chain(gemm):
         np.testing.assert_array_equal(D2.cpu().numpy(), want)
 
 
+def test_launch_cache_reuse_and_eviction(gemm):
+    """The handle caches prepared launches (plan, tensor maps, parameters) per
+    distinct call.  Six distinct problems cycled three times evict and refill
+    the cache; every result stays bit-exact, a forced configuration between
+    two identical calls takes effect, and new data behind the same pointers is
+    read anew."""
+    gemm.set_config(None)
+    shapes = [(256, 256, 64), (384, 128, 128), (128, 512, 64), (512, 256, 32), (256, 384, 96),
+              (640, 128, 64)]
+    cases = [Case(M=m, N=n, K=k, L=1, ab="f16", c="f32", d="f32", alpha=1.5, beta=-0.5,
+                  dist="int2", seed=100 + i) for i, (m, n, k) in enumerate(shapes)]
+    preps = [prepare(c) for c in cases]
+    for rnd in range(3):
+        for prep in preps:
+            D, Y = run_gpu(gemm, prep)
+            _finish(gemm)
+            compare_full(prep, D, Y, exact=True)
+    # identical call, forced configuration in between
+    prep = preps[0]
+    dev = torch.device("cuda")
+    A, B, C = prep.A.to(dev), prep.B.to(dev), prep.C.to(dev)
+    D = torch.empty(1, 256, 256, dtype=torch.float32, device=dev)
+    dt = G.make_dtypes("f16", "f32", "f32")
+    args = (256, 256, 64, 1, A, 64, 0, B, 64, 0, C, None, D, None, 1.5, -0.5, 0.0, dt)
+    gemm.run(*args)
+    first = gemm.last_config()
+    alt = (1, 128) if (first.cta_group, first.tile_n) != (1, 128) else (2, 256)
+    gemm.set_config(cta_group=alt[0], tile_n=alt[1])
+    gemm.run(*args)
+    forced = gemm.last_config()
+    assert (forced.cta_group, forced.tile_n) == alt
+    _finish(gemm)
+    compare_full(prep, D, None, exact=True)
+    # same pointers, new contents
+    A.zero_()
+    gemm.run(*args)
+    _finish(gemm)
+    want = oracle.round_to("f32", -0.5 * to_f64(prep.inp.C))
+    np.testing.assert_array_equal(D.cpu().numpy(), want)
+    gemm.set_config(None)
+
+
 def test_streams_and_repeat_determinism(gemm):
     case = SMALL["efc_f16"]
     prep = prepare(case)
