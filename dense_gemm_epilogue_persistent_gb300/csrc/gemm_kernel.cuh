@@ -25,10 +25,9 @@
 //               tile is processed in 32-column chunks through a ring of `slots`
 //               shared-memory slots: C and X sub-tiles are TMA-loaded `slots-1`
 //               chunks ahead (across tile boundaries, so the next tile's C/X arrive
-//               during its main loop) by one thread, and prefetched into L2 further
-//               ahead when only two slots fit; each thread reads its row, computes
-//               in fp32, writes D and Y back into the slot, and a thread of another
-//               warp TMA-stores them.
+//               during its main loop) by one thread; each thread reads its row,
+//               computes in fp32, writes D and Y back into the slot, and a thread
+//               of another warp TMA-stores them.
 // Every cluster walks the same static persistent tile sequence
 // t = cluster_id, cluster_id + num_clusters, ...; with two accumulator stages the
 // epilogue of tile i overlaps the main loop of tile i+1.
@@ -95,7 +94,6 @@ constexpr int kThreads = 192;
 constexpr int kAccStages = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kEpiChunk = 32;          // columns per epilogue chunk
-constexpr int kPrefetchChunks = 4;     // C/X chunks prefetched into L2 beyond the slot loads
 constexpr int kEpiLeader = 64;         // thread that issues the epilogue's TMA stores
 constexpr int kEpiLoader = 96;         // thread that issues the epilogue's TMA loads
 constexpr uint32_t kEpiBarrier = 1;    // named barrier of the 128 epilogue threads
@@ -521,22 +519,17 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     const int r = q * 32 + lane;            // this thread's row within the CTA's 128
     const bool epi_leader = threadIdx.x == kEpiLeader;
     const bool epi_loader = threadIdx.x == kEpiLoader;
-    // L2 prefetch runs ahead of the slot loads only when shared memory holds
-    // just two slots (loads one chunk ahead); with more slots the loads
-    // already run far enough ahead and the extra TMA issue would cost more.
-    const int n_prefetch = E == 2 ? kPrefetchChunks : 0;
     const bool loads = e.read_c || e.read_x;
     const uint32_t load_tx = (e.read_c ? sub_bytes(e.c_dt) : 0u) + (e.read_x ? sub_bytes(e.x_dt) : 0u);
     const uint64_t pol_in = make_l2_policy((p.l2_hints >> 2) & 3u);
     const uint64_t pol_out = make_l2_policy((p.l2_hints >> 4) & 3u);
 
     // The epilogue loader walks this CTA's stream of chunks (CHUNKS per whole
-    // tile, CHUNKS / 2 per half-width item, in item order) with two cursors:
-    // `ld` issues the TMA loads of C/X into the slots, E - 1 chunks ahead of
-    // the chunk being processed, and `pf` prefetches into L2 the chunks
-    // kPrefetchChunks beyond that.  A cursor computes an item's coordinates
-    // once, when it enters the item.  TMA coordinates are (column, row, batch)
-    // for row-major C/D/X/Y and (row, column, batch) for column-major ones.
+    // tile, CHUNKS / 2 per half-width item, in item order) with a cursor that
+    // issues the TMA loads of C/X into the slots, E - 1 chunks ahead of the
+    // chunk being processed.  The cursor computes an item's coordinates once,
+    // when it enters the item.  TMA coordinates are (column, row, batch) for
+    // row-major C/D/X/Y and (row, column, batch) for column-major ones.
     struct Cursor { int it, j, nch, row0, col0, tl; };
     auto cursor_enter = [&](Cursor& cc) {
       if (cc.it >= p.num_items) return;
@@ -561,7 +554,6 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       x1 = e.cd_m_major ? col : cc.row0;
     };
     Cursor ld{cluster_id, 0, 0, 0, 0, 0};
-    Cursor pf{cluster_id, 0, 0, 0, 0, 0};
     int ld_slot = 0;
     auto issue_loads = [&]() {              // epilogue loader only
       if (ld.it < p.num_items) {
@@ -576,24 +568,10 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       if (++ld_slot == E) ld_slot = 0;
       cursor_next(ld);
     };
-    auto issue_prefetch = [&]() {           // epilogue loader only
-      if (pf.it < p.num_items) {
-        int x0, x1;
-        cursor_xy(pf, x0, x1);
-        if (e.read_c) tma_prefetch_l2_3d(&tmC, x0, x1, pf.tl);
-        if (e.read_x) tma_prefetch_l2_3d(&tmX, x0, x1, pf.tl);
-      }
-      cursor_next(pf);
-    };
 
     if (epi_loader && loads) {
       cursor_enter(ld);
-      cursor_enter(pf);
-      for (int c = 0; c < E - 1; ++c) {
-        issue_loads();
-        cursor_next(pf);
-      }
-      for (int c = 0; c < n_prefetch; ++c) issue_prefetch();
+      for (int c = 0; c < E - 1; ++c) issue_loads();
     }
 
     int acc = 0;
@@ -702,10 +680,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           if (e.write_y) tma_store_3d(&tmY, s_addr + e.cd_bytes, x0, x1, tl, pol_out);
           bulk_commit_group();
         } else if (epi_loader && loads) {
-          // Meanwhile, in another warp: C/X of chunk gc+E-1, and an L2 prefetch
-          // further ahead.
-          issue_loads();
-          if (n_prefetch) issue_prefetch();
+          issue_loads();                    // meanwhile, in another warp: C/X of chunk gc+E-1
         }
         __syncwarp();                       // the issuing threads' warps reconverge
       }

@@ -182,15 +182,6 @@ __device__ __forceinline__ void tma_load_3d_pair_mc(uint32_t dst, const CUtensor
       : "memory");
 }
 
-// Prefetch one 3-D tiled box of a tensor into L2 (no shared memory, no
-// completion signal; coordinates follow the same rules as a load's).
-__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int32_t c0, int32_t c1,
-                                                   int32_t c2) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
-               :: "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
-}
-
 // 3-D tiled TMA store from this CTA's shared memory (bulk-group completion).
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int32_t c0,
                                              int32_t c1, int32_t c2, uint64_t pol) {
