@@ -336,6 +336,70 @@ def time_launches(torch, bound, stream, iters, warmup):
     return start.elapsed_time(end) / iters
 
 
+def time_reps(torch, bound, stream, iters, warmup=20, reps=5):
+    """Median and minimum (ms per launch) over `reps` repetitions of `iters`
+    back-to-back launches, after `warmup` untimed ones."""
+    for _ in range(warmup):
+        bound.launch(stream)
+    out = []
+    for _ in range(reps):
+        out.append(time_launches(torch, bound, stream, iters, 0))
+    out.sort()
+    return out[len(out) // 2], out[0]
+
+
+L2_BYTES = 129 * 10**6
+
+
+def time_cold_l2(torch, bound, stream, iters=20):
+    """Mean ms per launch with L2 scrubbed before each launch (a 512 MiB
+    buffer written on the same stream between launches; only the launch is
+    inside the events)."""
+    scrub = torch.empty(512 * 2**20, dtype=torch.uint8, device=bound.A.device)
+    total = 0.0
+    with torch.cuda.stream(stream):
+        for i in range(iters + 2):
+            scrub.fill_(i & 0xFF)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            bound.launch(stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if i >= 2:
+                total += e0.elapsed_time(e1)
+    del scrub
+    return total / iters
+
+
+def torch_cpu_seconds(w, inp, budget_s=20.0):
+    """The pages' own way of checking a result -- the custom-epilogue example
+    evaluates D on CPU tensors with PyTorch -- timed here on this host's cores:
+    fp32 matmul of the upcast inputs plus the fp32 epilogue, once, whole problem.
+    Skipped (None) when the problem would take longer than `budget_s` at
+    ~0.5 TFLOP/s."""
+    import torch
+    if w.flops / 0.5e12 > budget_s:
+        return None
+    fp8 = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+    up = lambda t, dt: (t.view(fp8[dt]) if dt in fp8 else t).float()
+    A, B = up(inp.A, w.ab), up(inp.B, w.b_type)
+    C = inp.C.float() if inp.C is not None else None
+    X = inp.X.float() if inp.X is not None else None
+    t0 = time.perf_counter()
+    acc = torch.bmm(A, B.transpose(1, 2))
+    D = w.alpha * acc
+    if C is not None and w.beta != 0:
+        D = D + w.beta * C
+    if w.relu:
+        D = torch.clamp_min(D, 0.0)
+    if X is not None and w.x_factor != 0:
+        D = D + w.x_factor * X
+    dt = time.perf_counter() - t0
+    del acc, D
+    return dt
+
+
 def main():
     args = parse_args()
     rank = int(os.environ.get("RANK", "0"))
@@ -502,20 +566,32 @@ def main():
         if not args.no_per_config:
             per_config = {}
             for name, wc in W.WORKLOADS.items():
-                if name == w.name:
-                    ms = kernel_ms
-                    c2 = cfg
-                else:
-                    bc = Bound(G, g, wc, W.make_inputs(wc), device)
-                    ms = time_launches(torch, bc, stream, iters=50, warmup=10)
-                    c2 = g.last_config()
-                    del bc
+                inp_c = inp if name == w.name else W.make_inputs(wc)
+                bc = bound if name == w.name else Bound(G, g, wc, inp_c, device)
+                # 20 warm-up and 100 timed back-to-back launches, median and
+                # minimum over 5 repetitions (L2 warm across launches)
+                ms, ms_min = time_reps(torch, bc, stream, iters=100)
+                c2 = g.last_config()
                 tf = wc.flops / (ms / 1e3) / 1e12
                 pk = tensor_peak(peaks, wc.ab)
-                per_config[name] = {"us": round(ms * 1e3, 2), "tflops": round(tf, 1),
-                                    "pct_of_peak": round(100 * tf / pk, 1), "peak_tflops": pk,
-                                    "kernel": f"{c2.tile_m}x{c2.tile_n} cta_group={c2.cta_group}"
-                                              f" stages={c2.stages} grid={c2.grid_ctas}"}
+                ent = {"us": round(ms * 1e3, 2), "us_min": round(ms_min * 1e3, 2),
+                       "tflops": round(tf, 1), "pct_of_peak": round(100 * tf / pk, 1),
+                       "peak_tflops": pk,
+                       "kernel": f"{c2.tile_m}x{c2.tile_n} cta_group={c2.cta_group}"
+                                 f" stages={c2.stages} grid={c2.grid_ctas}"}
+                if bc.nbytes_in() < L2_BYTES:
+                    # inputs fit in L2: also with L2 scrubbed before every launch
+                    cold = time_cold_l2(torch, bc, stream)
+                    ent["us_cold_l2"] = round(cold * 1e3, 2)
+                    ent["tflops_cold_l2"] = round(wc.flops / (cold / 1e3) / 1e12, 1)
+                if not args.no_cpu_baseline:
+                    tcpu = torch_cpu_seconds(wc, inp_c)
+                    if tcpu is not None:
+                        ent["torch_cpu_fp32_s"] = round(tcpu, 3)
+                        ent["torch_cpu_fp32_tflops"] = round(wc.flops / tcpu / 1e12, 3)
+                per_config[name] = ent
+                if bc is not bound:
+                    del bc
             st, _ = g.sync_status(stream.cuda_stream)
             if st != G.GEMM_OK:
                 raise SystemExit(f"per-config timing failed: {G.gemm_status_string(st)}")
