@@ -248,3 +248,24 @@ def test_plan_tail_split(lib):
     # multicast clusters share B across their groups: never split
     st, cfg = G.gemm_plan(p, 152, 232448, G.gemm_config_t(cta_group=2, tile_n=256, cluster_m=2))
     assert st == 0 and cfg.tail_split == 0
+
+
+def test_random_gpu_cases_are_valid_problems(lib):
+    """Every problem the randomised GPU parity test draws passes the host-side
+    validation (alignment, type combinations), so that test exercises the
+    kernel rather than the argument checks."""
+    import test_gpu_random as R
+    for i in range(R.N_CASES):
+        case, _ = R.draw_case(i)
+        dt = G.make_dtypes(case.ab, case.c or "f32", case.d, case.x or "f32", case.y or "f32",
+                           G.GEMM_MN_MAJOR if case.cd_m else G.GEMM_K_MAJOR, b=case.b,
+                           epilogue=G.GEMM_EPI_RELU if case.relu else G.GEMM_EPI_LINEAR,
+                           acc=case.acc)
+        es = W.ELEM_BYTES[case.ab]
+        lda = case.M if case.a_mn else case.K
+        ldb = case.N if case.b_mn else case.K
+        p = G.make_problem(case.M, case.N, case.K, case.L, 1 << 20, lda, int(case.a_mn),
+                           1 << 22, ldb, int(case.b_mn), (1 << 24) if case.c else None,
+                           (1 << 26) if case.x else None, 1 << 28, (1 << 30) if case.y else None,
+                           case.alpha, case.beta, case.xf, dt)
+        assert G.gemm_check(p) == G.GEMM_OK, (i, case)
