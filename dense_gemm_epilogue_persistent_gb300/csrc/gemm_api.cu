@@ -223,33 +223,43 @@ bool variant_supports(const gemm_problem_t& p, int cg, int bn, int mc) {
 }
 
 // Relative cost of running `tiles` tiles of one variant: waves of tiles times
-// the time of one tile, in units of one 128-byte-K-atom k-block of a 128 x 256
-// per-SM tile (512 tensor cycles).  A tile takes the longer of its main loop
-// and its epilogue.  Fitted to interleaved sweeps on GB300 of the benchmark
-// shapes (8192^3, 2048^3, 16 x 1024^2 x 4096, 4096^3 fp8/tf32, 3000 x 5000 x 4096):
-//   main loop per k-block  2x256: 1.0   1x256: 1.13   2x128: 1.3   1x128: 0.93;
-//     two CTA pairs sharing B by multicast: 0.985 (fewer 4-CTA clusters fit the
-//     GPCs -- 36 of 38 on GB300 -- which the wave count sees through `clusters`);
-//   fixed per tile (pipeline fill, epilogue tail): pair 17, single CTA 10;
-//   epilogue: tile_n/32 chunks; a chunk that waits for C/X loads costs about
-//     9 units (the load latency under load) spread over the slots - 1 chunks of
-//     lookahead, a store-only chunk about 1.5.
-//   a last wave split into half-width items (tail_split) costs ~0.6 of a wave
-//     (half the MMA work, but the same A traffic and stage overheads).
+// the time of one tile, in units of one 128-byte-K-atom k-block of a 256 x 256
+// CTA-pair tile.  A tile takes the longer of its main loop and its epilogue,
+// plus a fixed cost (pipeline fill, hand-offs, the tail of the epilogue).
+// Constants fitted (least squares on log time, variants compared within each
+// problem) to a GB300 sweep of every variant over 17 problems: 256^3 to 8192^3,
+// K from 256 to 8192, 16-bit, fp8 and tf32 inputs, fp32 and 16-bit epilogues with
+// and without C, X and Y, ragged and batched shapes:
+//   main loop per k-block  2x256: 1.0   1x256: 1.23   2x128: 0.72   1x128: 0.68;
+//   fixed per tile         2x256: 13.1  1x256: 10.6   2x128: 15.0   1x128: 11.0;
+//   epilogue: tile_n/32 chunks per CTA, each 1.64 + 0.043 per KB the chunk moves
+//     (C and X read, D and Y written, 128 x 32 elements each) + 6.0 spread over
+//     the slots - 1 chunks of C/X lookahead when it loads;
+//   a last wave split into half-width items (tail_split) costs ~0.6 of a wave.
+// Clusters of two CTA groups sharing B by multicast were never fastest in that
+// sweep, so the automatic choice leaves them out; a forced configuration may
+// still select them (their cost: the pair's, with the wave count of the 4-CTA
+// clusters that fit).
 double plan_cost(int64_t tiles, int64_t k_blocks, int cg, int mc, int bn, int64_t clusters,
-                 bool epi_loads, int epi_slots, bool can_split) {
+                 bool epi_loads, int epi_slots, double epi_kb, bool can_split) {
   clusters = std::max<int64_t>(1, clusters);
   const int64_t full = tiles / clusters, rem = tiles % clusters;
   const double waves =
       (double)full + (rem == 0 ? 0.0 : (can_split && 2 * rem <= clusters ? 0.6 : 1.0));
-  double per_kb;
-  if (bn == 256) per_kb = cg == 2 ? (mc == 2 ? 0.985 : 1.0) : 1.13;
-  else per_kb = cg == 2 ? 1.3 : 0.93;
-  const double fixed = cg == 2 ? 17.0 : 10.0;
-  const double main_loop = (double)k_blocks * per_kb + fixed;
-  const double chunk = epi_loads ? 9.0 / std::max(1, epi_slots - 1) : 1.5;
+  double per_kb, fixed;
+  if (bn == 256) {
+    per_kb = cg == 2 ? 1.0 : 1.23;
+    fixed = cg == 2 ? 13.1 : 10.6;
+  } else {
+    per_kb = cg == 2 ? 0.72 : 0.68;
+    fixed = cg == 2 ? 15.0 : 11.0;
+  }
+  (void)mc;
+  const double main_loop = (double)k_blocks * per_kb;
+  const double chunk =
+      1.64 + 0.043 * epi_kb + (epi_loads ? 6.0 / std::max(1, epi_slots - 1) : 0.0);
   const double epilogue = (double)(bn / gb300::kEpiChunk) * chunk;
-  return waves * std::max(main_loop, epilogue);
+  return waves * (std::max(main_loop, epilogue) + fixed);
 }
 
 // Whether the last wave of a variant may run as half-width items: CTA groups
@@ -294,12 +304,17 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
   const int fmc = forced ? forced->cluster_m : 0;
   int cg = 0, bn = 0, mc = 0;
   double best = 1e300;
+  // KB an epilogue chunk (128 x 32 elements of each tensor) moves per CTA.
+  const double epi_kb =
+      128.0 * gb300::kEpiChunk *
+      ((reads_c(p) ? dtype_bytes(p.dtypes.c) : 0) + (reads_x(p) ? dtype_bytes(p.dtypes.x) : 0) +
+       dtype_bytes(p.dtypes.d) + (p.Y ? dtype_bytes(p.dtypes.y) : 0)) / 1024.0;
   for (int a : {2, 1})
     for (int b : {256, 128})
       for (int m : {1, 2}) {
         if ((fcg && a != fcg) || (fbn && b != fbn)) continue;
-        // Automatic choice: multicast only for CTA pairs with 256-wide tiles.
-        if (fmc ? m != fmc : (m == 2 && !(a == 2 && b == 256))) continue;
+        // Automatic choice: no multicast clusters (see plan_cost).
+        if (fmc ? m != fmc : m == 2) continue;
         if (!variant_supports(p, a, b, m)) continue;
         const int64_t tiles = cdiv(std::max<int64_t>(p.M, 1), 128 * a * m) *
                               cdiv(std::max<int64_t>(p.N, 1), b) * std::max<int64_t>(p.L, 1);
@@ -307,6 +322,7 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
                                    resident_clusters(sm_count, clusters_by_size, a * m),
                                    reads_c(p) || reads_x(p),
                                    auto_slots(a, b, ab_bytes, epi_slot_bytes(p), smem_optin),
+                                   epi_kb,
                                    can_split_tail(p, a, b, m) &&
                                        !(forced && forced->tail_split == 1));
         if (c < best - 1e-9) { best = c; cg = a; bn = b; mc = m; }
