@@ -471,6 +471,51 @@ def test_dependent_launch_chain(gemm):
         np.testing.assert_array_equal(D2.cpu().numpy(), want)
 
 
+def test_cuda_graph_capture_and_replay(gemm):
+    """gemm_run calls captured into a CUDA graph (a dependent chain: D1 feeds
+    the second GEMM) replay to the same bits as the eager calls, also after
+    the inputs behind the captured pointers change."""
+    gemm.set_config(None)
+    g = torch.Generator().manual_seed(93)
+    M, K, N, N2 = 384, 128, 256, 192
+    dev = torch.device("cuda")
+    A1 = torch.randn(1, M, K, generator=g).to(torch.float16).to(dev)
+    B1 = torch.randn(1, N, K, generator=g).to(torch.float16).to(dev)
+    B2 = torch.randn(1, N2, N, generator=g).to(torch.float16).to(dev)
+    C2 = torch.randn(1, M, N2, generator=g).to(dev)
+    D1 = torch.empty(1, M, N, dtype=torch.float16, device=dev)
+    D2 = torch.empty(1, M, N2, dtype=torch.float32, device=dev)
+    dt16 = G.make_dtypes("f16", "f32", "f16")
+    dt32 = G.make_dtypes("f16", "f32", "f32")
+    s = torch.cuda.Stream()
+
+    def chain():
+        gemm.run(M, N, K, 1, A1, K, 0, B1, K, 0, None, None, D1, None, 1.0, 0.0, 0.0, dt16, s)
+        gemm.run(M, N2, N, 1, D1, N, 0, B2, N, 0, C2, None, D2, None, 0.5, -1.0, 0.0, dt32, s)
+
+    with torch.cuda.stream(s):
+        chain()
+    torch.cuda.synchronize()
+    want1, want2 = D1.clone(), D2.clone()
+    graph = torch.cuda.CUDAGraph()
+    D1.zero_(); D2.zero_()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph, stream=s):
+        chain()
+    for _ in range(3):
+        D1.zero_(); D2.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(D1, want1) and torch.equal(D2, want2)
+    # new data behind the captured pointers: the replay reads it
+    A1.mul_(-1)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(D1, -want1)
+    st, detail = gemm.sync_status()
+    assert st == G.GEMM_OK, detail
+
+
 def test_launch_cache_reuse_and_eviction(gemm):
     """The handle caches prepared launches (plan, tensor maps, parameters) per
     distinct call.  Six distinct problems cycled three times evict and refill
