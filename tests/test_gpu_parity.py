@@ -325,6 +325,24 @@ def test_f16_accumulator_bound_and_precision(gemm, variant, ab, b):
     gemm.set_config(None)
 
 
+def test_f16_accumulator_overflows_to_infinity(gemm):
+    """The fp16 accumulator's documented range: all-16 inputs give running sums
+    of 256 per k; at K = 240 the result (61440) is exact, from K = 256 on the
+    sum passes the fp16 maximum (65504) and Y and D are infinite (no
+    saturation)."""
+    gemm.set_config(None)
+    dev = torch.device("cuda")
+    dt = G.make_dtypes("f16", "f32", "f32", "f32", "f32", acc="f16")
+    for K, want in ((240, 61440.0), (256, float("inf")), (512, float("inf"))):
+        A = torch.full((1, 128, K), 16.0, dtype=torch.float16, device=dev)
+        B = torch.full((1, 136, K), 16.0, dtype=torch.float16, device=dev)
+        D = torch.empty(1, 128, 136, dtype=torch.float32, device=dev)
+        Y = torch.empty(1, 128, 136, dtype=torch.float32, device=dev)
+        gemm.run(128, 136, K, 1, A, K, 0, B, K, 0, None, None, D, Y, 0.5, 0.0, 0.0, dt)
+        _finish(gemm)
+        assert torch.all(Y == want) and torch.all(D == 0.5 * want), K
+
+
 def test_f16_accumulator_split_last_wave(gemm):
     """fp16 accumulation through the half-width items of a split last wave
     (100 pair tiles on 76 pairs: 24 split; the half-width instruction
