@@ -38,7 +38,10 @@ constexpr int kMaxStages = 12;
 constexpr int kMaxEpiSlots = 6;
 // Default L2 priorities: evict-first for every TMA copy (A/B loads, C/X loads,
 // D/Y stores).  Interleaved sustained sweeps on GB300 found it best or tied
-// on all five benchmark shapes (fp8 3000x5000x4096: +11% over evict-normal).
+// on all five benchmark shapes (fp8 3000x5000x4096: +11% over evict-normal);
+// 1500-launch runs under the power cap on 8192^3 (fp16 custom epilogue / bf16)
+// give 1450 / 1602 TFLOP/s against 1401 / 1559 with evict-normal A/B loads and
+// 1432 / 1600 with evict-last ones.
 constexpr int kDefaultL2Hints = 2 | (2 << 2) | (2 << 4);
 constexpr int kDefaultEpiWaitNs = 0;
 constexpr int kSmemSlack = 1024 + 16;   // base alignment + abort flag + watchdog-test barrier

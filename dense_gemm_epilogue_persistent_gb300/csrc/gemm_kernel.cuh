@@ -1,6 +1,8 @@
 // Persistent, warp-specialised batched GEMM with a fused epilogue for sm_103a.
 //
-//   Y = A*B,   D = alpha*(A*B) + beta*C + x_factor*X     (fp32 accumulate + epilogue)
+//   Y = A*B,   D = alpha*(A*B) + beta*C + x_factor*X
+//   (fp32 accumulation, or fp16 for fp16/fp8 inputs; fp32 epilogue; optional relu
+//   of alpha*(A*B) + beta*C before X is added)
 //
 // What the kernel computes and its warp roles follow "custom_epilogue_dense_gemm.py"
 // (CuTeDSL Blackwell example), module docstring "This GEMM works as follows" (DMA
@@ -30,7 +32,9 @@
 //               of another warp TMA-stores them.
 // Every cluster walks the same static persistent tile sequence
 // t = cluster_id, cluster_id + num_clusters, ...; with two accumulator stages the
-// epilogue of tile i overlaps the main loop of tile i+1.
+// epilogue of tile i overlaps the main loop of tile i+1.  The kernel touches
+// global memory only after griddepcontrol.wait, so a launch with programmatic
+// stream serialization overlaps its prologue with the previous grid's tail.
 //
 // Clusters: CG*MC CTAs = MC CTA groups (pairs when CG = 2) stacked along M.  The
 // groups of a cluster compute MC vertically adjacent tiles that share the same B
