@@ -95,6 +95,7 @@ def library():
             lib.gemm_destroy.argtypes = [vp]
             lib.gemm_run.argtypes = [vp, i64, i64, i64, i64, vp, i64, i32, vp, i64, i32, vp, vp,
                                      vp, vp, f32, f32, f32, ctypes.POINTER(gemm_dtypes_t), vp]
+            lib.gemm_run_host.argtypes = list(lib.gemm_run.argtypes)
             lib.gemm_sync_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
             lib.gemm_run_noalloc.argtypes = [i64, i64, i64, i64, vp, i64, i32, vp, i64, i32, vp,
                                              vp, vp, vp, f32, f32, f32,
@@ -170,6 +171,20 @@ def gemm_run(handle, M, N, K, L, A, lda, layoutA, B, ldb, layoutB, C, X, D, Y,
                             ctypes.byref(dtypes), _stream(stream))
     if check and st != GEMM_OK:
         raise GemmError(st, "gemm_run")
+    return st
+
+
+def gemm_run_host(handle, M, N, K, L, A, lda, layoutA, B, ldb, layoutB, C, X, D, Y,
+                  alpha, beta, x_factor, dtypes: gemm_dtypes_t, stream=None,
+                  check=True) -> int:
+    """gemm_run on HOST buffers (CPU tensors, pinned for overlap): the library
+    copies the inputs in, runs the GEMM and copies D and Y back, all enqueued
+    on `stream` (see the C header)."""
+    st = library().gemm_run_host(handle, M, N, K, L, _ptr(A), lda, layoutA, _ptr(B), ldb,
+                                 layoutB, _ptr(C), _ptr(X), _ptr(D), _ptr(Y), alpha, beta,
+                                 x_factor, ctypes.byref(dtypes), _stream(stream))
+    if check and st != GEMM_OK:
+        raise GemmError(st, "gemm_run_host")
     return st
 
 
@@ -263,6 +278,11 @@ class Gemm:
             x_factor, dtypes, stream=None):
         return gemm_run(self.handle, M, N, K, L, A, lda, layoutA, B, ldb, layoutB, C, X, D, Y,
                         alpha, beta, x_factor, dtypes, stream)
+
+    def run_host(self, M, N, K, L, A, lda, layoutA, B, ldb, layoutB, C, X, D, Y, alpha, beta,
+                 x_factor, dtypes, stream=None):
+        return gemm_run_host(self.handle, M, N, K, L, A, lda, layoutA, B, ldb, layoutB, C, X, D,
+                             Y, alpha, beta, x_factor, dtypes, stream)
 
     def sync_status(self, stream=None):
         return gemm_sync_status(self.handle, stream)

@@ -91,6 +91,9 @@ struct gemm_handle {
   LaunchEntry cache[kLaunchCacheEntries];
   int cache_next = 0;
   std::mutex mu;
+  void* ws = nullptr;          // gemm_run_host's device copies of its host buffers
+  size_t ws_bytes = 0;
+  std::mutex ws_mu;
 };
 
 namespace {
@@ -726,6 +729,7 @@ GEMM_API gemm_status_t gemm_destroy(gemm_handle_t h) {
   cudaGetDevice(&prev);
   cudaSetDevice(h->device);
   cudaFree(h->d_status);
+  if (h->ws) cudaFree(h->ws);
   cudaSetDevice(prev);
   delete h;
   return GEMM_OK;
@@ -837,6 +841,80 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
     return GEMM_ERR_CUDA;
   }
   h->last = ent->cfg;
+  return GEMM_OK;
+}
+
+GEMM_API gemm_status_t gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                                     int64_t L, const void* A, int64_t lda,
+                                     gemm_layout_t layoutA, const void* B, int64_t ldb,
+                                     gemm_layout_t layoutB, const void* C, const void* X,
+                                     void* D, void* Y, float alpha, float beta,
+                                     float x_factor, const gemm_dtypes_t* dtypes,
+                                     struct CUstream_st* stream) {
+  if (!h || !dtypes) return GEMM_ERR_INVALID_ARG;
+  gemm_problem_t p{M, N, K, L, A, lda, layoutA, B, ldb, layoutB, C, X, D, Y,
+                   alpha, beta, x_factor, *dtypes};
+  gemm_status_t st = validate(&p);
+  if (st != GEMM_OK) return st;
+  if (M == 0 || N == 0 || L == 0) return GEMM_OK;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device) {
+    cudaGetLastError();
+    return GEMM_ERR_INVALID_ARG;
+  }
+  // Element spans, first to last element: an operand with R rows of K (or K
+  // rows of R) per batch ends ld - (extent of its contiguous dimension)
+  // elements before a whole number of rows.
+  const size_t es = (size_t)dtype_bytes(dtypes->ab);
+  auto span = [](int64_t rows, int64_t ld, int64_t inner) {
+    return rows > 0 ? (size_t)((rows - 1) * ld + inner) : (size_t)0;
+  };
+  const bool a_mn = layoutA == GEMM_MN_MAJOR, b_mn = layoutB == GEMM_MN_MAJOR;
+  const size_t bytes_a = K > 0 ? es * (a_mn ? span(L * K, lda, M) : span(L * M, lda, K)) : 0;
+  const size_t bytes_b = K > 0 ? es * (b_mn ? span(L * K, ldb, N) : span(L * N, ldb, K)) : 0;
+  const size_t mnl = (size_t)M * (size_t)N * (size_t)L;
+  const size_t bytes_c = reads_c(p) ? mnl * dtype_bytes(dtypes->c) : 0;
+  const size_t bytes_x = reads_x(p) ? mnl * dtype_bytes(dtypes->x) : 0;
+  const size_t bytes_d = mnl * dtype_bytes(dtypes->d);
+  const size_t bytes_y = Y ? mnl * dtype_bytes(dtypes->y) : 0;
+  auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
+  const size_t off_b = up(bytes_a), off_c = off_b + up(bytes_b), off_x = off_c + up(bytes_c);
+  const size_t off_d = off_x + up(bytes_x), off_y = off_d + up(bytes_d);
+  const size_t need = off_y + up(bytes_y);
+  uint8_t* ws;
+  {
+    std::lock_guard<std::mutex> g(h->ws_mu);
+    if (h->ws_bytes < need) {
+      if (h->ws) cudaFree(h->ws);
+      h->ws = nullptr;
+      h->ws_bytes = 0;
+      if (cudaMalloc(&h->ws, need) != cudaSuccess) {
+        cudaGetLastError();
+        h->ws = nullptr;
+        return GEMM_ERR_CUDA;
+      }
+      h->ws_bytes = need;
+    }
+    ws = static_cast<uint8_t*>(h->ws);
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  auto h2d = [&](size_t off, const void* src, size_t n) {
+    return n == 0 || cudaMemcpyAsync(ws + off, src, n, cudaMemcpyHostToDevice, s) == cudaSuccess;
+  };
+  if (!h2d(0, A, bytes_a) || !h2d(off_b, B, bytes_b) || !h2d(off_c, C, bytes_c) ||
+      !h2d(off_x, X, bytes_x)) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  st = gemm_run(h, M, N, K, L, K > 0 ? ws : nullptr, lda, layoutA, K > 0 ? ws + off_b : nullptr,
+                ldb, layoutB, bytes_c ? ws + off_c : nullptr, bytes_x ? ws + off_x : nullptr,
+                ws + off_d, Y ? ws + off_y : nullptr, alpha, beta, x_factor, dtypes, stream);
+  if (st != GEMM_OK) return st;
+  if (cudaMemcpyAsync(D, ws + off_d, bytes_d, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      (Y && cudaMemcpyAsync(Y, ws + off_y, bytes_y, cudaMemcpyDeviceToHost, s) != cudaSuccess)) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
   return GEMM_OK;
 }
 

@@ -170,8 +170,8 @@ typedef struct {
  * and allocates a 4-byte device status word.  *out is NULL on failure. */
 gemm_status_t gemm_create(gemm_handle_t* out, int device);
 
-/* Release the handle and its status word.  NULL is accepted (no-op).  Work
- * already enqueued with this handle must be complete. */
+/* Release the handle, its status word and its host-call workspace.  NULL is
+ * accepted (no-op).  Work already enqueued with this handle must be complete. */
 gemm_status_t gemm_destroy(gemm_handle_t h);
 
 /* Enqueue D = alpha*(A*B) + beta*C + x_factor*X (and Y = A*B) on `stream`.
@@ -197,6 +197,30 @@ gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K, int64_t
                        const void* C, const void* X, void* D, void* Y,
                        float alpha, float beta, float x_factor,
                        const gemm_dtypes_t* dtypes, struct CUstream_st* stream);
+
+/* The same GEMM on HOST buffers.  A, B, C, X are read from host memory and D,
+ * Y written back to host memory through a device workspace the handle owns:
+ * on `stream`, in order, the inputs are copied to the device (each tensor's
+ * element span, from its first to its last element), the GEMM runs on the
+ * copies, and D and Y are copied back.  Returns once all of it is enqueued.
+ *
+ * Arguments, layouts, validation and result are gemm_run's (alignment is
+ * checked on the host pointers).  The host buffers must stay valid, inputs
+ * unmodified and outputs unread, until `stream` has passed the call
+ * (gemm_sync_status, or a stream synchronisation).  Page-locked (pinned) host
+ * memory lets the copies run asynchronously and overlap other streams;
+ * pageable memory works, with copies that synchronise with the host.
+ *
+ * The workspace grows to the largest call seen (cudaMalloc, which
+ * synchronises the device) and is freed by gemm_destroy.  Calls on one handle
+ * share it, so they must be ordered (one stream, or synchronised); to overlap
+ * calls, use one handle per stream.  Copy failures return GEMM_ERR_CUDA. */
+gemm_status_t gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K, int64_t L,
+                            const void* A, int64_t lda, gemm_layout_t layoutA,
+                            const void* B, int64_t ldb, gemm_layout_t layoutB,
+                            const void* C, const void* X, void* D, void* Y,
+                            float alpha, float beta, float x_factor,
+                            const gemm_dtypes_t* dtypes, struct CUstream_st* stream);
 
 /* Synchronise `stream`, then read and clear the handle's device status word.
  * Returns GEMM_ERR_DEVICE_TIMEOUT if any kernel since the last call hit its

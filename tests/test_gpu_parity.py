@@ -576,6 +576,79 @@ def test_launch_cache_reuse_and_eviction(gemm):
     gemm.set_config(None)
 
 
+def _run_host(gemm, prep, pinned=True, stream=None):
+    """gemm_run_host on the CPU storage of a prepared case.  Returns the host D
+    and Y (valid once the stream has passed the call) and the host inputs,
+    which the caller keeps alive until then (the copies read them
+    asynchronously)."""
+    from gemm_cases import out_shape
+    c = prep.case
+    pin = (lambda t: t.pin_memory()) if pinned else (lambda t: t)
+    A, B = pin(prep.A), pin(prep.B)
+    C = pin(prep.C) if prep.C is not None else None
+    X = pin(prep.X) if prep.X is not None else None
+    D = torch.empty(out_shape(c), dtype=W.TORCH_DTYPE[c.d], pin_memory=pinned)
+    Y = torch.empty(out_shape(c), dtype=W.TORCH_DTYPE[c.y], pin_memory=pinned) if c.y else None
+    dt = G.make_dtypes(c.ab, c.c or "f32", c.d, c.x or "f32", c.y or "f32",
+                       G.GEMM_MN_MAJOR if c.cd_m else G.GEMM_K_MAJOR, b=c.b,
+                       epilogue=G.GEMM_EPI_RELU if c.relu else G.GEMM_EPI_LINEAR, acc=c.acc)
+    gemm.run_host(c.M, c.N, c.K, c.L, A, A.shape[-1], int(c.a_mn), B, B.shape[-1], int(c.b_mn),
+                  C, X, D, Y, c.alpha, c.beta, c.xf, dt, stream)
+    return D, Y, (A, B, C, X)
+
+
+def test_run_host_matches_device_path(gemm):
+    """gemm_run_host (host buffers, copies through the handle's workspace) gives
+    the device path's bits: pinned and pageable buffers, an M-major A with a
+    padded leading dimension, batches, C/X/D/Y, a workspace that grows then is
+    reused by a smaller call, and K = 0."""
+    gemm.set_config(None)
+    cases = [
+        Case(M=296, N=264, K=200, L=2, ab="f16", c="f16", d="f16", x="bf16", y="f32",
+             a_mn=True, lda_pad=8, alpha=1.5, beta=-0.5, xf=0.25, seed=95),
+        Case(M=1024, N=1536, K=512, L=1, ab="bf16", c="f32", d="bf16", y="bf16", b_mn=True,
+             cd_m=True, alpha=1.0, beta=1.0, seed=96),
+        Case(M=200, N=136, K=0, L=3, ab="f16", c="f32", d="f32", x="f16", alpha=1.0, beta=2.0,
+             xf=-1.0, seed=97),
+        Case(M=384, N=512, K=256, L=1, ab="e4m3", b="e5m2", c="f16", d="f16", relu=True,
+             alpha=0.5, beta=1.0, dist="e4m3_pm4", seed=98),
+    ]
+    for pinned in (True, False):
+        for case in cases:
+            prep = prepare(case)
+            D_dev, Y_dev = run_gpu(gemm, prep)
+            D, Y, keep = _run_host(gemm, prep, pinned)
+            _finish(gemm)
+            del keep
+            assert torch.equal(D, D_dev.cpu()), (case, pinned)
+            if Y is not None:
+                assert torch.equal(Y, Y_dev.cpu()), (case, pinned)
+
+
+def test_run_host_two_handles_overlap(gemm):
+    """Calls on host buffers overlap across two handles on two streams (each
+    handle owns its workspace); every result matches the device path."""
+    gemm.set_config(None)
+    h2 = G.Gemm(0)
+    try:
+        streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+        handles = [gemm, h2]
+        preps = [prepare(Case(M=512, N=640, K=384, L=2, ab="f16", c="f16", d="f16", y="f16",
+                              alpha=1.0, beta=0.5, seed=110 + i)) for i in range(6)]
+        want = [tuple(t.cpu() for t in run_gpu(gemm, pr)) for pr in preps]
+        _finish(gemm)
+        got = []
+        for i, pr in enumerate(preps):
+            got.append(_run_host(handles[i % 2], pr, True, streams[i % 2].cuda_stream))
+        torch.cuda.synchronize()
+        for (D, Y, _), (Dw, Yw) in zip(got, want):
+            assert torch.equal(D, Dw) and torch.equal(Y, Yw)
+        st, _ = h2.sync_status()
+        assert st == G.GEMM_OK
+    finally:
+        h2.close()
+
+
 def test_streams_and_repeat_determinism(gemm):
     case = SMALL["efc_f16"]
     prep = prepare(case)
