@@ -33,6 +33,7 @@ GEMM_ERR_UNSUPPORTED_CONFIG = 7
 GEMM_F32, GEMM_F16, GEMM_BF16, GEMM_E4M3, GEMM_E5M2, GEMM_TF32 = 0, 1, 2, 3, 4, 5
 GEMM_K_MAJOR, GEMM_MN_MAJOR = 0, 1
 GEMM_EPI_LINEAR, GEMM_EPI_RELU = 0, 1
+GEMM_RING_STAT_WORDS = 12
 
 DTYPE_CODES = {"f32": GEMM_F32, "f16": GEMM_F16, "bf16": GEMM_BF16, "e4m3": GEMM_E4M3,
                "e5m2": GEMM_E5M2, "tf32": GEMM_TF32}
@@ -80,6 +81,16 @@ _lock = threading.Lock()
 _lib = None
 
 
+def select_library(path: str) -> None:
+    """Load the library at `path` instead of the product one (the
+    ring-statistics build, for instance).  Must precede the first call."""
+    global LIB_PATH
+    with _lock:
+        if _lib is not None and os.path.abspath(path) != os.path.abspath(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is already loaded")
+        LIB_PATH = path
+
+
 def library():
     """Load libgemm_gb300.so (raises if it has not been built)."""
     global _lib
@@ -96,6 +107,8 @@ def library():
             lib.gemm_run.argtypes = [vp, i64, i64, i64, i64, vp, i64, i32, vp, i64, i32, vp, vp,
                                      vp, vp, f32, f32, f32, ctypes.POINTER(gemm_dtypes_t), vp]
             lib.gemm_run_host.argtypes = list(lib.gemm_run.argtypes)
+            lib.gemm_ring_stats.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint64), i32,
+                                            ctypes.POINTER(ctypes.c_int)]
             lib.gemm_sync_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_uint32)]
             lib.gemm_run_noalloc.argtypes = [i64, i64, i64, i64, vp, i64, i32, vp, i64, i32, vp,
                                              vp, vp, vp, f32, f32, f32,
@@ -283,6 +296,19 @@ class Gemm:
                  x_factor, dtypes, stream=None):
         return gemm_run_host(self.handle, M, N, K, L, A, lda, layoutA, B, ldb, layoutB, C, X, D,
                              Y, alpha, beta, x_factor, dtypes, stream)
+
+    def ring_stats(self, stream=None):
+        """Per-CTA ring counters of the last launch (statistics build only):
+        a list of GEMM_RING_STAT_WORDS-long lists, CTA by CTA."""
+        max_ctas = 1024
+        buf = (ctypes.c_uint64 * (max_ctas * GEMM_RING_STAT_WORDS))()
+        n = ctypes.c_int(0)
+        st = library().gemm_ring_stats(self.handle, _stream(stream), buf, max_ctas,
+                                       ctypes.byref(n))
+        if st != GEMM_OK:
+            raise GemmError(st, "gemm_ring_stats")
+        w = GEMM_RING_STAT_WORDS
+        return [list(buf[i * w:(i + 1) * w]) for i in range(n.value)]
 
     def sync_status(self, stream=None):
         return gemm_sync_status(self.handle, stream)

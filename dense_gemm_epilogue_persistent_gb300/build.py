@@ -20,6 +20,11 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build", "gemm_gb300")
 LIB = os.path.join(HERE, "libgemm_gb300.so")
+# The ring-statistics build: the same sources with per-role wait counters
+# compiled in (GB300_RING_STATS=1), a separate library for studying the
+# pipeline; the product library compiles none of it.
+STATS_BUILD = os.path.join(ROOT, "_build", "gemm_gb300_stats")
+STATS_LIB = os.path.join(HERE, "libgemm_gb300_stats.so")
 
 SOURCES = ["gemm_api.cu", "kern_ab16_mc1.cu", "kern_ab16_mc2.cu", "kern_ab8_mc1.cu",
            "kern_ab8_mc2.cu", "kern_ab32_mc1.cu", "kern_ab32_mc2.cu"]
@@ -41,23 +46,27 @@ def _inputs():
     return files
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def _stale(lib: str) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(f) > t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Build the library if any source is newer than it; return its path."""
-    if not force and not _stale():
-        return LIB
+def build(force: bool = False, verbose: bool = False, ring_stats: bool = False) -> str:
+    """Build the library if any source is newer than it; return its path.
+    ring_stats: build the ring-statistics library instead of the product one."""
+    lib = STATS_LIB if ring_stats else LIB
+    bdir = STATS_BUILD if ring_stats else BUILD
+    extra = ["-DGB300_RING_STATS=1"] if ring_stats else []
+    if not force and not _stale(lib):
+        return lib
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(bdir, exist_ok=True)
 
     def compile_one(src):
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(bdir, src.replace(".cu", ".o"))
+        cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -69,14 +78,15 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                ring_stats="--ring-stats" in sys.argv))

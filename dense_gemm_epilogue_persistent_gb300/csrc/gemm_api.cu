@@ -94,6 +94,7 @@ struct gemm_handle {
   void* ws = nullptr;          // gemm_run_host's device copies of its host buffers
   size_t ws_bytes = 0;
   std::mutex ws_mu;
+  unsigned long long* d_stats = nullptr;   // ring statistics (statistics build only)
 };
 
 namespace {
@@ -690,8 +691,10 @@ GEMM_API gemm_status_t gemm_create(gemm_handle_t* out, int device) {
   {
     const void* kern = gb300::kernel_for(2, 2, 256, 2);
     const int smem = optin / 2 + 1024;
+    // The attribute is process-wide: raise it to the opt-in limit (as every
+    // prepared launch does), never lower it under another handle's launches.
     if (cudaSetDevice(device) == cudaSuccess &&
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) ==
             cudaSuccess) {
       for (int cs : {1, 2, 4}) {
         cudaLaunchConfig_t lc{};
@@ -719,6 +722,20 @@ GEMM_API gemm_status_t gemm_create(gemm_handle_t* out, int device) {
   h->smem_optin = optin;
   h->encode = reinterpret_cast<EncodeTiledFn>(fn);
   h->d_status = status;
+  if constexpr (gb300::kRingStats) {
+    // one counter block per CTA of the largest grid (one CTA per SM)
+    const size_t bytes = (size_t)sms * gb300::kStatWords * sizeof(unsigned long long);
+    if (cudaSetDevice(device) != cudaSuccess || cudaMalloc(&h->d_stats, bytes) != cudaSuccess ||
+        cudaMemset(h->d_stats, 0, bytes) != cudaSuccess) {
+      cudaGetLastError();
+      cudaSetDevice(prev);
+      cudaFree(h->d_stats);
+      cudaFree(status);
+      delete h;
+      return GEMM_ERR_CUDA;
+    }
+    cudaSetDevice(prev);
+  }
   *out = h;
   return GEMM_OK;
 }
@@ -730,6 +747,7 @@ GEMM_API gemm_status_t gemm_destroy(gemm_handle_t h) {
   cudaSetDevice(h->device);
   cudaFree(h->d_status);
   if (h->ws) cudaFree(h->ws);
+  if (h->d_stats) cudaFree(h->d_stats);
   cudaSetDevice(prev);
   delete h;
   return GEMM_OK;
@@ -834,6 +852,7 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
   lc.numAttrs = 2;
   ent->kp.status = h->d_status;
   ent->kp.timeout_ns = h->timeout_ns;
+  ent->kp.stats = h->d_stats;
   void* args[7] = {&ent->maps[0], &ent->maps[1], &ent->maps[2], &ent->maps[3], &ent->maps[4],
                    &ent->maps[5], &ent->kp};
   if (cudaLaunchKernelExC(&lc, ent->kern, args) != cudaSuccess) {
@@ -915,6 +934,23 @@ GEMM_API gemm_status_t gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int6
     cudaGetLastError();
     return GEMM_ERR_CUDA;
   }
+  return GEMM_OK;
+}
+
+GEMM_API gemm_status_t gemm_ring_stats(gemm_handle_t h, struct CUstream_st* stream,
+                                       uint64_t* out, int max_ctas, int* n_ctas) {
+  if (!h || !out || !n_ctas || max_ctas < 0) return GEMM_ERR_INVALID_ARG;
+  *n_ctas = 0;
+  if (!gb300::kRingStats || !h->d_stats) return GEMM_ERR_UNSUPPORTED_CONFIG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int n = std::min(h->last.grid_ctas, std::min(max_ctas, h->sm_count));
+  if (cudaStreamSynchronize(s) != cudaSuccess ||
+      (n > 0 && cudaMemcpy(out, h->d_stats, (size_t)n * gb300::kStatWords * sizeof(uint64_t),
+                           cudaMemcpyDeviceToHost) != cudaSuccess)) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  *n_ctas = n;
   return GEMM_OK;
 }
 

@@ -91,8 +91,37 @@ struct KernelParams {
                              //   bits 0-1 A/B loads, 2-3 C/X loads, 4-5 D/Y stores
   uint32_t* status;          // device status word (watchdog)
   unsigned long long timeout_ns;
+  unsigned long long* stats; // ring statistics (statistics build only; else unused)
   EpiParams epi;
 };
+
+// Ring statistics: a separate build of the library (GB300_RING_STATS=1) in
+// which each CTA's producer, MMA issuer and epilogue store thread count the
+// clock cycles they spend waiting on each barrier and in their loops, so the
+// ring's stall picture can be read per role.  The product build compiles none
+// of it.  Per CTA kStatWords counters, in the order of the enum.
+#ifndef GB300_RING_STATS
+#define GB300_RING_STATS 0
+#endif
+constexpr bool kRingStats = GB300_RING_STATS != 0;
+enum : int {
+  kStatMmaFull = 0,     // MMA issuer: cycles waiting for a stage to land
+  kStatMmaAcc,          //   ... waiting for a free accumulator stage
+  kStatMmaLoop,         //   ... in its whole loop
+  kStatMmaStages,       //   stages issued
+  kStatProdEmpty,       // producer: cycles waiting for a stage to drain
+  kStatProdLoop,        //   ... in its whole loop
+  kStatEpiTfull,        // epilogue store thread: cycles waiting for an accumulator
+  kStatEpiCfull,        //   ... waiting for C/X to land
+  kStatEpiLoop,         //   ... in its whole loop
+  kStatEpiChunks,       //   chunks processed
+  kStatWords = 12
+};
+
+__device__ __forceinline__ long long stat_clock() {
+  if constexpr (kRingStats) return clock64();
+  else return 0;
+}
 
 constexpr int kThreads = 192;
 constexpr int kAccStages = 2;
@@ -422,6 +451,8 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
+      long long st_empty = 0;
+      const long long st_t0 = stat_clock();
       for (int it = cluster_id; ok && it < p.num_items; it += num_clusters) {
         int half;
         const int t = item_tile(it, p, half);
@@ -435,7 +466,9 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         const int n0 = tn * BN + (half > 0 ? BN / 2 : 0) + (int)rank * (item_n / CG) +
                        (int)grp * (item_n / CG / MC);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
+          const long long t_w = stat_clock();
           if (!wait_phase(empty0 + 8u * s, ph ^ 1u, w, kWaitProducer)) { ok = false; break; }
+          if constexpr (kRingStats) st_empty += clock64() - t_w;
           const uint32_t fb = full0 + 8u * s;
           if (rank == 0) mbar_arrive_expect_tx(fb, tx_bytes);
           const uint32_t fb_target = (CG == 2) ? map_to_rank(fb, pair_leader) : fb;
@@ -474,6 +507,11 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           if (++s == S) { s = 0; ph ^= 1u; }
         }
       }
+      if constexpr (kRingStats) if (p.stats) {
+        unsigned long long* const o = p.stats + (size_t)blockIdx.x * kStatWords;
+        o[kStatProdEmpty] = st_empty;
+        o[kStatProdLoop] = clock64() - st_t0;
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -481,14 +519,20 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     if (rank == 0 && lane == 0) {
       int s = 0, acc = 0;
       uint32_t ph = 0, aph = 0;
+      long long st_full = 0, st_acc = 0, st_stages = 0;
+      const long long st_t0 = stat_clock();
       bool ok = !p.inject_stall || wait_phase(never_bar, 0u, w, kWaitInjected);
       for (int it = cluster_id; ok && it < p.num_items; it += num_clusters) {
+        const long long t_a = stat_clock();
         if (!wait_phase(tempty0 + 8u * acc, aph ^ 1u, w, kWaitMmaAcc)) break;
+        if constexpr (kRingStats) st_acc += clock64() - t_a;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         const uint32_t idesc = it < p.split_start ? p.idesc : p.idesc_half;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
+          const long long t_f = stat_clock();
           if (!wait_phase(full0 + 8u * s, ph, w, kWaitMmaFull)) { ok = false; break; }
+          if constexpr (kRingStats) { st_full += clock64() - t_f; ++st_stages; }
           tc_fence_after_sync();
           const uint32_t sa = a_ring + s * G::A_STAGE;
           const uint32_t sb = b_ring + s * G::B_STAGE;
@@ -514,6 +558,19 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         if (!ok) break;
         umma_commit<CG, (CG == 2)>(tfull0 + 8u * acc, pair_mask);   // accumulator ready
         if (++acc == kAccStages) { acc = 0; aph ^= 1u; }
+      }
+      if constexpr (kRingStats) if (p.stats) {
+        unsigned long long* const o = p.stats + (size_t)blockIdx.x * kStatWords;
+        o[kStatMmaFull] = st_full;
+        o[kStatMmaAcc] = st_acc;
+        o[kStatMmaLoop] = clock64() - st_t0;
+        o[kStatMmaStages] = st_stages;
+      }
+    }
+    if constexpr (kRingStats) {
+      if (p.stats && rank != 0 && lane == 0) {   // the pair's other CTA issues no MMAs
+        unsigned long long* const o = p.stats + (size_t)blockIdx.x * kStatWords;
+        o[kStatMmaFull] = o[kStatMmaAcc] = o[kStatMmaLoop] = o[kStatMmaStages] = 0ull;
       }
     }
     __syncwarp();
@@ -582,6 +639,8 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     uint32_t aph = 0;
     int gc = 0;                             // chunk counter of this CTA's stream
     bool ok = true;
+    long long st_tfull = 0, st_cfull = 0;
+    const long long st_t0 = stat_clock();
     for (int it = cluster_id; ok && it < p.num_items; it += num_clusters) {
       int half;
       const int t = item_tile(it, p, half);
@@ -589,7 +648,9 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       tile_coords(t, p, tm, tn, tl);
       const int nchunks = half < 0 ? G::CHUNKS : G::CHUNKS / 2;
       const int ncol0 = tn * BN + (half > 0 ? BN / 2 : 0);
+      const long long t_t = stat_clock();
       const bool ready = wait_phase(tfull0 + 8u * acc, aph, w, kWaitEpilogue, p.epi_wait_ns);
+      if constexpr (kRingStats) st_tfull += clock64() - t_t;
       __syncwarp();
       ok = named_barrier_and(kEpiBarrier, 128, ready);
       if (!ok) break;
@@ -625,7 +686,9 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         uint8_t* const slot = gbase + (epi0 - base) + (uint32_t)slot_idx * slot_bytes;
         float cv[kEpiChunk], xv[kEpiChunk];
         bool got = true;
+        const long long t_c = stat_clock();
         if (loads) got = wait_phase(cfull0 + 8u * slot_idx, (uint32_t)(gc / E) & 1u, w, kWaitEpiLoad);
+        if constexpr (kRingStats) st_cfull += clock64() - t_c;
         if (got && e.read_c) {
           smem_read_row(slot, e.c_dt, e.cd_m_major, r, cv);
         } else {
@@ -691,6 +754,15 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       if (++acc == kAccStages) { acc = 0; aph ^= 1u; }
     }
     if (epi_leader) bulk_wait_group_all();
+    if constexpr (kRingStats) {
+      if (epi_leader && p.stats) {
+        unsigned long long* const o = p.stats + (size_t)blockIdx.x * kStatWords;
+        o[kStatEpiTfull] = st_tfull;
+        o[kStatEpiCfull] = st_cfull;
+        o[kStatEpiLoop] = clock64() - st_t0;
+        o[kStatEpiChunks] = gc;
+      }
+    }
     __syncwarp();
   }
 

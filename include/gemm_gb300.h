@@ -222,6 +222,23 @@ gemm_status_t gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K, in
                             float alpha, float beta, float x_factor,
                             const gemm_dtypes_t* dtypes, struct CUstream_st* stream);
 
+/* Ring statistics, for studying the kernel's pipeline (no counterpart on the
+ * pages).  Only the statistics build of the library (libgemm_gb300_stats.so,
+ * compiled with GB300_RING_STATS=1; the product library returns
+ * GEMM_ERR_UNSUPPORTED_CONFIG) counts, in each CTA of the last launch, the
+ * clock cycles its roles spend waiting on the pipeline's barriers.  The call
+ * synchronises `stream`, then copies min(grid CTAs, max_ctas) blocks of
+ * GEMM_RING_STAT_WORDS counters to `out` (CTA-major) and stores the count in
+ * *n_ctas.  Counters, in order: MMA issuer waiting for a stage to land,
+ * waiting for a free accumulator stage, its whole loop, stages issued (these
+ * four are zero in the non-leader CTA of a pair); producer waiting for a
+ * stage to drain, its whole loop; epilogue store thread waiting for a
+ * finished accumulator, waiting for C/X to land, its whole loop, chunks
+ * processed; two spare words. */
+#define GEMM_RING_STAT_WORDS 12
+gemm_status_t gemm_ring_stats(gemm_handle_t h, struct CUstream_st* stream, uint64_t* out,
+                              int max_ctas, int* n_ctas);
+
 /* Synchronise `stream`, then read and clear the handle's device status word.
  * Returns GEMM_ERR_DEVICE_TIMEOUT if any kernel since the last call hit its
  * watchdog, GEMM_ERR_CUDA if the stream reported an error, else GEMM_OK.

@@ -269,3 +269,13 @@ def test_random_gpu_cases_are_valid_problems(lib):
                            (1 << 26) if case.x else None, 1 << 28, (1 << 30) if case.y else None,
                            case.alpha, case.beta, case.xf, dt)
         assert G.gemm_check(p) == G.GEMM_OK, (i, case)
+
+
+def test_ring_stats_rejected_by_product_library(lib):
+    """The product library compiles no ring statistics: gemm_ring_stats
+    rejects a missing handle or output and never touches the device."""
+    import ctypes
+    buf = (ctypes.c_uint64 * 12)()
+    n = ctypes.c_int(-1)
+    assert lib.gemm_ring_stats(None, None, buf, 1, ctypes.byref(n)) == G.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_ring_stats(None, None, None, 1, ctypes.byref(n)) == G.GEMM_ERR_INVALID_ARG
