@@ -41,7 +41,10 @@ constexpr int kMaxEpiSlots = 6;
 // on all five benchmark shapes (fp8 3000x5000x4096: +11% over evict-normal);
 // 1500-launch runs under the power cap on 8192^3 (fp16 custom epilogue / bf16)
 // give 1450 / 1602 TFLOP/s against 1401 / 1559 with evict-normal A/B loads and
-// 1432 / 1600 with evict-last ones.
+// 1432 / 1600 with evict-last ones; separate A and B policies (A kept longer, since
+// the tile order reuses A row-panels across the waves of a strip) were all worse:
+// A normal / B first 1410 / 1560, A 25 %-evict-last / B first 1410 / 1570,
+// A first / B normal 1370 / 1546, against 1468 / 1625 in the same runs.
 constexpr int kDefaultL2Hints = 2 | (2 << 2) | (2 << 4);
 constexpr int kDefaultEpiWaitNs = 0;
 constexpr int kSmemSlack = 1024 + 16;   // base alignment + abort flag + watchdog-test barrier
