@@ -1,4 +1,4 @@
-"""Randomised GPU parity: seeded problems drawn across every input type, accumulator,
+"""Randomised GPU parity: 80 seeded problems drawn across every input type, accumulator,
 layout, optional tensor, epilogue variant, kernel variant and ragged shape the library
 takes, each compared element by element with the fp64 oracle (the bounds of
 gemm_cases).  Shapes keep the leading dimensions 16-byte aligned, as the C ABI
@@ -18,7 +18,7 @@ AB = [("f16", None), ("bf16", None), ("e4m3", None), ("e5m2", None), ("e4m3", "e
 OUT = ["f32", "f16", "bf16"]
 VARIANTS = [None, (1, 128, 1), (1, 256, 1), (2, 128, 1), (2, 256, 1), (1, 128, 2),
             (1, 256, 2), (2, 128, 2), (2, 256, 2)]
-N_CASES = 40
+N_CASES = 80
 
 
 def _round_up(v, m):
