@@ -372,6 +372,28 @@ def test_ragged_shapes(gemm, M, N, K, L):
     compare_full(prep, D, Y)
 
 
+@pytest.mark.parametrize("M,N,K,L,cd_m,variant", [
+    (64, 64, 32, 257, False, None), (40, 72, 48, 300, False, (2, 128, 1)),
+    (1, 8, 64, 129, False, None), (136, 1, 16, 65, True, (1, 128, 2)),
+])
+def test_many_small_batches(gemm, M, N, K, L, cd_m, variant):
+    """Batched problems with many small, ragged members: batch index, tile
+    order across batches and the last-wave split all in play.  (A single
+    column needs column-major C/D: the packed leading dimension must be
+    16-byte aligned.)"""
+    if variant:
+        _force(gemm, *variant)
+    else:
+        gemm.set_config(None)
+    case = Case(M=M, N=N, K=K, L=L, ab="bf16", c="f32", d="f16", y="f32", cd_m=cd_m,
+                alpha=0.5, beta=-1.0, seed=M * 7 + L)
+    prep = prepare(case)
+    D, Y = run_gpu(gemm, prep)
+    _finish(gemm)
+    compare_full(prep, D, Y)
+    gemm.set_config(None)
+
+
 def test_k_zero(gemm):
     case = Case(M=200, N=136, K=0, L=2, ab="bf16", c="f32", d="f32", x="f16", y="f32",
                 alpha=3.0, beta=0.5, xf=-2.0, seed=5)
