@@ -907,6 +907,12 @@ GEMM_API gemm_status_t gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int6
   {
     std::lock_guard<std::mutex> g(h->ws_mu);
     if (h->ws_bytes < need) {
+      // Earlier calls may still be reading or writing the old workspace:
+      // let the device drain before it is released (growth is rare).
+      if (h->ws && cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+      }
       if (h->ws) cudaFree(h->ws);
       h->ws = nullptr;
       h->ws_bytes = 0;
