@@ -584,7 +584,7 @@ def main():
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": warm, "ms_per_step": max_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": w.ab + (f"/{w.b}" if w.b else "") + f" in, {w.acc} accumulate",
+            "dtype": w.ab + (f"/{w.b}" if w.b else ""), "accumulate": w.acc,
             "data": "synthetic",
             "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "L": w.L,
                        "ab": w.ab, "c": w.c, "d": w.d, "x": w.x, "y": w.y,
