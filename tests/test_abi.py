@@ -279,3 +279,20 @@ def test_ring_stats_rejected_by_product_library(lib):
     n = ctypes.c_int(-1)
     assert lib.gemm_ring_stats(None, None, buf, 1, ctypes.byref(n)) == G.GEMM_ERR_INVALID_ARG
     assert lib.gemm_ring_stats(None, None, None, 1, ctypes.byref(n)) == G.GEMM_ERR_INVALID_ARG
+
+
+def test_plan_single_wave_trades_a_stage_for_epilogue_slots(lib):
+    """One wave of tiles (every CTA runs one tile, its epilogue exposed): the
+    planner takes one ring stage fewer when the ring could be at least four
+    deep, and the freed shared memory becomes epilogue slots.  More than one
+    wave, or a forced stage count, keeps the deepest ring."""
+    dt = G.make_dtypes("bf16", "f32", "f32")
+    one = _p(M=2048, N=2048, K=2048, lda=2048, ldb=2048, dtypes=dt)     # 128 tiles of 128x256
+    st, cfg = G.gemm_plan(one, 152, 232448)
+    assert st == 0 and (cfg.cta_group, cfg.tile_n) == (1, 256)
+    st, deep = G.gemm_plan(one, 152, 232448, G.gemm_config_t(cta_group=1, tile_n=256, stages=4))
+    assert st == 0 and deep.stages == 4
+    assert cfg.tiles <= 152 and cfg.stages == deep.stages - 1 and cfg.epi_slots > deep.epi_slots
+    many = _p(M=4096, N=4096, K=2048, lda=2048, ldb=2048, dtypes=dt)
+    st, cfg2 = G.gemm_plan(many, 152, 232448, G.gemm_config_t(cta_group=1, tile_n=256))
+    assert st == 0 and cfg2.tiles > 152 and cfg2.stages == 4
