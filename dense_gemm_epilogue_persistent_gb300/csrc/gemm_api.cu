@@ -595,6 +595,9 @@ gemm_status_t prepare_launch(gemm_handle* h, const gemm_problem_t& p, LaunchEntr
   kp.l2_hints = (uint32_t)cfg.l2_hints;
   kp.epi_wait_ns = (uint32_t)cfg.epi_wait_ns;
   kp.inject_stall = cfg.inject_stall;
+  // fp16 accumulators keep increasing K: their rounding points are defined on
+  // running sums from k = 0.
+  kp.k_alternate = acc_f16 ? 0 : 1;
   kp.status = h->d_status;
   kp.timeout_ns = h->timeout_ns;
   kp.epi.c_dt = dtypes->c;

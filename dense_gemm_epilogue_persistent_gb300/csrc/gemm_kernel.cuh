@@ -87,6 +87,7 @@ struct KernelParams {
   uint32_t idesc_half;       // instruction descriptor of a half-width item (N / 2)
   uint32_t epi_wait_ns;      // suspend-time hint of the epilogue's accumulator wait (0: none)
   int inject_stall;          // test only: the MMA warp first waits on a barrier nobody arrives at
+  int k_alternate;           // odd waves of tiles walk K from the last k-block down
   uint32_t l2_hints;         // L2 eviction priority (0 normal, 1 last, 2 first):
                              //   bits 0-1 A/B loads, 2-3 C/X loads, 4-5 D/Y stores
   uint32_t* status;          // device status word (watchdog)
@@ -201,6 +202,7 @@ __device__ __forceinline__ void tile_coords(int t, const KernelParams& p, int& t
   const int rr = r - g * span;
   tm = first_m + rr % gm;
   tn = rr / gm;
+  if (g & 1) tn = p.tiles_n - 1 - tn;   // odd strips walk N backwards (serpentine)
 }
 
 // Work item -> tile and half.  Items below split_start are whole tiles; the
@@ -465,6 +467,11 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         const int m0 = tm * G::CM + (int)grp * (G::BM * CG) + (int)rank * G::BM;
         const int n0 = tn * BN + (half > 0 ? BN / 2 : 0) + (int)rank * (item_n / CG) +
                        (int)grp * (item_n / CG / MC);
+        // Alternate waves walk K in opposite directions, so the k-blocks one
+        // wave reads last are the first the next wave reads, while they are
+        // still in L2.  The MMA side only counts stages, so the order is the
+        // producer's alone.
+        const bool k_down = p.k_alternate && ((it / num_clusters) & 1);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           const long long t_w = stat_clock();
           if (!wait_phase(empty0 + 8u * s, ph ^ 1u, w, kWaitProducer)) { ok = false; break; }
@@ -472,7 +479,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           const uint32_t fb = full0 + 8u * s;
           if (rank == 0) mbar_arrive_expect_tx(fb, tx_bytes);
           const uint32_t fb_target = (CG == 2) ? map_to_rank(fb, pair_leader) : fb;
-          const int k0 = kb * G::BK;
+          const int k0 = (k_down ? p.k_blocks - 1 - kb : kb) * G::BK;
           const uint32_t sa = a_ring + s * G::A_STAGE;
           const uint32_t sb = b_ring + s * G::B_STAGE;
           auto issue = [&](const CUtensorMap* map, uint32_t dst, int c0, int c1) {
