@@ -104,7 +104,10 @@ typedef struct {
  *   tile_n      output tile width: 128 or 256.
  *   stages      depth of the shared-memory A/B ring (0 = as deep as fits).
  *   group_m     tile rasterisation: tiles are walked in column strips
- *               group_m tiles high (0 = automatic).
+ *               group_m tiles high, odd strips from the last column back;
+ *               odd waves of tiles also walk K from the last k-block down
+ *               (fp32 accumulators), so each wave starts on the operand
+ *               blocks the previous one read last (0 = automatic: 12).
  *   cluster_m   CTA groups per thread-block cluster, stacked along M, that share
  *               their B tile through TMA multicast: 1 or 2 (0 = automatic).  The
  *               cluster holds cta_group * cluster_m CTAs.
