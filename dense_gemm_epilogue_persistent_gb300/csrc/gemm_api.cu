@@ -381,8 +381,8 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
   const int64_t tiles_n = cdiv(std::max<int64_t>(p.N, 1), bn);
   const int64_t tiles = tiles_m * tiles_n * std::max<int64_t>(p.L, 1);
   // Strips of 12 tile rows: with the serpentine strip order and the K
-  // direction alternating per wave, 8192^3 reads 1.205 GB from DRAM per launch
-  // at 12 (1.234 GB at 8, 1.515 GB at 4, 1.306 GB at 16) and runs 0.5-0.8 %
+  // direction alternating per wave, 8192^3 reads 1.206 GB from DRAM per launch
+  // at 12 (1.235 GB at 8, 1.514 GB at 4, 1.307 GB at 16) and runs 0.5-0.8 %
   // faster than at 8; other shapes measured the same at 8 and 12.
   int group_m = forced && forced->group_m ? forced->group_m : 12;
   group_m = (int)std::max<int64_t>(1, std::min<int64_t>(group_m, tiles_m));
