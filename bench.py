@@ -183,9 +183,10 @@ def oracle_problem_for(w, inp):
                           w.cd_m_major, w.alpha, w.beta, w.x_factor, b_dtype=w.b, relu=w.relu)
 
 
-def time_oracle_sample(w, inp, seconds: float):
-    """Time the oracle as it stands on whole rows of the workload until about
-    `seconds` of CPU work; return the throughput and the sample it ran."""
+def _oracle_rows(w, inp, seconds: float):
+    """Run the oracle as it stands on whole output rows (every batch) until
+    about `seconds` of CPU work or the whole problem; return (rows, seconds,
+    cores)."""
     import oracle
     p = oracle_problem_for(w, inp)
     cores = oracle.max_threads()
@@ -197,10 +198,28 @@ def time_oracle_sample(w, inp, seconds: float):
         t_total += time.perf_counter() - t0
         rows += chunk * w.L
         m += chunk
+    return rows, t_total, cores
+
+
+def time_oracle_sample(w, inp, seconds: float):
+    """Time the oracle as it stands on whole rows of the workload until about
+    `seconds` of CPU work; return the throughput and the sample it ran."""
+    rows, t_total, cores = _oracle_rows(w, inp, seconds)
     flops = 2.0 * rows * w.N * w.K
     return {"value": flops / t_total / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{rows} full output rows ({rows * w.N} entries, K={w.K}) of {w.name}, "
                       f"fp64 triple loop, {t_total:.1f} s"}
+
+
+def oracle_seconds(w, inp, seconds: float = 2.0):
+    """The oracle's time for the whole problem: measured when it finishes
+    within about `seconds` (the small workloads), else projected from whole
+    rows timed for that long."""
+    rows, t_total, cores = _oracle_rows(w, inp, seconds)
+    full = rows == w.M * w.L
+    total = t_total if full else t_total * (w.M * w.L) / rows
+    return {"s": round(total, 3), "measured_in_full": full, "cores": cores,
+            "rows_timed": rows}
 
 
 def run_reference(args, rank):
@@ -570,6 +589,9 @@ def main():
                     if tcpu is not None:
                         ent["torch_cpu_fp32_s"] = round(tcpu, 3)
                         ent["torch_cpu_fp32_tflops"] = round(wc.flops / tcpu / 1e12, 3)
+                    # in full for the small problems, projected from 2 s of rows otherwise
+                    ent["oracle_cpu"] = oracle_seconds(wc, inp_c,
+                                                       10.0 if wc.flops < 2e10 else 2.0)
                 per_config[name] = ent
                 if bc is not bound:
                     del bc
