@@ -1,10 +1,11 @@
 """Run a workload under forced launch configurations.
 
     python -m dense_gemm_epilogue_persistent_gb300.tune WORKLOAD [--group-m 4,8,12]
-        [--l2-hints 42,40] [--cta-group N] [--tile-n N] [--launches N] [--once]
+        [--l2-hints 42,40] [--cta-group N] [--tile-n N] [--stages 2,3]
+        [--epi-slots 2,4] [--launches N] [--once]
 
-For each combination of the listed group_m and l2_hints values (other fields
-automatic unless given) it runs the workload back to back `--launches` times
+For each combination of the listed group_m, l2_hints, stages and epi_slots
+values (0 or absent: automatic; other fields automatic unless given) it runs the workload back to back `--launches` times
 and prints TFLOP/s from CUDA events; with --once it runs exactly one launch per
 configuration and times nothing, for a profiler capturing one launch of each
 (e.g. ncu -k regex:persistent).  Run from the repository root (it reads the
@@ -33,6 +34,8 @@ def main(argv=None) -> int:
                          "2 first); 0 = automatic, 0x100 = all normal")
     ap.add_argument("--cta-group", type=int, default=0)
     ap.add_argument("--tile-n", type=int, default=0)
+    ap.add_argument("--stages", default=None)
+    ap.add_argument("--epi-slots", default=None)
     ap.add_argument("--launches", type=int, default=200)
     ap.add_argument("--once", action="store_true")
     args = ap.parse_args(argv)
@@ -50,9 +53,11 @@ def main(argv=None) -> int:
         g.run(w.M, w.N, w.K, w.L, A, A.shape[-1], int(w.a_mn_major), B, B.shape[-1],
               int(w.b_mn_major), C, X, D, Y, w.alpha, w.beta, w.x_factor, dt)
 
-    for gm, l2 in itertools.product(_ints(args.group_m), _ints(args.l2_hints)):
+    for gm, l2, st, es in itertools.product(_ints(args.group_m), _ints(args.l2_hints),
+                                            _ints(args.stages), _ints(args.epi_slots)):
         g.set_config(G.gemm_config_t(cta_group=args.cta_group, tile_n=args.tile_n, group_m=gm,
-                                     l2_hints=(l2 | 0x100) if l2 else 0))
+                                     l2_hints=(l2 | 0x100) if l2 else 0, stages=st,
+                                     epi_slots=es))
         out = {"workload": args.workload}
         if args.once:
             run()
