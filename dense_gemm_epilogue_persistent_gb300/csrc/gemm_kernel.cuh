@@ -172,13 +172,18 @@ struct Watch {
 // Bounded wait for the phase with parity `parity`.  A non-zero `hint_ns` lets
 // the hardware suspend the thread up to that long per probe (for long waits
 // whose spinning would take issue slots from the TMA and MMA warps).
+// kLocal: a barrier only this CTA's own TMA loads complete (CTA-scope acquire).
+template <bool kLocal = false>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const Watch& w,
                                            uint32_t role, uint32_t hint_ns = 0) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto probe = [&]() {
+    if constexpr (kLocal) return mbar_try_wait_cta(bar, parity);
+    else return hint_ns ? mbar_try_wait_hint(bar, parity, hint_ns) : mbar_try_wait(bar, parity);
+  };
+  if (kLocal ? mbar_try_wait_cta(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
-    if (hint_ns ? mbar_try_wait_hint(bar, parity, hint_ns) : mbar_try_wait(bar, parity))
-      return true;
+    if (probe()) return true;
     if (*w.abort) return false;
     if (globaltimer_ns() - t0 > w.timeout_ns) {
       *w.abort = 1u;
@@ -645,6 +650,8 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     int acc = 0;
     uint32_t aph = 0;
     int gc = 0;                             // chunk counter of this CTA's stream
+    int slot_idx = 0;                       // gc % E
+    uint32_t slot_ph = 0;                   // (gc / E) & 1: phase of the slot's cfull barrier
     bool ok = true;
     long long st_tfull = 0, st_cfull = 0;
     const long long st_t0 = stat_clock();
@@ -666,9 +673,25 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
 #pragma unroll 1
       for (int j = 0; j < nchunks; ++j, ++gc) {
+        // The accumulator columns are requested first: their latency overlaps
+        // the wait for C/X and the shared-memory reads below.
         uint32_t raw_acc[32];
         tmem_load_32cols(tbase + 32u * j, raw_acc);
-        tmem_wait_ld();
+        uint8_t* const slot = gbase + (epi0 - base) + (uint32_t)slot_idx * slot_bytes;
+        float cv[kEpiChunk], xv[kEpiChunk];
+        bool got = true;
+        const long long t_c = stat_clock();
+        if (loads) got = wait_phase<true>(cfull0 + 8u * slot_idx, slot_ph, w, kWaitEpiLoad);
+        if constexpr (kRingStats) st_cfull += clock64() - t_c;
+        if (got && e.read_c) {
+          smem_read_row(slot, e.c_dt, e.cd_m_major, r, cv);
+        } else {
+#pragma unroll
+          for (int i = 0; i < kEpiChunk; ++i) cv[i] = 0.f;
+        }
+        if (got && e.read_x) smem_read_row(slot + e.cd_bytes, e.x_dt, e.cd_m_major, r, xv);
+        __syncwarp();                       // the .aligned wait needs the whole warp
+        tmem_wait_ld(raw_acc);
         // Normalise the accumulator to fp32 bit patterns once per chunk (uniform
         // branches), so the per-element epilogue below is the same for every case.
         if (p.k_blocks == 0) {
@@ -689,20 +712,6 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           }
           __syncwarp();
         }
-        const int slot_idx = gc % E;
-        uint8_t* const slot = gbase + (epi0 - base) + (uint32_t)slot_idx * slot_bytes;
-        float cv[kEpiChunk], xv[kEpiChunk];
-        bool got = true;
-        const long long t_c = stat_clock();
-        if (loads) got = wait_phase(cfull0 + 8u * slot_idx, (uint32_t)(gc / E) & 1u, w, kWaitEpiLoad);
-        if constexpr (kRingStats) st_cfull += clock64() - t_c;
-        if (got && e.read_c) {
-          smem_read_row(slot, e.c_dt, e.cd_m_major, r, cv);
-        } else {
-#pragma unroll
-          for (int i = 0; i < kEpiChunk; ++i) cv[i] = 0.f;
-        }
-        if (got && e.read_x) smem_read_row(slot + e.cd_bytes, e.x_dt, e.cd_m_major, r, xv);
         // Every thread has read the slot (and agrees whether to go on) before any
         // thread overwrites it with D and Y.
         __syncwarp();
@@ -756,6 +765,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         } else if (epi_loader && loads) {
           issue_loads();                    // meanwhile, in another warp: C/X of chunk gc+E-1
         }
+        if (++slot_idx == E) { slot_idx = 0; slot_ph ^= 1u; }
         __syncwarp();                       // the issuing threads' warps reconverge
       }
       if (++acc == kAccStages) { acc = 0; aph ^= 1u; }
