@@ -27,12 +27,16 @@
 //               tile is processed in 32-column chunks through a ring of `slots`
 //               shared-memory slots: C and X sub-tiles are TMA-loaded `slots-1`
 //               chunks ahead (across tile boundaries, so the next tile's C/X arrive
-//               during its main loop) by one thread; each thread reads its row,
-//               computes in fp32, writes D and Y back into the slot, and a thread
-//               of another warp TMA-stores them.
+//               during its main loop) by one thread; each thread requests its
+//               accumulator columns, reads its C/X row while they load, computes
+//               in fp32, writes D and Y back into the slot, and a thread of another
+//               warp TMA-stores them.
 // Every cluster walks the same static persistent tile sequence
 // t = cluster_id, cluster_id + num_clusters, ...; with two accumulator stages the
-// epilogue of tile i overlaps the main loop of tile i+1.  The kernel touches
+// epilogue of tile i overlaps the main loop of tile i+1.  Tiles are ordered in
+// strips of group_m tile rows, odd strips walking N backwards, and odd waves of
+// tiles walk K downwards (fp32 accumulators), so each wave starts on the operand
+// blocks the previous one read last, while they are still in L2.  The kernel touches
 // global memory only after griddepcontrol.wait, so a launch with programmatic
 // stream serialization overlaps its prologue with the previous grid's tail.
 //
