@@ -80,13 +80,19 @@ DEVICE_SOURCES = ("gemm_kernel.cuh", "ptx.cuh", "kernels.h")
 
 def kernel_source_digest():
     """Digest of the device code (the kernel template, its PTX wrappers and
-    the instantiation units)."""
+    the instantiation units), comments and layout stripped, so that a
+    comment-only edit keeps a recorded profile valid."""
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_gemm_epilogue_persistent_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f in DEVICE_SOURCES or f.startswith("kern_"):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + fh.read())
+            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+                text = fh.read()
+            text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+            text = re.sub(r"//[^\n]*", " ", text)
+            text = " ".join(text.split())
+            h.update(f.encode() + text.encode())
     return h.hexdigest()[:16]
 
 
