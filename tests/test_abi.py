@@ -296,3 +296,18 @@ def test_plan_single_wave_trades_a_stage_for_epilogue_slots(lib):
     many = _p(M=4096, N=4096, K=2048, lda=2048, ldb=2048, dtypes=dt)
     st, cfg2 = G.gemm_plan(many, 152, 232448, G.gemm_config_t(cta_group=1, tile_n=256))
     assert st == 0 and cfg2.tiles > 152 and cfg2.stages == 4
+
+
+def test_plan_group_m_default_and_clamp(lib):
+    """Tiles are walked in strips 12 tile rows high unless forced; the strip
+    never exceeds the problem's tile rows."""
+    dt = G.make_dtypes("f16", "f16", "f16", "f16", "f16")
+    big = _p(M=8192, N=8192, K=8192, lda=8192, ldb=8192, dtypes=dt)
+    st, cfg = G.gemm_plan(big, 152, 232448)
+    assert st == 0 and cfg.group_m == 12
+    st, cfg = G.gemm_plan(big, 152, 232448, G.gemm_config_t(group_m=5))
+    assert st == 0 and cfg.group_m == 5
+    small = _p(M=1024, N=8192, K=256, lda=256, ldb=256, dtypes=dt)
+    st, cfg = G.gemm_plan(small, 152, 232448)
+    tiles_m = -(-1024 // cfg.tile_m)
+    assert st == 0 and cfg.group_m == min(12, tiles_m)
