@@ -2,10 +2,10 @@
 
     python -m dense_gemm_epilogue_persistent_gb300.tune WORKLOAD [--group-m 4,8,12]
         [--l2-hints 42,40] [--cta-group N] [--tile-n N] [--stages 2,3]
-        [--epi-slots 2,4] [--launches N] [--once]
+        [--epi-slots 2,4] [--epi-wait-ns 0,1000] [--launches N] [--once]
 
-For each combination of the listed group_m, l2_hints, stages and epi_slots
-values (0 or absent: automatic; other fields automatic unless given) it runs the workload back to back `--launches` times
+For each combination of the listed group_m, l2_hints, stages, epi_slots and
+epi_wait_ns values (absent: automatic; other fields automatic unless given) it runs the workload back to back `--launches` times
 and prints TFLOP/s from CUDA events; with --once it runs exactly one launch per
 configuration and times nothing, for a profiler capturing one launch of each
 (e.g. ncu -k regex:persistent).  Run from the repository root (it reads the
@@ -36,6 +36,8 @@ def main(argv=None) -> int:
     ap.add_argument("--tile-n", type=int, default=0)
     ap.add_argument("--stages", default=None)
     ap.add_argument("--epi-slots", default=None)
+    ap.add_argument("--epi-wait-ns", default=None,
+                    help="suspend hint of the epilogue's accumulator wait (0 = none)")
     ap.add_argument("--launches", type=int, default=200)
     ap.add_argument("--once", action="store_true")
     args = ap.parse_args(argv)
@@ -53,11 +55,12 @@ def main(argv=None) -> int:
         g.run(w.M, w.N, w.K, w.L, A, A.shape[-1], int(w.a_mn_major), B, B.shape[-1],
               int(w.b_mn_major), C, X, D, Y, w.alpha, w.beta, w.x_factor, dt)
 
-    for gm, l2, st, es in itertools.product(_ints(args.group_m), _ints(args.l2_hints),
-                                            _ints(args.stages), _ints(args.epi_slots)):
+    waits = [None] if args.epi_wait_ns is None else _ints(args.epi_wait_ns)
+    for gm, l2, st, es, ew in itertools.product(_ints(args.group_m), _ints(args.l2_hints),
+                                                _ints(args.stages), _ints(args.epi_slots), waits):
         g.set_config(G.gemm_config_t(cta_group=args.cta_group, tile_n=args.tile_n, group_m=gm,
                                      l2_hints=(l2 | 0x100) if l2 else 0, stages=st,
-                                     epi_slots=es))
+                                     epi_slots=es, epi_wait_ns=0 if ew is None else ew + 1))
         out = {"workload": args.workload}
         if args.once:
             run()
@@ -79,7 +82,8 @@ def main(argv=None) -> int:
         if st != G.GEMM_OK:
             raise RuntimeError(f"{G.gemm_status_string(st)} {detail:#x}")
         cfg = g.last_config()
-        out.update(group_m=cfg.group_m, l2_hints=cfg.l2_hints, cta_group=cfg.cta_group,
+        out.update(group_m=cfg.group_m, l2_hints=cfg.l2_hints, epi_wait_ns=cfg.epi_wait_ns,
+                   cta_group=cfg.cta_group,
                    tile_n=cfg.tile_n, stages=cfg.stages, epi_slots=cfg.epi_slots)
         print(json.dumps(out), flush=True)
     g.close()
