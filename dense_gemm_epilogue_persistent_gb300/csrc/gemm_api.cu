@@ -635,6 +635,39 @@ gemm_status_t prepare_launch(gemm_handle* h, const gemm_problem_t& p, LaunchEntr
   return GEMM_OK;
 }
 
+// Resident clusters of 1, 2 and 4 CTAs at one CTA per SM (every
+// configuration uses more than half of the shared memory), from the occupancy
+// calculator on a representative kernel; `device` must be current.  The
+// kernel's shared-memory attribute is process-wide: it is raised to the
+// opt-in limit, as every prepared launch raises it, and never lowered, since
+// another handle may have launches prepared with more than the size queried
+// here.  Counts the calculator does not give stay 0 (the planner then
+// assumes SMs / cluster size).
+void query_cluster_occupancy(int device, int sms, int optin, int (&clusters)[5]) {
+  (void)device;
+  const void* kern = gb300::kernel_for(2, 2, 256, 2);
+  const int smem = optin / 2 + 1024;
+  if (kern && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) ==
+                  cudaSuccess) {
+    for (int cs : {1, 2, 4}) {
+      cudaLaunchConfig_t lc{};
+      cudaLaunchAttribute attr[1];
+      lc.gridDim = dim3((unsigned)(cs * sms));
+      lc.blockDim = dim3(gb300::kThreads);
+      lc.dynamicSmemBytes = (size_t)smem;
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = (unsigned)cs;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      lc.attrs = attr;
+      lc.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &lc) == cudaSuccess) clusters[cs] = n;
+    }
+  }
+  cudaGetLastError();
+}
+
 }  // namespace
 
 // ====================================================================== C ABI
@@ -705,37 +738,11 @@ GEMM_API gemm_status_t gemm_create(gemm_handle_t* out, int device) {
     cudaGetLastError();
     return GEMM_ERR_CUDA;
   }
-  // Resident clusters of 1, 2 and 4 CTAs at one CTA per SM (every
-  // configuration uses more than half of the shared memory), from the
-  // occupancy calculator on a representative kernel.
+  // Resident clusters of 1, 2 and 4 CTAs at one CTA per SM.
   int clusters[5] = {0, 0, 0, 0, 0};
-  {
-    const void* kern = gb300::kernel_for(2, 2, 256, 2);
-    const int smem = optin / 2 + 1024;
-    // The attribute is process-wide: raise it to the opt-in limit (as every
-    // prepared launch does), never lower it under another handle's launches.
-    if (cudaSetDevice(device) == cudaSuccess &&
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) ==
-            cudaSuccess) {
-      for (int cs : {1, 2, 4}) {
-        cudaLaunchConfig_t lc{};
-        cudaLaunchAttribute attr[1];
-        lc.gridDim = dim3((unsigned)(cs * sms));
-        lc.blockDim = dim3(gb300::kThreads);
-        lc.dynamicSmemBytes = (size_t)smem;
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)cs;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        lc.attrs = attr;
-        lc.numAttrs = 1;
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, kern, &lc) == cudaSuccess) clusters[cs] = n;
-      }
-    }
-    cudaGetLastError();
-    cudaSetDevice(prev);
-  }
+  if (cudaSetDevice(device) == cudaSuccess) query_cluster_occupancy(device, sms, optin, clusters);
+  cudaGetLastError();
+  cudaSetDevice(prev);
   gemm_handle* h = new gemm_handle();
   for (int i = 0; i < 5; ++i) h->clusters_by_size[i] = clusters[i];
   h->device = device;
@@ -1059,29 +1066,7 @@ gemm_status_t noalloc_setup(gemm_handle& h, int device) {
     return GEMM_ERR_CUDA;
   }
   int clusters[5] = {0, 0, 0, 0, 0};
-  {
-    const void* kern = gb300::kernel_for(2, 2, 256, 2);
-    const int smem = optin / 2 + 1024;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
-        cudaSuccess) {
-      for (int cs : {1, 2, 4}) {
-        cudaLaunchConfig_t lc{};
-        cudaLaunchAttribute attr[1];
-        lc.gridDim = dim3((unsigned)(cs * sms));
-        lc.blockDim = dim3(gb300::kThreads);
-        lc.dynamicSmemBytes = (size_t)smem;
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)cs;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        lc.attrs = attr;
-        lc.numAttrs = 1;
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, kern, &lc) == cudaSuccess) clusters[cs] = n;
-      }
-    }
-    cudaGetLastError();
-  }
+  query_cluster_occupancy(device, sms, optin, clusters);
   for (int i = 0; i < 5; ++i) h.clusters_by_size[i] = clusters[i];
   h.device = device;
   h.sm_count = sms;
@@ -1126,10 +1111,12 @@ GEMM_API gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int64_t
   const gemm_status_t st = gemm_run(&slot.handle, M, N, K, L, A, lda, layoutA, B, ldb, layoutB,
                                     C, X, D, Y, alpha, beta, x_factor, dtypes, stream);
   if (st != GEMM_OK || !watchdog_out) return st;
+  // Read back on the caller's stream only (a plain cudaMemcpy would also wait
+  // on every other blocking stream of the device).
   uint32_t word = 0;
-  if (cudaStreamSynchronize(s) != cudaSuccess ||
-      cudaMemcpy(&word, slot.handle.d_status, sizeof(word), cudaMemcpyDeviceToHost) !=
-          cudaSuccess) {
+  if (cudaMemcpyAsync(&word, slot.handle.d_status, sizeof(word), cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
     cudaGetLastError();
     return GEMM_ERR_CUDA;
   }

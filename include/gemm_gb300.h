@@ -57,9 +57,13 @@ typedef enum {
   GEMM_ERR_UNSUPPORTED_CONFIG = 7  /* a forced kernel configuration cannot run this problem */
 } gemm_status_t;
 
-/* GEMM_TF32: fp32 storage read by the tensor core at tf32 precision (10-bit
- * mantissa; A and B must be K-major).  Values whose low 13 mantissa bits are
- * not zero are not exact inputs: the tensor core does not see those bits. */
+/* GEMM_TF32: fp32 storage read by the tensor core at tf32 precision (sign,
+ * exponent and the upper 10 fraction bits; A and B must be K-major).  Any fp32
+ * bit pattern is accepted.  Values that are tf32 values (low 13 fraction bits
+ * zero) are exact inputs and the result meets the fp32-input bound; for other
+ * values each operand is off by less than 2^-10 relative, each product by
+ * less than 2^-9 + 2^-20, and the accumulator bound grows by that term:
+ * |acc - exact| <= (2^-9 + 2^-20 + 2^-10) * sum_k |a*b|. */
 typedef enum {
   GEMM_F32 = 0, GEMM_F16 = 1, GEMM_BF16 = 2, GEMM_E4M3 = 3, GEMM_E5M2 = 4, GEMM_TF32 = 5
 } gemm_dtype_t;
@@ -302,9 +306,13 @@ gemm_status_t gemm_set_timeout_ns(gemm_handle_t h, uint64_t ns);
  * the GPU (different streams, no ordering between them) race on the status
  * word: one may clear or report the other's watchdog record.
  *
- * watchdog_out NULL: asynchronous, like gemm_run.  Non-NULL: the call then
- * synchronises `stream`, stores the status word there and returns
- * GEMM_ERR_DEVICE_TIMEOUT if it is non-zero. */
+ * watchdog_out NULL: asynchronous, like gemm_run; a watchdog record of that
+ * launch is then never reported (there is no handle to read it with, and the
+ * next call clears the word before its own launch).  Non-NULL: the call
+ * synchronises `stream` (only that stream), stores the status word there and
+ * returns GEMM_ERR_DEVICE_TIMEOUT if it is non-zero; pass NULL while
+ * `stream` is being captured into a graph, since a synchronisation would end
+ * the capture. */
 gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int64_t L,
                                const void* A, int64_t lda, gemm_layout_t layoutA,
                                const void* B, int64_t ldb, gemm_layout_t layoutB,

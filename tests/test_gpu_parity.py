@@ -12,8 +12,8 @@ import torch
 import oracle
 import workloads as W
 import dense_gemm_epilogue_persistent_gb300 as G
-from gemm_cases import (Case, compare_full, compare_sampled, logical, prepare, run_gpu,
-                        to_f64)
+from gemm_cases import (Case, assert_within, compare_full, compare_sampled, logical,
+                        oracle_problem, prepare, run_gpu, to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -260,6 +260,38 @@ def test_tf32_integers_exact(gemm):
     D, Y = run_gpu(gemm, prep)
     _finish(gemm)
     compare_full(prep, D, Y, exact=True)
+
+
+def test_tf32_general_fp32_inputs(gemm):
+    """GEMM_TF32 on fp32 values that are NOT tf32 values (low 13 fraction bits
+    set).  The tensor core reads sign, exponent and the upper 10 fraction bits
+    (truncated or rounded: either way each operand is off by less than 2^-10
+    relative), so each product is off by less than 2^-9 + 2^-20 relative and
+    the accumulator bound gains that term: |D - ref| <= (2^-9 + 2^-20 + 2^-10)
+    |alpha| sum|ab| + 2^-10 (|beta c| + |x_factor x|) against the exact result
+    on the fp32 values as given."""
+    case = Case(M=384, N=520, K=264, L=1, ab="tf32", c="f32", d="f32", x="f32", y="f32",
+                alpha=1.25, beta=0.5, xf=-2.0, dist="normal1", seed=68)
+    prep = prepare(case)
+    g = torch.Generator().manual_seed(1068)
+    prep.A = torch.randn(case.L, case.M, case.K, generator=g).contiguous()
+    prep.B = torch.randn(case.L, case.N, case.K, generator=g).contiguous()
+    low = lambda t: (t.view(torch.int32) & 0x1FFF) != 0
+    assert low(prep.A).float().mean() > 0.99 and low(prep.B).float().mean() > 0.99
+    gemm.set_config(None)
+    D, Y = run_gpu(gemm, prep)
+    _finish(gemm)
+    D_ref, Y_ref, S = oracle.gemm(oracle_problem(prep))
+    Cv, Xv = to_f64(prep.inp.C), to_f64(prep.inp.X)
+    acc_bound = (2.0 ** -9 + 2.0 ** -20 + 2.0 ** -10) * S
+    assert_within("D", to_f64(D), D_ref,
+                  abs(case.alpha) * acc_bound + 2.0 ** -10 * (abs(case.beta * Cv) +
+                                                              abs(case.xf * Xv)))
+    assert_within("Y", to_f64(Y), Y_ref, acc_bound)
+    # the operands' low bits are really dropped: Y is farther from the exact
+    # product of the fp32 values than fp32 accumulation of exact tf32 operands
+    # puts it (about 2^-20 of sum|ab| at this K)
+    assert np.max(np.abs(to_f64(Y) - Y_ref) / S) > 2.0 ** -17
 
 
 # ------------------------------------------------------------ fp16 accumulator

@@ -7,8 +7,13 @@ memory gemm_create would allocate.
 
 This file is collected last on purpose: if it fails, a run that stops at the
 first failure has already run every other test.  It must also pass alone in a
-fresh process, where its first call performs the per-device set-up.
+fresh process, where its first call performs the per-device set-up; the last
+test here runs the others that way.
 """
+import os
+import subprocess
+import sys
+
 import numpy as np
 import pytest
 import torch
@@ -51,6 +56,44 @@ def _dtypes(case):
                          G.GEMM_MN_MAJOR if case.cd_m else G.GEMM_K_MAJOR)
 
 
+def _run_handle(g, prep, stream):
+    c = prep.case
+    A, B, C, X = _device_inputs(prep)
+    D, Y = _outputs(c)
+    g.run(c.M, c.N, c.K, c.L, A, A.shape[-1], int(c.a_mn), B, B.shape[-1], int(c.b_mn), C, X,
+          D, Y, c.alpha, c.beta, c.xf, _dtypes(c), stream)
+    st, detail = g.sync_status(stream)
+    assert st == G.GEMM_OK, (G.gemm_status_string(st), hex(detail))
+    return D, Y
+
+
+def test_handle_still_runs_after_noalloc():
+    """A handle whose launch was prepared (with the most shared memory its
+    kernel allows) before the first no-allocation call must still launch
+    afterwards: the one-time set-up of gemm_run_noalloc may raise, but never
+    lower, a kernel's process-wide shared-memory limit.  Runs first in this
+    file, so in a fresh process the set-up happens between the two launches."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    prep = prepare(CASES[0])
+    stream = torch.cuda.current_stream()
+    g = G.Gemm(0)
+    try:
+        g.set_config(cta_group=2, tile_n=256, cluster_m=2)
+        D0, Y0 = _run_handle(g, prep, stream)
+        c = prep.case
+        A, B, C, X = _device_inputs(prep)
+        D1, Y1 = _outputs(c)
+        st, word = G.gemm_run_noalloc(c.M, c.N, c.K, c.L, A, A.shape[-1], int(c.a_mn), B,
+                                      B.shape[-1], int(c.b_mn), C, X, D1, Y1, c.alpha, c.beta,
+                                      c.xf, _dtypes(c), stream, watchdog=True)
+        assert st == G.GEMM_OK and word == 0
+        D2, Y2 = _run_handle(g, prep, stream)     # the cached launch, after the set-up
+        assert torch.equal(D0, D2) and torch.equal(Y0, Y2)
+    finally:
+        g.close()
+
+
 def test_noalloc_matches_gemm_run_two_calls_in_a_row():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
@@ -78,6 +121,17 @@ def test_noalloc_matches_gemm_run_two_calls_in_a_row():
     assert st == G.GEMM_OK and word == 0
     torch.cuda.synchronize()
 
+    # a warm call allocates nothing: neither device memory (free bytes of the
+    # device) nor anything from torch's caching allocator
+    free0 = torch.cuda.mem_get_info()[0]
+    n_alloc0 = torch.cuda.memory_stats().get("allocation.all.allocated", 0)
+    st, word = G.gemm_run_noalloc(c.M, c.N, c.K, c.L, A, A.shape[-1], int(c.a_mn), B,
+                                  B.shape[-1], int(c.b_mn), C, X, D_sync, Y_sync, c.alpha,
+                                  c.beta, c.xf, _dtypes(c), stream, watchdog=True)
+    assert st == G.GEMM_OK and word == 0
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert torch.cuda.memory_stats().get("allocation.all.allocated", 0) == n_alloc0
+
     # the same problems through the existing entry point
     g = G.Gemm(0)
     try:
@@ -102,7 +156,25 @@ def test_noalloc_matches_gemm_run_two_calls_in_a_row():
                 y_old = to_f64(logical(Y_ref, c.cd_m))
                 assert_within("Y noalloc vs gemm_run", y_new, y_old,
                               TOL_REL * S + ulp_at(c.y, Y_exact))
+                assert_within("Y noalloc vs oracle", y_new, Y_exact,
+                              TOL_REL * S + ulp_at(c.y, Y_exact))
         # the synchronising call gave the same result as the first call
         assert torch.equal(D_sync, got[0][0]) and torch.equal(Y_sync, got[0][1])
     finally:
         g.close()
+
+
+def test_noalloc_alone_in_a_fresh_process():
+    """The tests above, run again in a new process where nothing else has
+    touched the library: the first no-allocation call does the set-up."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    if os.environ.get("GEMM_NOALLOC_CHILD"):
+        pytest.skip("already the fresh process")
+    env = dict(os.environ, GEMM_NOALLOC_CHILD="1")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-p", "no:cacheprovider",
+                        os.path.abspath(__file__), "-k", "not fresh_process"],
+                       cwd=root, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
+    assert "2 passed" in r.stdout, r.stdout[-2000:]
