@@ -117,12 +117,17 @@ def recorded_traffic(workload: str, cfg):
 
 # ---------------------------------------------------------------- clocks
 
-class ClockSampler:
-    """nvidia-smi samples (every 100 ms) of this GPU's clocks, power and
-    throttle reasons while the timed region runs."""
+LOAD_W = 300.0        # a sample drawing more than this is "under load" (idle: ~170-190 W)
 
-    def __init__(self, pci_bus: int | None):
+
+class ClockSampler:
+    """nvidia-smi samples (every `period_ms`) of this GPU's clocks, power and
+    throttle reasons while a timed region runs.  The reported SM clock is the
+    median over the samples taken under load (all samples if none was)."""
+
+    def __init__(self, pci_bus: int | None, period_ms: int = 20):
         self.pci_bus = pci_bus
+        self.period_ms = period_ms
         self.proc = None
         self.out = None
 
@@ -131,13 +136,14 @@ class ClockSampler:
             self.out = open(os.path.join("/tmp", f"clocks_{os.getpid()}.csv"), "w+")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={SMI_FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=self.out, stderr=subprocess.DEVNULL)
+                 "-lms", str(self.period_ms)], stdout=self.out, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
     def stop(self):
         if not self.proc:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "samples_under_load": 0}
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -162,7 +168,8 @@ class ClockSampler:
             except ValueError:
                 return None
 
-        sm = [x for x in (num(r[1]) for r in mine) if x is not None]
+        loaded = [r for r in mine if (num(r[3]) or 0.0) > LOAD_W]
+        sm = [x for x in (num(r[1]) for r in (loaded or mine)) if x is not None]
         smax = [x for x in (num(r[2]) for r in mine) if x is not None]
         power = [x for x in (num(r[3]) for r in mine) if x is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -170,7 +177,8 @@ class ClockSampler:
                           if r[5 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
-                "samples": len(mine), "power_w_max": max(power) if power else None}
+                "samples": len(mine), "samples_under_load": len(loaded),
+                "period_ms": self.period_ms, "power_w_max": max(power) if power else None}
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -438,8 +446,14 @@ def main():
 
     import workloads as W
     from dense_gemm_epilogue_persistent_gb300 import build as _build
-    _build.build()
     import dense_gemm_epilogue_persistent_gb300 as G
+    if world > 1:
+        # A job that drives several GPUs builds and loads only the library
+        # without multicast kernels (no TMA multicast load in any of its
+        # sources); a single-GPU run takes the full library.
+        G.select_library(_build.build(kind="nomc"))
+    else:
+        _build.build()
 
     torch.cuda.set_device(local_rank)
     pg = init_ranks(world, rank)
@@ -574,17 +588,34 @@ def main():
             for name, wc in W.WORKLOADS.items():
                 inp_c = inp if name == w.name else W.make_inputs(wc)
                 bc = bound if name == w.name else Bound(G, g, wc, inp_c, device)
-                # 20 warm-up and 100 timed back-to-back launches, median and
-                # minimum over 5 repetitions (L2 warm across launches)
-                ms, ms_min = time_reps(torch, bc, stream, iters=100)
+                # 20 warm-up and 5 repetitions of N timed back-to-back
+                # launches (N = 100, or enough for 0.3 s per repetition on the
+                # benchmark workload, so that the clock sampler running over
+                # them sees the load); median and minimum (L2 warm across
+                # launches)
+                iters = 100
+                if name == w.name:
+                    iters = max(100, int(0.3e3 / max(kernel_ms, 1e-3)))
+                sampler_c = ClockSampler(getattr(props, "pci_bus_id", None))
+                sampler_c.start()
+                time.sleep(0.1)
+                ms, ms_min = time_reps(torch, bc, stream, iters=iters)
+                clk = sampler_c.stop()
                 c2 = g.last_config()
                 tf = wc.flops / (ms / 1e3) / 1e12
                 pk = tensor_peak(peaks, wc.ab)
                 ent = {"us": round(ms * 1e3, 2), "us_min": round(ms_min * 1e3, 2),
                        "tflops": round(tf, 1), "pct_of_peak": round(100 * tf / pk, 1),
-                       "peak_tflops": pk,
+                       "peak_tflops": pk, "launches_per_rep": iters,
                        "kernel": f"{c2.tile_m}x{c2.tile_n} cta_group={c2.cta_group}"
-                                 f" stages={c2.stages} grid={c2.grid_ctas}"}
+                                 f" cluster={c2.cluster_m}x{c2.cluster_n}"
+                                 f" stages={c2.stages} slots={c2.epi_slots}"
+                                 f" grid={c2.grid_ctas}",
+                       "clock": {"sm_mhz": clk["sm_mhz"], "samples": clk["samples"],
+                                 "samples_under_load": clk["samples_under_load"],
+                                 "reasons": clk["reasons"]}}
+                if clk["sm_mhz"] and clk["samples_under_load"]:
+                    ent["tflops_per_mhz"] = round(tf / clk["sm_mhz"], 4)
                 if bc.nbytes_in() < L2_BYTES:
                     # inputs fit in L2: also with L2 scrubbed before every launch
                     cold = time_cold_l2(torch, bc, stream)
@@ -606,6 +637,18 @@ def main():
                 raise SystemExit(f"per-config timing failed: {G.gemm_status_string(st)}")
         if not args.no_cpu_baseline:
             cpu_baseline = time_oracle_sample(w, inp, args.cpu_seconds)
+
+    # TFLOP/s per MHz of the benchmark workload, from its per-config region
+    # (seconds of back-to-back launches with the clock sampler running).
+    per_mhz = None
+    if per_config and w.name in per_config and "tflops_per_mhz" in per_config[w.name]:
+        pc = per_config[w.name]
+        per_mhz = {"value": pc["tflops_per_mhz"], "tflops": pc["tflops"],
+                   "sm_mhz": pc["clock"]["sm_mhz"],
+                   "samples_under_load": pc["clock"]["samples_under_load"],
+                   "region": f"per_config[{w.name}]: 5 x {pc['launches_per_rep']} back-to-back "
+                             "launches, median repetition; clock = median SM MHz of the "
+                             "samples under load in that region"}
 
     if rank == 0:
         line = {
@@ -631,6 +674,7 @@ def main():
             "cpu_baseline": cpu_baseline,
             "e2e": e2e,
             "clocks": clocks,
+            "tflops_per_mhz": per_mhz,
             "gpu_launches": args.steps,
             "kernel_ms_mean": kernel_ms,
             "per_config": per_config,

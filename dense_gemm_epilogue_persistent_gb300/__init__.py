@@ -18,7 +18,10 @@ import os
 import threading
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
+# The library for a process that drives one GPU (every kernel variant), and
+# the one for processes that drive several GPUs (no multicast kernels).
 LIB_PATH = os.path.join(_HERE, "libgemm_gb300.so")
+NOMC_LIB_PATH = os.path.join(_HERE, "libgemm_gb300_nomc.so")
 
 # enums (include/gemm_gb300.h)
 GEMM_OK = 0
@@ -29,6 +32,7 @@ GEMM_ERR_UNSUPPORTED_ARCH = 4
 GEMM_ERR_CUDA = 5
 GEMM_ERR_DEVICE_TIMEOUT = 6
 GEMM_ERR_UNSUPPORTED_CONFIG = 7
+GEMM_ERR_DEVICE_CHECK = 8
 
 GEMM_F32, GEMM_F16, GEMM_BF16, GEMM_E4M3, GEMM_E5M2, GEMM_TF32 = 0, 1, 2, 3, 4, 5
 GEMM_K_MAJOR, GEMM_MN_MAJOR = 0, 1
@@ -53,7 +57,8 @@ class gemm_config_t(ctypes.Structure):
                 ("grid_ctas", ctypes.c_int), ("epi_slots", ctypes.c_int),
                 ("epi_slot_bytes", ctypes.c_int), ("cluster_m", ctypes.c_int),
                 ("l2_hints", ctypes.c_int), ("epi_wait_ns", ctypes.c_int),
-                ("inject_stall", ctypes.c_int), ("tail_split", ctypes.c_int)]
+                ("inject_stall", ctypes.c_int), ("tail_split", ctypes.c_int),
+                ("cluster_n", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

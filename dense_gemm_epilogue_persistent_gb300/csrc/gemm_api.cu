@@ -12,6 +12,7 @@
 // cudaDevAttrMaxSharedMemoryPerBlockOptin before launching.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cstdint>
@@ -47,7 +48,9 @@ constexpr int kMaxEpiSlots = 6;
 // A first / B normal 1370 / 1546, against 1468 / 1625 in the same runs.
 constexpr int kDefaultL2Hints = 2 | (2 << 2) | (2 << 4);
 constexpr int kDefaultEpiWaitNs = 0;
-constexpr int kSmemSlack = 1024 + 16;   // base alignment + abort flag + watchdog-test barrier
+// base alignment + abort flag + watchdog-test barrier + the epilogue warps'
+// ring-batch barriers
+constexpr int kSmemSlack = 1024 + 16 + 32;
 
 struct VariantState {
   bool smem_attr_set = false;  // max dynamic smem attribute raised to the opt-in limit
@@ -76,6 +79,30 @@ struct LaunchEntry {
 
 constexpr int kLaunchCacheEntries = 4;
 
+// NVTX ranges in the "gemm_gb300" domain around every entry point that
+// enqueues work (and around planning and tensor-map encoding on a launch-cache
+// miss), so that a profiler's timeline and its range filters (ncu --nvtx
+// --nvtx-include "gemm_gb300@gemm_run/") can pick the library's calls out.
+// Without a tool attached each push and pop returns at once.
+nvtxDomainHandle_t nvtx_domain() {
+  static const nvtxDomainHandle_t d = nvtxDomainCreateA("gemm_gb300");
+  return d;
+}
+
+struct NvtxRange {
+  explicit NvtxRange(const char* name) {
+    nvtxEventAttributes_t a{};
+    a.version = NVTX_VERSION;
+    a.size = NVTX_EVENT_ATTRIB_STRUCT_SIZE;
+    a.messageType = NVTX_MESSAGE_TYPE_ASCII;
+    a.message.ascii = name;
+    nvtxDomainRangePushEx(nvtx_domain(), &a);
+  }
+  ~NvtxRange() { nvtxDomainRangePop(nvtx_domain()); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
 }  // namespace
 
 struct gemm_handle {
@@ -88,8 +115,8 @@ struct gemm_handle {
   gemm_config_t forced_cfg{};
   gemm_config_t last{};
   uint64_t timeout_ns = kDefaultTimeoutNs;
-  VariantState variants[3][2][2][2];   // [ab 16/8/32][cta_group 1/2][tile_n 128/256][mc 1/2]
-  int clusters_by_size[5] = {0, 0, 0, 0, 0};   // resident clusters of 1, 2, 4 CTAs
+  VariantState variants[3][2][2][2][2];   // [ab 16/8/32][cta_group][k atoms][mc][nc]
+  int clusters_by_size[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};   // resident clusters of 1, 2, 4, 8 CTAs
   uint64_t config_gen = 0;
   LaunchEntry cache[kLaunchCacheEntries];
   int cache_next = 0;
@@ -193,11 +220,10 @@ gemm_status_t validate(const gemm_problem_t* pp) {
 
 // A/B ring bytes per CTA: stages x (A stage + B stage) + 8 bytes per
 // mbarrier (full and empty per stage, full and empty per accumulator stage)
-// + 4 bytes of tensor-memory address.  A stage holds k_atoms 128-byte-wide
-// K atoms of 128 A rows and tile_n / cta_group B rows.
-int ring_bytes(int cta_group, int tile_n, int ab_bytes, int stages) {
-  (void)ab_bytes;
-  const int stage = (128 * 128 + (tile_n / cta_group) * 128) * gb300::k_atoms(cta_group, tile_n);
+// + 4 bytes of tensor-memory address.  A stage holds `ka` 128-byte-wide K
+// atoms of 128 A rows and tile_n / cta_group B rows.
+int ring_bytes(int cta_group, int tile_n, int ka, int stages) {
+  const int stage = (128 * 128 + (tile_n / cta_group) * 128) * ka;
   return stages * stage + 8 * (2 * stages + 2 * gb300::kAccStages) + 4;
 }
 
@@ -215,20 +241,28 @@ int epi_slot_bytes(const gemm_problem_t& p) {
 
 // Dynamic shared memory of one CTA: A/B ring, epilogue slots, every mbarrier
 // (full/empty per stage, full/empty per accumulator stage, one per epilogue
-// slot), tensor-memory address and abort flag, plus 1 KiB of alignment slack.
-int total_smem(int cg, int bn, int ab_bytes, int stages, int slots, int slot_bytes) {
-  return ring_bytes(cg, bn, ab_bytes, stages) + slots * slot_bytes + 8 * slots + 4 + kSmemSlack;
+// warp and slot), tensor-memory address and abort flag, plus 1 KiB of
+// alignment slack.
+int total_smem(int cg, int bn, int ka, int stages, int slots, int slot_bytes) {
+  return ring_bytes(cg, bn, ka, stages) + slots * slot_bytes + 8 * 4 * slots + 4 + kSmemSlack;
 }
 
-bool variant_supports(const gemm_problem_t& p, int cg, int bn, int mc) {
+// Tile widths: multiples of 32 from 64 to 256 (the custom-epilogue example's
+// "Constraints" allow MMA tile N from 32 to 256 in steps of 32; 32 is left
+// out, its tiles are too thin to feed the tensor pipe from shared memory).
+bool valid_tile_n(int bn) { return bn >= 64 && bn <= 256 && bn % 32 == 0; }
+
+bool variant_supports(const gemm_problem_t& p, int cg, int bn, int mc, int nc) {
   if (cg != 1 && cg != 2) return false;
-  if (bn != 128 && bn != 256) return false;
-  if (mc != 1 && mc != 2) return false;
+  if (!valid_tile_n(bn)) return false;
+  if ((mc != 1 && mc != 2) || (nc != 1 && nc != 2)) return false;
   const int ab_bytes = dtype_bytes(p.dtypes.ab);
   const int atom = 128 / ab_bytes;
-  // MN-major B is staged (and multicast) in swizzle atoms of `atom` rows.
+  // MN-major operands are staged (and multicast) in swizzle atoms of `atom`
+  // rows: a CTA's B part (tile_n / cta_group / mc rows) and A part (128 / nc
+  // rows) must be whole atoms.
   if (p.layoutB == GEMM_MN_MAJOR && (bn / cg / mc) % atom != 0) return false;
-  if (p.layoutA == GEMM_MN_MAJOR && 128 % atom != 0) return false;
+  if (p.layoutA == GEMM_MN_MAJOR && (128 / nc) % atom != 0) return false;
   return true;
 }
 
@@ -239,32 +273,34 @@ bool variant_supports(const gemm_problem_t& p, int cg, int bn, int mc) {
 // Constants fitted (least squares on log time, variants compared within each
 // problem) to a GB300 sweep of every variant over 17 problems: 256^3 to 8192^3,
 // K from 256 to 8192, 16-bit, fp8 and tf32 inputs, fp32 and 16-bit epilogues with
-// and without C, X and Y, ragged and batched shapes:
-//   main loop per k-block  2x256: 1.0   1x256: 1.23   2x128: 0.72   1x128: 0.68;
-//   fixed per tile         2x256: 13.1  1x256: 10.6   2x128: 15.0   1x128: 11.0;
-//   epilogue: tile_n/32 chunks per CTA, each 1.64 + 0.043 per KB the chunk moves
-//     (C and X read, D and Y written, 128 x 32 elements each) + 6.0 spread over
-//     the slots - 1 chunks of C/X lookahead when it loads;
-//   a last wave split into half-width items (tail_split) costs ~0.6 of a wave.
-// Clusters of two CTA groups sharing B by multicast were never fastest in that
-// sweep, so the automatic choice leaves them out; a forced configuration may
-// still select them (their cost: the pair's, with the wave count of the 4-CTA
-// clusters that fit).
-double plan_cost(int64_t tiles, int64_t k_blocks, int cg, int mc, int bn, int64_t clusters,
+// and without C, X and Y, ragged and batched shapes.  Main loop per k-block:
+// the tile's share of tensor work (tile_n / 256) plus a feed overhead that
+// grows as the tile narrows (each CTA still stages 128 A rows per k-block):
+//   CTA pairs          tile_n/256 + 0.22 (256 - tile_n)/128   (2x256: 1.0, 2x128: 0.72)
+//   single CTAs, 2 atoms per stage   tile_n/256 + 0.18 (256 - tile_n)/128   (1x128: 0.68)
+//   single CTAs, 1 atom per stage    1.23 tile_n/256                       (1x256: 1.23)
+// fixed per tile: pairs 15.0 - 1.9 (tile_n - 128)/128, single CTAs 11.0 -
+// 0.4 (tile_n - 128)/128; epilogue: tile_n/32 chunks per CTA, each 1.64 + 0.043
+// per KB the chunk moves (C and X read, D and Y written, 128 x 32 elements
+// each) + 6.0 spread over the slots - 1 chunks of C/X lookahead when it
+// loads; a last wave split into half-width items (tail_split) costs ~0.6 of
+// a wave.  Clusters that share operands by multicast pay the wave count of
+// the larger clusters that fit.
+double plan_cost(int64_t tiles, int64_t k_blocks, int cg, int ka, int bn, int64_t clusters,
                  bool epi_loads, int epi_slots, double epi_kb, bool can_split) {
   clusters = std::max<int64_t>(1, clusters);
   const int64_t full = tiles / clusters, rem = tiles % clusters;
   const double waves =
       (double)full + (rem == 0 ? 0.0 : (can_split && 2 * rem <= clusters ? 0.6 : 1.0));
+  const double w = bn / 256.0;
   double per_kb, fixed;
-  if (bn == 256) {
-    per_kb = cg == 2 ? 1.0 : 1.23;
-    fixed = cg == 2 ? 13.1 : 10.6;
+  if (cg == 2) {
+    per_kb = w + 0.22 * (256 - bn) / 128.0;
+    fixed = 15.0 - 1.9 * (bn - 128) / 128.0;
   } else {
-    per_kb = cg == 2 ? 0.72 : 0.68;
-    fixed = cg == 2 ? 15.0 : 11.0;
+    per_kb = ka == 1 ? 1.23 * w : w + 0.18 * (256 - bn) / 128.0;
+    fixed = 11.0 - 0.4 * (bn - 128) / 128.0;
   }
-  (void)mc;
   const double main_loop = (double)k_blocks * per_kb;
   const double chunk =
       1.64 + 0.043 * epi_kb + (epi_loads ? 6.0 / std::max(1, epi_slots - 1) : 0.0);
@@ -272,23 +308,28 @@ double plan_cost(int64_t tiles, int64_t k_blocks, int cg, int mc, int bn, int64_
   return waves * (std::max(main_loop, epilogue) + fixed);
 }
 
-// Whether the last wave of a variant may run as half-width items: CTA groups
-// without multicast (a cluster's groups share B), and B staged in whole
-// 128-byte atoms at half width.
-bool can_split_tail(const gemm_problem_t& p, int cg, int bn, int mc) {
-  if (mc != 1) return false;
+// Whether the last wave of a variant may run as half-width items: clusters of
+// one CTA group (groups of a larger cluster share operands), half tiles that
+// are whole epilogue chunks, and B staged in whole 128-byte atoms at half
+// width.
+bool can_split_tail(const gemm_problem_t& p, int cg, int bn, int mc, int nc) {
+  if (mc != 1 || nc != 1) return false;
+  if ((bn / 2) % gb300::kEpiChunk != 0) return false;
   const int atom = 128 / dtype_bytes(p.dtypes.ab);
   return p.layoutB == GEMM_K_MAJOR || (bn / cg / 2) % atom == 0;
 }
 
 // Epilogue slots the planner gives a variant: the deepest ring that leaves two
-// slots, then every further slot that fits (at most kMaxEpiSlots).
-int auto_slots(int cg, int bn, int ab_bytes, int slot, int smem_optin) {
+// slots (one stage less when the problem is a single wave of tiles and the
+// ring stays at least three deep), then every further slot that fits (at
+// most kMaxEpiSlots).
+int auto_slots(int cg, int bn, int ka, int slot, int smem_optin, bool one_wave) {
   int stages = 0;
-  while (stages < kMaxStages && total_smem(cg, bn, ab_bytes, stages + 1, 2, slot) <= smem_optin)
+  while (stages < kMaxStages && total_smem(cg, bn, ka, stages + 1, 2, slot) <= smem_optin)
     ++stages;
+  if (one_wave && stages >= 4) --stages;
   int slots = 2;
-  while (slots < kMaxEpiSlots && total_smem(cg, bn, ab_bytes, stages, slots + 1, slot) <= smem_optin)
+  while (slots < kMaxEpiSlots && total_smem(cg, bn, ka, stages, slots + 1, slot) <= smem_optin)
     ++slots;
   return slots;
 }
@@ -296,7 +337,8 @@ int auto_slots(int cg, int bn, int ab_bytes, int slot, int smem_optin) {
 // Resident clusters of `csize` CTAs: the device's measured occupancy when
 // known (clusters_by_size[csize]), else SMs / csize.
 int64_t resident_clusters(int sm_count, const int* clusters_by_size, int csize) {
-  if (clusters_by_size && clusters_by_size[csize] > 0) return clusters_by_size[csize];
+  if (clusters_by_size && csize <= 8 && clusters_by_size[csize] > 0)
+    return clusters_by_size[csize];
   return std::max(1, sm_count / csize);
 }
 
@@ -312,41 +354,58 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
   const int fcg = forced ? forced->cta_group : 0;
   const int fbn = forced ? forced->tile_n : 0;
   const int fmc = forced ? forced->cluster_m : 0;
-  int cg = 0, bn = 0, mc = 0;
+  const int fnc = forced ? forced->cluster_n : 0;
+  int cg = 0, bn = 0, mc = 0, nc = 0;
   double best = 1e300;
   // KB an epilogue chunk (128 x 32 elements of each tensor) moves per CTA.
   const double epi_kb =
       128.0 * gb300::kEpiChunk *
       ((reads_c(p) ? dtype_bytes(p.dtypes.c) : 0) + (reads_x(p) ? dtype_bytes(p.dtypes.x) : 0) +
        dtype_bytes(p.dtypes.d) + (p.Y ? dtype_bytes(p.dtypes.y) : 0)) / 1024.0;
+  // Widest tiles first: among equal costs the wider (fewer-tile) one wins.
+  // The automatic choice takes widths of 128 and more (the range the cost
+  // model's constants were measured on); 64 and 96 run when forced.
   for (int a : {2, 1})
-    for (int b : {256, 128})
-      for (int m : {1, 2}) {
-        if ((fcg && a != fcg) || (fbn && b != fbn)) continue;
-        // Automatic choice: no multicast clusters (see plan_cost).
-        if (fmc ? m != fmc : m == 2) continue;
-        if (!variant_supports(p, a, b, m)) continue;
-        const int64_t tiles = cdiv(std::max<int64_t>(p.M, 1), 128 * a * m) *
-                              cdiv(std::max<int64_t>(p.N, 1), b) * std::max<int64_t>(p.L, 1);
-        const double c = plan_cost(tiles, cdiv(p.K, 128 / ab_bytes), a, m, b,
-                                   resident_clusters(sm_count, clusters_by_size, a * m),
-                                   reads_c(p) || reads_x(p),
-                                   auto_slots(a, b, ab_bytes, epi_slot_bytes(p), smem_optin),
-                                   epi_kb,
-                                   can_split_tail(p, a, b, m) &&
-                                       !(forced && forced->tail_split == 1));
-        if (c < best - 1e-9) { best = c; cg = a; bn = b; mc = m; }
-      }
+    for (int b = 256; b >= 64; b -= 32)
+      for (int m : {1, 2})
+        for (int n : {1, 2}) {
+          if ((fcg && a != fcg) || (fbn && b != fbn)) continue;
+          if (!fbn && b < 128) continue;
+          // The library for multi-GPU processes has no multicast kernels.
+          if (!GB300_MULTICAST && (m > 1 || n > 1)) continue;
+          // Automatic choice: no operand-sharing clusters (see plan_cost); a
+          // forced cluster shape fixes both extents (0 counts as 1).
+          if (fmc || fnc) {
+            if (m != std::max(fmc, 1) || n != std::max(fnc, 1)) continue;
+          } else if (m != 1 || n != 1) {
+            continue;
+          }
+          if (!variant_supports(p, a, b, m, n)) continue;
+          const int ka = gb300::k_atoms(a, b);
+          const int64_t tiles = cdiv(std::max<int64_t>(p.M, 1), 128 * a * m) *
+                                cdiv(std::max<int64_t>(p.N, 1), (int64_t)b * n) *
+                                std::max<int64_t>(p.L, 1);
+          const int64_t units = resident_clusters(sm_count, clusters_by_size, a * m * n);
+          const double c = plan_cost(tiles, cdiv(p.K, 128 / ab_bytes), a, ka, b, units,
+                                     reads_c(p) || reads_x(p),
+                                     auto_slots(a, b, ka, epi_slot_bytes(p), smem_optin,
+                                                tiles <= units),
+                                     epi_kb,
+                                     can_split_tail(p, a, b, m, n) &&
+                                         !(forced && forced->tail_split == 1));
+          if (c < best - 1e-9) { best = c; cg = a; bn = b; mc = m; nc = n; }
+        }
   if (!cg) return GEMM_ERR_UNSUPPORTED_CONFIG;
-  if (gemm_tmem_columns(128, bn) * gb300::kAccStages > (int)gb300::kTmemCols)
-    return GEMM_ERR_UNSUPPORTED_CONFIG;
+  if (gemm_tmem_columns(128, bn) > (int)gb300::kAccStride) return GEMM_ERR_UNSUPPORTED_CONFIG;
+  const int ka = gb300::k_atoms(cg, bn);
+  const int csize = cg * mc * nc;
 
   // Epilogue slots: a C/D region and an X/Y region of 128 x 32 elements each,
   // sized for the wider of the two types that share it.
   const int slot = epi_slot_bytes(p);
   auto max_stages_for = [&](int slots) {
     int n = 0;
-    while (n < kMaxStages && total_smem(cg, bn, ab_bytes, n + 1, slots, slot) <= smem_optin) ++n;
+    while (n < kMaxStages && total_smem(cg, bn, ka, n + 1, slots, slot) <= smem_optin) ++n;
     return n;
   };
   // The deepest A/B ring that still leaves two epilogue slots, then every
@@ -354,32 +413,26 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
   // keeps the epilogue ahead of fast main loops (8-bit inputs, short K).
   const int max_stages = max_stages_for(2);
   int stages = forced && forced->stages ? forced->stages : max_stages;
+  const int64_t tiles_m = cdiv(std::max<int64_t>(p.M, 1), 128 * cg * mc);
+  const int64_t tiles_n = cdiv(std::max<int64_t>(p.N, 1), (int64_t)bn * nc);
+  const int64_t tiles = tiles_m * tiles_n * std::max<int64_t>(p.L, 1);
+  const int64_t units = resident_clusters(sm_count, clusters_by_size, csize);
   // One wave: every CTA runs one tile and then its whole epilogue, which nothing
   // overlaps.  A ring one stage shallower (still >= 3 deep) frees room for more
   // epilogue slots, so C/X load further ahead (2048^3 bf16, fp32 C/D: 24.3 ->
   // 21.7 us with 3 stages and 5 slots instead of 4 and 2; 2 stages is slower).
-  {
-    const int64_t wave_tiles = cdiv(std::max<int64_t>(p.M, 1), 128 * cg * mc) *
-                               cdiv(std::max<int64_t>(p.N, 1), bn) * std::max<int64_t>(p.L, 1);
-    if (!(forced && forced->stages) && max_stages >= 4 &&
-        wave_tiles <= resident_clusters(sm_count, clusters_by_size, cg * mc))
-      stages = max_stages - 1;
-  }
+  if (!(forced && forced->stages) && max_stages >= 4 && tiles <= units) stages = max_stages - 1;
   if (stages < 2 || stages > max_stages) return GEMM_ERR_UNSUPPORTED_CONFIG;
   int slots = 2;
-  while (slots < kMaxEpiSlots &&
-         total_smem(cg, bn, ab_bytes, stages, slots + 1, slot) <= smem_optin)
+  while (slots < kMaxEpiSlots && total_smem(cg, bn, ka, stages, slots + 1, slot) <= smem_optin)
     ++slots;
   if (forced && forced->epi_slots) {
     slots = forced->epi_slots;
     if (slots < 2 || slots > kMaxEpiSlots ||
-        total_smem(cg, bn, ab_bytes, stages, slots, slot) > smem_optin)
+        total_smem(cg, bn, ka, stages, slots, slot) > smem_optin)
       return GEMM_ERR_UNSUPPORTED_CONFIG;
   }
 
-  const int64_t tiles_m = cdiv(std::max<int64_t>(p.M, 1), 128 * cg * mc);
-  const int64_t tiles_n = cdiv(std::max<int64_t>(p.N, 1), bn);
-  const int64_t tiles = tiles_m * tiles_n * std::max<int64_t>(p.L, 1);
   // Strips of 12 tile rows: with the serpentine strip order and the K
   // direction alternating per wave, 8192^3 reads 1.206 GB from DRAM per launch
   // at 12 (1.235 GB at 8, 1.514 GB at 4, 1.307 GB at 16) and runs 0.5-0.8 %
@@ -394,27 +447,26 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
   c.group_m = group_m;
   c.tile_m = 128 * cg;
   c.cluster_m = mc;
+  c.cluster_n = nc;
   c.l2_hints = forced && (forced->l2_hints & 0x100) ? (forced->l2_hints & 0x3F) : kDefaultL2Hints;
   c.epi_wait_ns = forced && forced->epi_wait_ns > 0 ? forced->epi_wait_ns - 1 : kDefaultEpiWaitNs;
   c.inject_stall = forced && forced->inject_stall ? 1 : 0;
-  c.tile_k = 128 / ab_bytes * gb300::k_atoms(cg, bn);
+  c.tile_k = 128 / ab_bytes * ka;
   c.acc_stages = gb300::kAccStages;
-  c.ring_bytes = ring_bytes(cg, bn, ab_bytes, stages);
+  c.ring_bytes = ring_bytes(cg, bn, ka, stages);
   c.epi_slots = slots;
   c.epi_slot_bytes = slot;
   // At least half the opt-in limit: one CTA per SM, so no two CTAs ever
   // contend for the 512 tensor-memory columns each allocates.
-  c.smem_bytes = std::max(total_smem(cg, bn, ab_bytes, stages, slots, slot),
-                          smem_optin / 2 + 1024);
+  c.smem_bytes = std::max(total_smem(cg, bn, ka, stages, slots, slot), smem_optin / 2 + 1024);
   c.tiles = tiles;
-  const int64_t units = resident_clusters(sm_count, clusters_by_size, cg * mc);
   int64_t split = 0;
-  if (can_split_tail(p, cg, bn, mc) && !(forced && forced->tail_split == 1)) {
+  if (can_split_tail(p, cg, bn, mc, nc) && !(forced && forced->tail_split == 1)) {
     const int64_t rem = tiles % units;
     if (rem > 0 && 2 * rem <= units) split = rem;
   }
   c.tail_split = (int)split;
-  c.grid_ctas = (int)(std::min<int64_t>(tiles + split, units) * cg * mc);
+  c.grid_ctas = (int)(std::min<int64_t>(tiles + split, units) * csize);
   *out = c;
   return GEMM_OK;
 }
@@ -453,10 +505,10 @@ bool encode_operand(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int dt
   return r == CUDA_SUCCESS;
 }
 
-// Epilogue tensor map over a packed M x N x L tensor, box = 128 rows x 32
-// columns.  Row-major: dims {N, M, L}, 128-byte (fp32) or 64-byte (16-bit) rows
-// swizzled to match the epilogue's shared-memory reads.  Column-major: dims
-// {M, N, L}, unswizzled.
+// Epilogue tensor map over a packed M x N x L tensor, box = 32 rows x 32
+// columns (one epilogue warp's rows of one chunk).  Row-major: dims {N, M, L},
+// 128-byte (fp32) or 64-byte (16-bit) rows swizzled to match the epilogue's
+// shared-memory reads.  Column-major: dims {M, N, L}, unswizzled.
 bool encode_epi(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int dt, int64_t M,
                 int64_t N, int64_t L, bool m_major) {
   const int64_t es = dtype_bytes(dt);
@@ -468,13 +520,13 @@ bool encode_epi(EncodeTiledFn enc, CUtensorMap* map, const void* ptr, int dt, in
     dims[0] = (cuuint64_t)N; dims[1] = (cuuint64_t)M; dims[2] = (cuuint64_t)L;
     strides[0] = (cuuint64_t)(N * es);
     strides[1] = (cuuint64_t)(N * es * M);
-    box[0] = gb300::kEpiChunk; box[1] = 128; box[2] = 1;
+    box[0] = gb300::kEpiChunk; box[1] = gb300::kSubRows; box[2] = 1;
     sw = es == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   } else {
     dims[0] = (cuuint64_t)M; dims[1] = (cuuint64_t)N; dims[2] = (cuuint64_t)L;
     strides[0] = (cuuint64_t)(M * es);
     strides[1] = (cuuint64_t)(M * es * N);
-    box[0] = 128; box[1] = gb300::kEpiChunk; box[2] = 1;
+    box[0] = gb300::kSubRows; box[1] = gb300::kEpiChunk; box[2] = 1;
     sw = CU_TENSOR_MAP_SWIZZLE_NONE;
   }
   CUresult r = enc(map, ty, 3, const_cast<void*>(ptr), dims, strides, box, estr,
@@ -517,11 +569,13 @@ gemm_status_t prepare_launch(gemm_handle* h, const gemm_problem_t& p, LaunchEntr
   if (st != GEMM_OK) return st;
 
   const int ab_bytes = dtype_bytes(dtypes->ab);
-  const int csize = cfg.cta_group * cfg.cluster_m;
-  const void* kern = gb300::kernel_for(ab_bytes, cfg.cta_group, cfg.tile_n, cfg.cluster_m);
+  const int csize = cfg.cta_group * cfg.cluster_m * cfg.cluster_n;
+  const int ka = gb300::k_atoms(cfg.cta_group, cfg.tile_n);
+  const void* kern =
+      gb300::kernel_for(ab_bytes, cfg.cta_group, ka, cfg.cluster_m, cfg.cluster_n);
   if (!kern) return GEMM_ERR_UNSUPPORTED_CONFIG;
   VariantState& vs = h->variants[ab_bytes == 2 ? 0 : ab_bytes == 1 ? 1 : 2][cfg.cta_group - 1]
-                                [cfg.tile_n == 256 ? 1 : 0][cfg.cluster_m - 1];
+                                [ka - 1][cfg.cluster_m - 1][cfg.cluster_n - 1];
 
   cudaLaunchConfig_t lc{};
   cudaLaunchAttribute attr[1];
@@ -562,7 +616,11 @@ gemm_status_t prepare_launch(gemm_handle* h, const gemm_problem_t& p, LaunchEntr
   std::memset(&tmA, 0, sizeof(tmA));
   std::memset(&tmB, 0, sizeof(tmB));
   if (K > 0) {
-    if (!encode_operand(h->encode, &tmA, A, dtypes->ab, M, K, L, lda, a_mn, 128, cfg.tile_k) ||
+    // Each CTA loads 128 / cluster_n A rows and tile_n / cta_group / cluster_m
+    // B rows per K atom (the rest of its slices arrive from the CTAs that
+    // share them).
+    if (!encode_operand(h->encode, &tmA, A, dtypes->ab, M, K, L, lda, a_mn, 128 / cfg.cluster_n,
+                        cfg.tile_k) ||
         !encode_operand(h->encode, &tmB, B, dtypes->ab, N, K, L, ldb, b_mn,
                         cfg.tile_n / cfg.cta_group / cfg.cluster_m, cfg.tile_k))
       return GEMM_ERR_CUDA;
@@ -581,8 +639,9 @@ gemm_status_t prepare_launch(gemm_handle* h, const gemm_problem_t& p, LaunchEntr
 
   KernelParams kp{};
   kp.M = (int)M; kp.N = (int)N; kp.K = (int)K; kp.L = (int)L;
+  kp.bn = cfg.tile_n;
   kp.tiles_m = (int)cdiv(M, (int64_t)cfg.tile_m * cfg.cluster_m);
-  kp.tiles_n = (int)cdiv(N, cfg.tile_n);
+  kp.tiles_n = (int)cdiv(N, (int64_t)cfg.tile_n * cfg.cluster_n);
   kp.num_tiles = (int)cfg.tiles;
   kp.k_blocks = (int)cdiv(K, cfg.tile_k);
   kp.group_m = cfg.group_m;
@@ -635,7 +694,14 @@ gemm_status_t prepare_launch(gemm_handle* h, const gemm_problem_t& p, LaunchEntr
   return GEMM_OK;
 }
 
-// Resident clusters of 1, 2 and 4 CTAs at one CTA per SM (every
+// Status of a non-zero device status word: a failed bounds check of the
+// debug build (0xD0......) or a watchdog timeout (0xE0......).
+gemm_status_t status_of_word(uint32_t word) {
+  if (word == 0) return GEMM_OK;
+  return (word >> 24) == 0xD0u ? GEMM_ERR_DEVICE_CHECK : GEMM_ERR_DEVICE_TIMEOUT;
+}
+
+// Resident clusters of 1, 2, 4 and 8 CTAs at one CTA per SM (every
 // configuration uses more than half of the shared memory), from the occupancy
 // calculator on a representative kernel; `device` must be current.  The
 // kernel's shared-memory attribute is process-wide: it is raised to the
@@ -643,13 +709,13 @@ gemm_status_t prepare_launch(gemm_handle* h, const gemm_problem_t& p, LaunchEntr
 // another handle may have launches prepared with more than the size queried
 // here.  Counts the calculator does not give stay 0 (the planner then
 // assumes SMs / cluster size).
-void query_cluster_occupancy(int device, int sms, int optin, int (&clusters)[5]) {
+void query_cluster_occupancy(int device, int sms, int optin, int (&clusters)[9]) {
   (void)device;
-  const void* kern = gb300::kernel_for(2, 2, 256, 2);
+  const void* kern = gb300::kernel_for(2, 2, 2, 1, 1);
   const int smem = optin / 2 + 1024;
   if (kern && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) ==
                   cudaSuccess) {
-    for (int cs : {1, 2, 4}) {
+    for (int cs : {1, 2, 4, 8}) {
       cudaLaunchConfig_t lc{};
       cudaLaunchAttribute attr[1];
       lc.gridDim = dim3((unsigned)(cs * sms));
@@ -682,6 +748,7 @@ GEMM_API const char* gemm_status_string(gemm_status_t s) {
     case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA";
     case GEMM_ERR_DEVICE_TIMEOUT: return "GEMM_ERR_DEVICE_TIMEOUT";
     case GEMM_ERR_UNSUPPORTED_CONFIG: return "GEMM_ERR_UNSUPPORTED_CONFIG";
+    case GEMM_ERR_DEVICE_CHECK: return "GEMM_ERR_DEVICE_CHECK";
   }
   return "GEMM_ERR_UNKNOWN";
 }
@@ -738,13 +805,13 @@ GEMM_API gemm_status_t gemm_create(gemm_handle_t* out, int device) {
     cudaGetLastError();
     return GEMM_ERR_CUDA;
   }
-  // Resident clusters of 1, 2 and 4 CTAs at one CTA per SM.
-  int clusters[5] = {0, 0, 0, 0, 0};
+  // Resident clusters of 1, 2, 4 and 8 CTAs at one CTA per SM.
+  int clusters[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
   if (cudaSetDevice(device) == cudaSuccess) query_cluster_occupancy(device, sms, optin, clusters);
   cudaGetLastError();
   cudaSetDevice(prev);
   gemm_handle* h = new gemm_handle();
-  for (int i = 0; i < 5; ++i) h->clusters_by_size[i] = clusters[i];
+  for (int i = 0; i < 9; ++i) h->clusters_by_size[i] = clusters[i];
   h->device = device;
   h->sm_count = sms;
   h->smem_optin = optin;
@@ -790,8 +857,9 @@ GEMM_API gemm_status_t gemm_set_config(gemm_handle_t h, const gemm_config_t* cfg
     return GEMM_OK;
   }
   if ((cfg->cta_group && cfg->cta_group != 1 && cfg->cta_group != 2) ||
-      (cfg->tile_n && cfg->tile_n != 128 && cfg->tile_n != 256) || cfg->stages < 0 ||
+      (cfg->tile_n && !valid_tile_n(cfg->tile_n)) || cfg->stages < 0 ||
       (cfg->cluster_m && cfg->cluster_m != 1 && cfg->cluster_m != 2) ||
+      (cfg->cluster_n && cfg->cluster_n != 1 && cfg->cluster_n != 2) ||
       cfg->epi_slots < 0 || cfg->epi_slots > kMaxEpiSlots || cfg->epi_wait_ns < 0 ||
       cfg->tail_split < 0 || cfg->tail_split > 1 ||
       cfg->epi_wait_ns > 1000001 ||
@@ -821,6 +889,7 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
                                 int64_t ldb, gemm_layout_t layoutB, const void* C, const void* X,
                                 void* D, void* Y, float alpha, float beta, float x_factor,
                                 const gemm_dtypes_t* dtypes, struct CUstream_st* stream) {
+  NvtxRange range("gemm_run");
   if (!h || !dtypes) return GEMM_ERR_INVALID_ARG;
   gemm_problem_t p{M, N, K, L, A, lda, layoutA, B, ldb, layoutB, C, X, D, Y,
                    alpha, beta, x_factor, *dtypes};
@@ -853,6 +922,7 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
   if (!ent) {
     LaunchEntry& slot = h->cache[h->cache_next];
     slot.valid = false;
+    NvtxRange prep("gemm_run:plan_and_encode");
     st = prepare_launch(h, p, slot);
     if (st != GEMM_OK) return st;
     slot.key = key;
@@ -898,6 +968,7 @@ GEMM_API gemm_status_t gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int6
                                      void* D, void* Y, float alpha, float beta,
                                      float x_factor, const gemm_dtypes_t* dtypes,
                                      struct CUstream_st* stream) {
+  NvtxRange range("gemm_run_host");
   if (!h || !dtypes) return GEMM_ERR_INVALID_ARG;
   gemm_problem_t p{M, N, K, L, A, lda, layoutA, B, ldb, layoutB, C, X, D, Y,
                    alpha, beta, x_factor, *dtypes};
@@ -1005,7 +1076,7 @@ GEMM_API gemm_status_t gemm_sync_status(gemm_handle_t h, struct CUstream_st* str
   if (word != 0) {
     cudaMemsetAsync(h->d_status, 0, sizeof(uint32_t), s);
     cudaStreamSynchronize(s);
-    return GEMM_ERR_DEVICE_TIMEOUT;
+    return status_of_word(word);
   }
   return GEMM_OK;
 }
@@ -1065,9 +1136,9 @@ gemm_status_t noalloc_setup(gemm_handle& h, int device) {
     cudaGetLastError();
     return GEMM_ERR_CUDA;
   }
-  int clusters[5] = {0, 0, 0, 0, 0};
+  int clusters[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
   query_cluster_occupancy(device, sms, optin, clusters);
-  for (int i = 0; i < 5; ++i) h.clusters_by_size[i] = clusters[i];
+  for (int i = 0; i < 9; ++i) h.clusters_by_size[i] = clusters[i];
   h.device = device;
   h.sm_count = sms;
   h.smem_optin = optin;
@@ -1085,6 +1156,7 @@ GEMM_API gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int64_t
                                         float alpha, float beta, float x_factor,
                                         const gemm_dtypes_t* dtypes, struct CUstream_st* stream,
                                         uint32_t* watchdog_out) {
+  NvtxRange range("gemm_run_noalloc");
   if (watchdog_out) *watchdog_out = 0;
   // Scratch a call needs against what the array holds (a constant one word).
   if (kNoallocWordsPerCall > kNoallocScratchWords) return GEMM_ERR_INVALID_ARG;
@@ -1121,5 +1193,5 @@ GEMM_API gemm_status_t gemm_run_noalloc(int64_t M, int64_t N, int64_t K, int64_t
     return GEMM_ERR_CUDA;
   }
   *watchdog_out = word;
-  return word ? GEMM_ERR_DEVICE_TIMEOUT : GEMM_OK;
+  return status_of_word(word);
 }

@@ -40,13 +40,20 @@
 // global memory only after griddepcontrol.wait, so a launch with programmatic
 // stream serialization overlaps its prologue with the previous grid's tail.
 //
-// Clusters: CG*MC CTAs = MC CTA groups (pairs when CG = 2) stacked along M.  The
-// groups of a cluster compute MC vertically adjacent tiles that share the same B
-// columns, so each CTA loads only 1/MC of its B slice and TMA-multicasts it to
-// the matching CTA of every group (the multicast pattern of
-// "04_mma_tma_2sm_sm100.cu", "TMA Setup": B is multicast along cluster M).  A
-// ring slot may then be refilled only after every group's MMA has drained it,
-// so MMA completion is multicast to all CTAs of the cluster.
+// Clusters: CG*MC*NC CTAs = MC x NC CTA groups (pairs when CG = 2), MC stacked
+// along M and NC side by side along N.  Groups in one column of the cluster
+// compute vertically adjacent tiles with the same B columns, so each CTA
+// loads only 1/MC of its B slice and TMA-multicasts it to the matching CTA of
+// every group in that column; groups in one row share A rows the same way
+// (1/NC of the A slice each, multicast along the row).  This is the multicast
+// pattern of "04_mma_tma_2sm_sm100.cu", "TMA Setup": B multicast along cluster
+// M, A along cluster N.  A ring slot may then be refilled only after every
+// group's MMA has drained it, so MMA completion is multicast to all CTAs of
+// the cluster.  The multicast loads themselves live in ptx_multicast.cuh,
+// which only the units instantiating such clusters include.
+//
+// The tile width BN (a multiple of 32 up to 256) is a launch parameter; the
+// two accumulator stages sit 256 tensor-memory columns apart whatever BN is.
 //
 // Every barrier wait is bounded (watchdog): on expiry the kernel records a code
 // in a device status word, raises a CTA-wide abort flag, lets in-flight copies
@@ -79,7 +86,8 @@ struct EpiParams {
 
 struct KernelParams {
   int M, N, K, L;
-  int tiles_m, tiles_n;      // tiles per batch along M (of 128*cta_group*MC rows) and N
+  int bn;                    // tile width of one CTA group (multiple of 32, <= 256)
+  int tiles_m, tiles_n;      // cluster tiles per batch along M (128*CG*MC rows) and N (BN*NC)
   int num_tiles;             // tiles_m * tiles_n * L
   int k_blocks;              // ceil(K / tile_k)
   int group_m;               // rasterisation strip height (tiles)
@@ -132,33 +140,41 @@ constexpr int kThreads = 192;
 constexpr int kAccStages = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kEpiChunk = 32;          // columns per epilogue chunk
-constexpr int kEpiLeader = 64;         // thread that issues the epilogue's TMA stores
-constexpr int kEpiLoader = 96;         // thread that issues the epilogue's TMA loads
-constexpr uint32_t kEpiBarrier = 1;    // named barrier of the 128 epilogue threads
+constexpr int kEpiLeader = 64;         // epilogue thread that records the ring statistics
+constexpr int kSubRows = 32;           // rows of one epilogue warp's sub-tiles
 
-template <int CG, int BN, int AB_BYTES, int MC>
+constexpr uint32_t kAccStride = 256;   // tensor-memory columns between accumulator stages
+
+template <int CG, int AB_BYTES, int KA, int MC, int NC>
 struct Geometry {
-  static constexpr int KA = k_atoms(CG, BN);     // 128-byte K atoms per ring stage
   static constexpr int BM = 128;                 // A rows staged per CTA
   static constexpr int ATOM_K = 128 / AB_BYTES;  // K of one 128-byte swizzle row
-  static constexpr int BK = ATOM_K * KA;         // K per ring stage
-  static constexpr int BN_CTA = BN / CG;         // B rows staged per CTA
+  static constexpr int BK = ATOM_K * KA;         // K per ring stage (KA 128-byte K atoms)
   static constexpr int A_ATOM = BM * 128;        // bytes of one K-major A atom (128 rows)
-  static constexpr int B_ATOM = BN_CTA * 128;    // bytes of one K-major B atom
   static constexpr int A_STAGE = A_ATOM * KA;    // bytes
-  static constexpr int B_STAGE = B_ATOM * KA;    // bytes
   static constexpr int UMMA_K = 32 / AB_BYTES;   // K per tcgen05.mma (32 bytes: 8 tf32,
                                                  // 16 fp16/bf16, 32 fp8)
   static constexpr int K_STEPS = BK / UMMA_K;    // instructions per stage
   static constexpr int STEPS_PER_ATOM = ATOM_K / UMMA_K;   // 4
   static constexpr int ATOM_MN = 128 / AB_BYTES; // MN extent of one MN-major swizzle atom
   static constexpr int ATOM_BYTES = BK * 128;    // bytes of one MN-major atom column
-  static constexpr int CHUNKS = BN / kEpiChunk;  // epilogue chunks per tile
-  static constexpr int CLUSTER = CG * MC;        // CTAs per cluster
+  static constexpr int GROUPS = MC * NC;         // CTA groups per cluster
+  static constexpr int CLUSTER = CG * GROUPS;    // CTAs per cluster
   static constexpr int CM = BM * CG * MC;        // output rows per cluster tile
-  static constexpr int BN_PART = BN_CTA / MC;    // B rows each CTA loads (and multicasts)
-  static_assert(BN % kEpiChunk == 0 && BN <= 256, "tile_n");
-  static_assert(kAccStages * BN <= (int)kTmemCols, "accumulators must fit tensor memory");
+  static constexpr int A_PART = BM / NC;         // A rows each CTA loads (and multicasts)
+  static_assert(KA == 1 || KA == 2, "k atoms per stage");
+  static_assert(CLUSTER <= 8, "portable cluster size");
+  static_assert(kAccStages * kAccStride <= kTmemCols, "accumulators must fit tensor memory");
+};
+
+// The B-side sizes that follow from the runtime tile width.
+struct TileN {
+  int bn;        // output columns of one CTA group's tile
+  int bn_cta;    // B rows staged per CTA (bn / CG)
+  int bn_part;   // B rows each CTA loads (and multicasts): bn_cta / MC
+  int b_atom;    // bytes of one K-major B atom (bn_cta rows of 128 bytes)
+  int b_stage;   // bytes of B per ring stage
+  int chunks;    // 32-column epilogue chunks per whole tile
 };
 
 // Watchdog codes: 0xE0RRBBBB, RR = role, BBBB = low 16 bits of blockIdx.x.
@@ -172,6 +188,41 @@ struct Watch {
   uint32_t* status;
   unsigned long long timeout_ns;
 };
+
+// Debug build (GB300_DEBUG=1, a separate library): before use, every TMA
+// copy's shared-memory range and inner coordinate (16-byte aligned, stores not
+// below zero), every tensor-memory column range the MMA writes or the
+// epilogue reads, and every MMA operand address are checked.  A failed check
+// records 0xD0CCBBBB (CC the check, BBBB the low 16 bits of the block) in the
+// status word, raises the abort flag and skips the access, so the launch ends
+// through the watchdog's drain path; nothing traps.  The product build
+// compiles none of it.
+#ifndef GB300_DEBUG
+#define GB300_DEBUG 0
+#endif
+constexpr bool kDebug = GB300_DEBUG != 0;
+enum : uint32_t {
+  kChkLoadA = 1, kChkLoadB = 2, kChkMmaTmem = 3, kChkMmaSmem = 4, kChkEpiTmem = 5,
+  kChkEpiSmem = 6, kChkEpiLoad = 7, kChkEpiStore = 8
+};
+
+__device__ __forceinline__ bool dbg_check(bool cond, uint32_t check, const Watch& w) {
+  if constexpr (!kDebug) {
+    (void)cond; (void)check; (void)w;
+    return true;
+  } else {
+    if (cond) return true;
+    *w.abort = 1u;
+    atomicCAS(w.status, 0u, 0xD0000000u | (check << 16) | (blockIdx.x & 0xFFFFu));
+    return false;
+  }
+}
+
+// [lo, lo + bytes) lies inside [begin, end).
+__device__ __forceinline__ bool in_range(uint32_t lo, uint32_t bytes, uint32_t begin,
+                                         uint32_t end) {
+  return lo >= begin && lo + bytes <= end;
+}
 
 // Bounded wait for the phase with parity `parity`.  A non-zero `hint_ns` lets
 // the hardware suspend the thread up to that long per probe (for long waits
@@ -247,12 +298,13 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t w) {
   return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
-// Epilogue sub-tiles hold 128 rows x 32 columns of one tensor, as TMA lays them out:
+// Epilogue sub-tiles hold one warp's 32 rows x 32 columns of one tensor, as TMA
+// lays them out:
 //   row-major tensors: [row][32 columns], 128-byte rows (fp32, 128-byte swizzle:
 //     16-byte chunk j of row r sits at chunk j ^ (r & 7)) or 64-byte rows (16-bit,
 //     64-byte swizzle: chunk j ^ ((r >> 1) & 3));
-//   column-major tensors: [column][128 rows], unswizzled.
-// Thread r touches only row r; the swizzles make each 8-row group of a warp hit
+//   column-major tensors: [column][32 rows], unswizzled.
+// Lane r touches only row r; the swizzles make each 8-row group of a warp hit
 // distinct banks.  The type and layout branches are uniform and sit outside the
 // element loops, and 16-bit values convert two at a time.
 __device__ __forceinline__ void smem_read_row(const uint8_t* sub, int dt, int m_major, int r,
@@ -290,13 +342,13 @@ __device__ __forceinline__ void smem_read_row(const uint8_t* sub, int dt, int m_
     if (dt == DT_F32) {
 #pragma unroll
       for (int c = 0; c < kEpiChunk; ++c)
-        v[c] = *reinterpret_cast<const float*>(sub + (c * 128 + r) * 4);
+        v[c] = *reinterpret_cast<const float*>(sub + (c * kSubRows + r) * 4);
     } else {
       uint32_t w[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const uint32_t lo = *reinterpret_cast<const uint16_t*>(sub + (2 * i * 128 + r) * 2);
-        const uint32_t hi = *reinterpret_cast<const uint16_t*>(sub + ((2 * i + 1) * 128 + r) * 2);
+        const uint32_t lo = *reinterpret_cast<const uint16_t*>(sub + (2 * i * kSubRows + r) * 2);
+        const uint32_t hi = *reinterpret_cast<const uint16_t*>(sub + ((2 * i + 1) * kSubRows + r) * 2);
         w[i] = lo | (hi << 16);
       }
       if (dt == DT_BF16) {
@@ -326,7 +378,7 @@ __device__ __forceinline__ void smem_write_row(uint8_t* sub, int dt, int m_major
             make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
     } else {
 #pragma unroll
-      for (int c = 0; c < kEpiChunk; ++c) *reinterpret_cast<float*>(sub + (c * 128 + r) * 4) = v[c];
+      for (int c = 0; c < kEpiChunk; ++c) *reinterpret_cast<float*>(sub + (c * kSubRows + r) * 4) = v[c];
     }
     return;
   }
@@ -346,19 +398,20 @@ __device__ __forceinline__ void smem_write_row(uint8_t* sub, int dt, int m_major
   } else {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      *reinterpret_cast<uint16_t*>(sub + (2 * i * 128 + r) * 2) = (uint16_t)(w[i] & 0xFFFFu);
-      *reinterpret_cast<uint16_t*>(sub + ((2 * i + 1) * 128 + r) * 2) = (uint16_t)(w[i] >> 16);
+      *reinterpret_cast<uint16_t*>(sub + (2 * i * kSubRows + r) * 2) = (uint16_t)(w[i] & 0xFFFFu);
+      *reinterpret_cast<uint16_t*>(sub + ((2 * i + 1) * kSubRows + r) * 2) = (uint16_t)(w[i] >> 16);
     }
   }
 }
 
+// Bytes of one warp's sub-tile of a tensor of type dt.
 __device__ __forceinline__ uint32_t sub_bytes(int dt) {
-  return (uint32_t)(128 * kEpiChunk) * (dt == DT_F32 ? 4u : 2u);
+  return (uint32_t)(kSubRows * kEpiChunk) * (dt == DT_F32 ? 4u : 2u);
 }
 
 // ------------------------------------------------------------------ the kernel
 
-template <int CG, int BN, int AB_BYTES, int MC>
+template <int CG, int AB_BYTES, int KA, int MC, int NC>
 __global__ void __launch_bounds__(kThreads, 1)
 persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
@@ -367,9 +420,18 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmD,
                        const __grid_constant__ CUtensorMap tmY,
                        const __grid_constant__ KernelParams p) {
-  using G = Geometry<CG, BN, AB_BYTES, MC>;
+  using G = Geometry<CG, AB_BYTES, KA, MC, NC>;
   constexpr int KIND = (AB_BYTES == 1) ? 1 : (AB_BYTES == 4 ? 2 : 0);
   constexpr bool MULTI = G::CLUSTER > 1;
+  const int BN = p.bn;
+  TileN tn_geo;
+  tn_geo.bn = BN;
+  tn_geo.bn_cta = BN / CG;
+  tn_geo.bn_part = tn_geo.bn_cta / MC;
+  tn_geo.b_atom = tn_geo.bn_cta * 128;
+  tn_geo.b_stage = tn_geo.b_atom * KA;
+  tn_geo.chunks = BN / kEpiChunk;
+  const TileN& T = tn_geo;
 
   // The next GEMM of the stream may start its prologue on SMs this grid leaves
   // idle; it touches global memory only after its own dependency wait below.
@@ -386,14 +448,19 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   const int lane = threadIdx.x & 31;
   const uint32_t crank = MULTI ? cluster_ctarank() : 0u;
   const uint32_t rank = crank % CG;               // CTA within its pair
-  const uint32_t grp = crank / CG;                // pair (group) within the cluster
+  const uint32_t grp = crank / CG;                // group within the cluster: gn * MC + gm
+  const uint32_t gm = grp % MC;                   // the group's row in the cluster (along M)
+  const uint32_t gn = grp / MC;                   // ... and column (along N)
   const uint32_t pair_leader = grp * CG;          // cluster rank of the pair's leader
   const int cluster_id = blockIdx.x / G::CLUSTER;
   const int num_clusters = gridDim.x / G::CLUSTER;
-  // CTAs receiving this CTA's B part: the same peer position in every group.
-  uint16_t b_mask = 0;
+  // CTAs receiving this CTA's B part: the same peer position in every group of
+  // its cluster column; its A part: the same position in every group of its row.
+  uint16_t b_mask = 0, a_mask = 0;
 #pragma unroll
-  for (int g = 0; g < MC; ++g) b_mask |= (uint16_t)(1u << (g * CG + rank));
+  for (int g = 0; g < MC; ++g) b_mask |= (uint16_t)(1u << ((gn * MC + g) * CG + rank));
+#pragma unroll
+  for (int g = 0; g < NC; ++g) a_mask |= (uint16_t)(1u << ((g * MC + gm) * CG + rank));
   const uint16_t all_mask = (uint16_t)((1u << G::CLUSTER) - 1u);
   const uint16_t pair_mask = (uint16_t)(((1u << CG) - 1u) << pair_leader);
   const int S = p.stages;
@@ -402,31 +469,35 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   const uint32_t slot_bytes = e.cd_bytes + e.xy_bytes;
 
   // [B ring][A ring][epilogue slots][full x S][empty x S][tfull x 2][tempty x 2]
-  // [cfull x E][tmem address][abort flag][never]  ("never": a barrier nothing
+  // [cfull x 4E (per epilogue warp and slot)][tmem address][abort flag][never]
+  // [rfull x 4 (per epilogue warp)]  ("never": a barrier nothing
   // arrives at, waited on only when a stall is injected to test the watchdog)
   const uint32_t b_ring = base;
-  const uint32_t a_ring = b_ring + S * G::B_STAGE;
+  const uint32_t a_ring = b_ring + S * T.b_stage;
   const uint32_t epi0 = a_ring + S * G::A_STAGE;
   const uint32_t bars = epi0 + E * slot_bytes;
   const uint32_t full0 = bars, empty0 = bars + 8u * S;
   const uint32_t tfull0 = bars + 16u * S, tempty0 = tfull0 + 16u;
   const uint32_t cfull0 = tempty0 + 16u;
-  const uint32_t holder = cfull0 + 8u * E;
+  const uint32_t holder = cfull0 + 8u * 4u * E;     // a cfull barrier per warp and slot
   volatile uint32_t* const holder_ptr = reinterpret_cast<volatile uint32_t*>(gbase + (holder - base));
   volatile uint32_t* const abort_ptr = holder_ptr + 1;
   const uint32_t never_bar = holder + 8u;
+  const uint32_t rfull0 = never_bar + 8u;           // a ring-batch barrier per epilogue warp
+  const uint32_t ring_bytes = (uint32_t)S * ((uint32_t)G::A_STAGE + (uint32_t)T.b_stage);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8u * s, 1);
-      mbar_init(empty0 + 8u * s, MC);          // one MMA commit per group
+      mbar_init(empty0 + 8u * s, G::GROUPS);   // one MMA commit per group
     }
     for (int a = 0; a < kAccStages; ++a) {
       mbar_init(tfull0 + 8u * a, 1);
       mbar_init(tempty0 + 8u * a, 4 * CG);   // every epilogue warp of the CTA (pair)
     }
-    for (int s = 0; s < E; ++s) mbar_init(cfull0 + 8u * s, 1);
+    for (int s = 0; s < 4 * E; ++s) mbar_init(cfull0 + 8u * s, 1);
     mbar_init(never_bar, 1);
+    for (int q = 0; q < 4; ++q) mbar_init(rfull0 + 8u * q, 1);
     *abort_ptr = 0u;
     fence_barrier_init();
     if (p.k_blocks > 0) {                    // A and B are encoded only when K > 0
@@ -458,7 +529,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     // ---------------------------------------------------------- TMA producer
     if (lane == 0) {
       const uint64_t pol = make_l2_policy(p.l2_hints & 3u);
-      const uint32_t tx_bytes = (uint32_t)(CG * (G::A_STAGE + G::B_STAGE));
+      const uint32_t tx_bytes = (uint32_t)(CG * (G::A_STAGE + T.b_stage));
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
@@ -471,11 +542,12 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         tile_coords(t, p, tm, tn, tl);
         // A half-width item covers columns [half * BN/2, +BN/2) of its tile: its
         // CTAs load full B boxes from that origin and the MMA reads their first
-        // half.
+        // half.  m0: this CTA's 128 A rows; n0: the first of its B rows, plus
+        // the offset of the part it loads for its cluster column.
         const int item_n = half < 0 ? BN : BN / 2;
-        const int m0 = tm * G::CM + (int)grp * (G::BM * CG) + (int)rank * G::BM;
-        const int n0 = tn * BN + (half > 0 ? BN / 2 : 0) + (int)rank * (item_n / CG) +
-                       (int)grp * (item_n / CG / MC);
+        const int m0 = tm * G::CM + (int)gm * (G::BM * CG) + (int)rank * G::BM;
+        const int n0 = tn * (BN * NC) + (int)gn * BN + (half > 0 ? BN / 2 : 0) +
+                       (int)rank * (item_n / CG) + (int)gm * (item_n / CG / MC);
         // Alternate waves walk K in opposite directions, so the k-blocks one
         // wave reads last are the first the next wave reads, while they are
         // still in L2.  The MMA side only counts stages, so the order is the
@@ -490,36 +562,49 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           const uint32_t fb_target = (CG == 2) ? map_to_rank(fb, pair_leader) : fb;
           const int k0 = (k_down ? p.k_blocks - 1 - kb : kb) * G::BK;
           const uint32_t sa = a_ring + s * G::A_STAGE;
-          const uint32_t sb = b_ring + s * G::B_STAGE;
-          auto issue = [&](const CUtensorMap* map, uint32_t dst, int c0, int c1) {
-            if constexpr (CG == 1) tma_load_3d(dst, map, fb_target, c0, c1, tl, pol);
-            else tma_load_3d_pair(dst, map, fb_target, c0, c1, tl, pol);
+          const uint32_t sb = b_ring + s * T.b_stage;
+          // (debug build: the box's bytes inside this stage, the inner
+          // coordinate a whole 16 bytes)
+          auto issue_a = [&](uint32_t dst, int c0, int c1, uint32_t bytes) {
+            if (!dbg_check(in_range(dst, bytes, sa, sa + G::A_STAGE) &&
+                               ((long long)c0 * AB_BYTES) % 16 == 0 && c1 >= 0,
+                           kChkLoadA, w)) { ok = false; return; }
+            OperandLoad<CG, (NC > 1)>::load(dst, &tmA, fb_target, c0, c1, tl, a_mask, pol);
           };
-          auto issue_b = [&](uint32_t dst, int c0, int c1) {
-            if constexpr (MC == 1) issue(&tmB, dst, c0, c1);
-            else if constexpr (CG == 1)
-              tma_load_3d_mc(dst, &tmB, fb_target, c0, c1, tl, b_mask, pol);
-            else tma_load_3d_pair_mc(dst, &tmB, fb_target, c0, c1, tl, b_mask, pol);
+          auto issue_b = [&](uint32_t dst, int c0, int c1, uint32_t bytes) {
+            if (!dbg_check(in_range(dst, bytes, sb, sb + (uint32_t)T.b_stage) &&
+                               ((long long)c0 * AB_BYTES) % 16 == 0 && c1 >= 0,
+                           kChkLoadB, w)) { ok = false; return; }
+            OperandLoad<CG, (MC > 1)>::load(dst, &tmB, fb_target, c0, c1, tl, b_mask, pol);
           };
           if (!p.a_mn_major) {
+            // boxes {ATOM_K, A_PART}: this CTA's part of its cluster row's A rows
 #pragma unroll
-            for (int a = 0; a < G::KA; ++a)                    // boxes {ATOM_K, 128}
-              issue(&tmA, sa + a * G::A_ATOM, k0 + a * G::ATOM_K, m0);
+            for (int a = 0; a < KA; ++a)
+              issue_a(sa + a * G::A_ATOM + gn * G::A_PART * 128, k0 + a * G::ATOM_K,
+                      m0 + (int)gn * G::A_PART, G::A_PART * 128);
           } else {
+            // boxes {ATOM_MN, BK}: this CTA's share of the A rows' MN atoms
+            constexpr int PER = G::BM / G::ATOM_MN / NC;
 #pragma unroll
-            for (int j = 0; j < G::BM / G::ATOM_MN; ++j)       // boxes {ATOM_MN, BK}
-              issue(&tmA, sa + j * G::ATOM_BYTES, m0 + j * G::ATOM_MN, k0);
+            for (int j = 0; j < PER; ++j) {
+              const int aj = (int)gn * PER + j;
+              issue_a(sa + aj * G::ATOM_BYTES, m0 + aj * G::ATOM_MN, k0, G::ATOM_BYTES);
+            }
           }
           if (!p.b_mn_major) {
+            // boxes {ATOM_K, bn_part}
 #pragma unroll
-            for (int a = 0; a < G::KA; ++a)                    // boxes {ATOM_K, BN_PART}
-              issue_b(sb + a * G::B_ATOM + grp * G::BN_PART * 128, k0 + a * G::ATOM_K, n0);
+            for (int a = 0; a < KA; ++a)
+              issue_b(sb + a * T.b_atom + gm * T.bn_part * 128, k0 + a * G::ATOM_K, n0,
+                      (uint32_t)T.bn_part * 128u);
           } else {
-            constexpr int ATOMS = G::BN_PART / G::ATOM_MN;     // boxes {ATOM_MN, BK}
-#pragma unroll
-            for (int j = 0; j < ATOMS; ++j)
-              issue_b(sb + (grp * ATOMS + j) * G::ATOM_BYTES, n0 + j * G::ATOM_MN, k0);
+            const int atoms = T.bn_part / G::ATOM_MN;          // boxes {ATOM_MN, BK}
+            for (int j = 0; j < atoms; ++j)
+              issue_b(sb + ((int)gm * atoms + j) * G::ATOM_BYTES, n0 + j * G::ATOM_MN, k0,
+                      G::ATOM_BYTES);
           }
+          if (kDebug && !ok) break;
           if (++s == S) { s = 0; ph ^= 1u; }
         }
       }
@@ -543,15 +628,20 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         if (!wait_phase(tempty0 + 8u * acc, aph ^ 1u, w, kWaitMmaAcc)) break;
         if constexpr (kRingStats) st_acc += clock64() - t_a;
         tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        const uint32_t d_tmem = tmem_base + (uint32_t)acc * kAccStride;
         const uint32_t idesc = it < p.split_start ? p.idesc : p.idesc_half;
+        // (debug build: the item's accumulator columns inside its stage)
+        if (!dbg_check((uint32_t)(it < p.split_start ? BN : BN / 2) <= kAccStride &&
+                           (uint32_t)acc * kAccStride + kAccStride <= kTmemCols,
+                       kChkMmaTmem, w))
+          break;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           const long long t_f = stat_clock();
           if (!wait_phase(full0 + 8u * s, ph, w, kWaitMmaFull)) { ok = false; break; }
           if constexpr (kRingStats) { st_full += clock64() - t_f; ++st_stages; }
           tc_fence_after_sync();
           const uint32_t sa = a_ring + s * G::A_STAGE;
-          const uint32_t sb = b_ring + s * G::B_STAGE;
+          const uint32_t sb = b_ring + s * T.b_stage;
 #pragma unroll
           for (int k = 0; k < G::K_STEPS; ++k) {
             // K-major: atoms of rows x 128 bytes, 8-row groups 1024 bytes
@@ -565,9 +655,21 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                 : smem_desc_sw128(sa + ka * G::A_ATOM + kk * 32, 16, 1024);
             const uint64_t bd = p.b_mn_major
                 ? smem_desc_sw128(sb + k * G::UMMA_K * 128, G::ATOM_BYTES, 1024)
-                : smem_desc_sw128(sb + ka * G::B_ATOM + kk * 32, 16, 1024);
+                : smem_desc_sw128(sb + ka * T.b_atom + kk * 32, 16, 1024);
+            // (debug build: both operands' start addresses inside the stage)
+            if (kDebug && !dbg_check(
+                    in_range(p.a_mn_major ? sa + k * G::UMMA_K * 128 : sa + ka * G::A_ATOM + kk * 32,
+                             32, sa, sa + G::A_STAGE) &&
+                        in_range(p.b_mn_major ? sb + k * G::UMMA_K * 128
+                                              : sb + ka * T.b_atom + kk * 32,
+                                 32, sb, sb + (uint32_t)T.b_stage),
+                    kChkMmaSmem, w)) {
+              ok = false;
+              break;
+            }
             umma<CG, KIND>(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
           }
+          if (kDebug && !ok) break;
           umma_commit<CG, MULTI>(empty0 + 8u * s, all_mask);   // slot drained: tell every loader
           if (++s == S) { s = 0; ph ^= 1u; }
         }
@@ -592,21 +694,30 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     __syncwarp();
   } else {
     // ---------------------------------------------------------- epilogue
+    // Each epilogue warp runs its own pipeline over the 32 tile rows whose
+    // accumulator lanes it may read, through its own ring of `slots`
+    // shared-memory sub-slots (32 rows x 32 columns of C/D and of X/Y): lane 0
+    // TMA-loads the C/X sub-tiles E - 1 chunks ahead (across tile
+    // boundaries), every lane reads its row, computes D and Y and writes them
+    // back in place, and lane 0 TMA-stores them.  The four warps never wait on
+    // one another; they meet only in the accumulator stage's release count.
     const int q = warp & 3;                 // TMEM lane quarter this warp may read
-    const int r = q * 32 + lane;            // this thread's row within the CTA's 128
-    const bool epi_leader = threadIdx.x == kEpiLeader;
-    const bool epi_loader = threadIdx.x == kEpiLoader;
+    const bool lead = lane == 0;
     const bool loads = e.read_c || e.read_x;
     const uint32_t load_tx = (e.read_c ? sub_bytes(e.c_dt) : 0u) + (e.read_x ? sub_bytes(e.x_dt) : 0u);
+    const uint32_t sub = slot_bytes / 4;               // one warp's share of a slot
+    const uint32_t cd_sub = e.cd_bytes / 4;            // ... of which C/D
+    const uint32_t ring0 = epi0 + (uint32_t)(q * E) * sub;
+    const uint32_t bar0 = cfull0 + 8u * (uint32_t)(q * E);
     const uint64_t pol_in = make_l2_policy((p.l2_hints >> 2) & 3u);
     const uint64_t pol_out = make_l2_policy((p.l2_hints >> 4) & 3u);
 
-    // The epilogue loader walks this CTA's stream of chunks (CHUNKS per whole
-    // tile, CHUNKS / 2 per half-width item, in item order) with a cursor that
-    // issues the TMA loads of C/X into the slots, E - 1 chunks ahead of the
-    // chunk being processed.  The cursor computes an item's coordinates once,
-    // when it enters the item.  TMA coordinates are (column, row, batch) for
-    // row-major C/D/X/Y and (row, column, batch) for column-major ones.
+    // Lane 0 walks this CTA's stream of chunks (BN / 32 per whole tile, half
+    // that per half-width item, in item order) with a cursor that issues the
+    // TMA loads of its rows' C/X into the warp's sub-slots.  The cursor
+    // computes an item's coordinates once, when it enters the item.  TMA
+    // coordinates are (column, row, batch) for row-major C/D/X/Y and (row,
+    // column, batch) for column-major ones.
     struct Cursor { int it, j, nch, row0, col0, tl; };
     auto cursor_enter = [&](Cursor& cc) {
       if (cc.it >= p.num_items) return;
@@ -614,9 +725,9 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       const int t = item_tile(cc.it, p, half);
       int tm, tn;
       tile_coords(t, p, tm, tn, cc.tl);
-      cc.nch = half < 0 ? G::CHUNKS : G::CHUNKS / 2;
-      cc.row0 = tm * G::CM + (int)grp * (G::BM * CG) + (int)rank * G::BM;
-      cc.col0 = tn * BN + (half > 0 ? BN / 2 : 0);
+      cc.nch = half < 0 ? T.chunks : T.chunks / 2;
+      cc.row0 = tm * G::CM + (int)gm * (G::BM * CG) + (int)rank * G::BM + q * kSubRows;
+      cc.col0 = tn * (BN * NC) + (int)gn * BN + (half > 0 ? BN / 2 : 0);
     };
     auto cursor_next = [&](Cursor& cc) {
       if (cc.it < p.num_items && ++cc.j == cc.nch) {
@@ -630,26 +741,40 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       x0 = e.cd_m_major ? cc.row0 : col;
       x1 = e.cd_m_major ? col : cc.row0;
     };
+    // (debug build: a C/X load's sub-slot inside the slots or the drained
+    // ring, its inner coordinate a whole 16 bytes of both types)
+    const uint32_t slots_end = epi0 + (uint32_t)E * slot_bytes;
+    auto inner_ok = [&](int x, int dt) { return ((long long)x * (dt == DT_F32 ? 4 : 2)) % 16 == 0; };
+    auto load_ok = [&](uint32_t dst, int x0) {
+      const bool in_slots = in_range(dst, sub, ring0, ring0 + (uint32_t)E * sub) &&
+                            dst + sub <= slots_end;
+      const bool in_ring = in_range(dst, sub, b_ring, b_ring + ring_bytes);
+      return (in_slots || in_ring) && (!e.read_c || inner_ok(x0, e.c_dt)) &&
+             (!e.read_x || inner_ok(x0, e.x_dt));
+    };
     Cursor ld{cluster_id, 0, 0, 0, 0, 0};
     int ld_slot = 0;
-    auto issue_loads = [&]() {              // epilogue loader only
+    auto issue_loads = [&]() {              // lane 0 only
       if (ld.it < p.num_items) {
         int x0, x1;
         cursor_xy(ld, x0, x1);
-        const uint32_t slot = epi0 + (uint32_t)ld_slot * slot_bytes;
-        const uint32_t bar = cfull0 + 8u * (uint32_t)ld_slot;
-        mbar_arrive_expect_tx(bar, load_tx);
-        if (e.read_c) tma_load_3d(slot, &tmC, bar, x0, x1, ld.tl, pol_in);
-        if (e.read_x) tma_load_3d(slot + e.cd_bytes, &tmX, bar, x0, x1, ld.tl, pol_in);
+        const uint32_t slot = ring0 + (uint32_t)ld_slot * sub;
+        const uint32_t bar = bar0 + 8u * (uint32_t)ld_slot;
+        if (dbg_check(load_ok(slot, x0), kChkEpiLoad, w)) {
+          mbar_arrive_expect_tx(bar, load_tx);
+          if (e.read_c) tma_load_3d(slot, &tmC, bar, x0, x1, ld.tl, pol_in);
+          if (e.read_x) tma_load_3d(slot + cd_sub, &tmX, bar, x0, x1, ld.tl, pol_in);
+        }
       }
       if (++ld_slot == E) ld_slot = 0;
       cursor_next(ld);
     };
 
-    if (epi_loader && loads) {
+    if (lead && loads) {
       cursor_enter(ld);
       for (int c = 0; c < E - 1; ++c) issue_loads();
     }
+    __syncwarp();
 
     int acc = 0;
     uint32_t aph = 0;
@@ -664,36 +789,75 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       const int t = item_tile(it, p, half);
       int tm, tn, tl;
       tile_coords(t, p, tm, tn, tl);
-      const int nchunks = half < 0 ? G::CHUNKS : G::CHUNKS / 2;
-      const int ncol0 = tn * BN + (half > 0 ? BN / 2 : 0);
+      const int nchunks = half < 0 ? T.chunks : T.chunks / 2;
+      const int ncol0 = tn * (BN * NC) + (int)gn * BN + (half > 0 ? BN / 2 : 0);
       const long long t_t = stat_clock();
       const bool ready = wait_phase(tfull0 + 8u * acc, aph, w, kWaitEpilogue, p.epi_wait_ns);
       if constexpr (kRingStats) st_tfull += clock64() - t_t;
-      __syncwarp();
-      ok = named_barrier_and(kEpiBarrier, 128, ready);
+      ok = __all_sync(0xFFFFFFFFu, ready);
       if (!ok) break;
       tc_fence_after_sync();
-      const int row0 = tm * G::CM + (int)grp * (G::BM * CG) + (int)rank * G::BM;
-      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      // This CTA's last item: once its accumulator is ready the operand ring
+      // has been drained for good (no main loop follows), so the C/X chunks
+      // the lookahead has not loaded yet all go into the ring at once, and
+      // the rest of the epilogue waits on one load latency, not one per
+      // chunk.  batch0: first chunk of the item taken from the ring (nchunks:
+      // none).
+      // Only lane 0 keeps the cursor; it decides and tells the warp.
+      int batch0 = nchunks;
+      if (loads && it + num_clusters >= p.num_items) {
+        if (lead && ld.it == it && (uint32_t)(nchunks - ld.j) * 4u * sub <= ring_bytes) {
+          batch0 = ld.j;
+          mbar_arrive_expect_tx(rfull0 + 8u * q, (uint32_t)(nchunks - batch0) * load_tx);
+          for (int c = 0; c < nchunks - batch0; ++c) {
+            int x0, x1;
+            cursor_xy(ld, x0, x1);
+            const uint32_t dst = b_ring + (uint32_t)(c * 4 + q) * sub;
+            if (!dbg_check(load_ok(dst, x0), kChkEpiLoad, w)) break;
+            if (e.read_c) tma_load_3d(dst, &tmC, rfull0 + 8u * q, x0, x1, ld.tl, pol_in);
+            if (e.read_x) tma_load_3d(dst + cd_sub, &tmX, rfull0 + 8u * q, x0, x1, ld.tl, pol_in);
+            cursor_next(ld);
+          }
+          ld.it = p.num_items;               // the cursor has nothing left to load
+        }
+        batch0 = __shfl_sync(0xFFFFFFFFu, batch0, 0);
+      }
+      const int row0 = tm * G::CM + (int)gm * (G::BM * CG) + (int)rank * G::BM + q * kSubRows;
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * kAccStride;
 #pragma unroll 1
       for (int j = 0; j < nchunks; ++j, ++gc) {
         // The accumulator columns are requested first: their latency overlaps
         // the wait for C/X and the shared-memory reads below.
         uint32_t raw_acc[32];
-        tmem_load_32cols(tbase + 32u * j, raw_acc);
-        uint8_t* const slot = gbase + (epi0 - base) + (uint32_t)slot_idx * slot_bytes;
+        // (debug build: the chunk's 32 columns inside the item's accumulator)
+        if (dbg_check(32 * (j + 1) <= (half < 0 ? BN : BN / 2) &&
+                          (uint32_t)acc * kAccStride + 32u * (j + 1) <= kTmemCols,
+                      kChkEpiTmem, w))
+          tmem_load_32cols(tbase + 32u * j, raw_acc);
+        else
+          for (int i = 0; i < 32; ++i) raw_acc[i] = 0u;
+        const bool from_ring = j >= batch0;
+        const uint32_t s_addr = from_ring ? b_ring + (uint32_t)((j - batch0) * 4 + q) * sub
+                                          : ring0 + (uint32_t)slot_idx * sub;
+        uint8_t* const slot = gbase + (s_addr - base);
         float cv[kEpiChunk], xv[kEpiChunk];
-        bool got = true;
+        bool got = dbg_check(from_ring ? in_range(s_addr, sub, b_ring, b_ring + ring_bytes)
+                                       : in_range(s_addr, sub, ring0, ring0 + (uint32_t)E * sub) &&
+                                             s_addr + sub <= slots_end,
+                             kChkEpiSmem, w);
         const long long t_c = stat_clock();
-        if (loads) got = wait_phase<true>(cfull0 + 8u * slot_idx, slot_ph, w, kWaitEpiLoad);
+        if (loads && got)
+          got = from_ring ? wait_phase<true>(rfull0 + 8u * q, 0u, w, kWaitEpiLoad)
+                          : wait_phase<true>(bar0 + 8u * slot_idx, slot_ph, w, kWaitEpiLoad);
         if constexpr (kRingStats) st_cfull += clock64() - t_c;
+        got = __all_sync(0xFFFFFFFFu, got);
         if (got && e.read_c) {
-          smem_read_row(slot, e.c_dt, e.cd_m_major, r, cv);
+          smem_read_row(slot, e.c_dt, e.cd_m_major, lane, cv);
         } else {
 #pragma unroll
           for (int i = 0; i < kEpiChunk; ++i) cv[i] = 0.f;
         }
-        if (got && e.read_x) smem_read_row(slot + e.cd_bytes, e.x_dt, e.cd_m_major, r, xv);
+        if (got && e.read_x) smem_read_row(slot + cd_sub, e.x_dt, e.cd_m_major, lane, xv);
         __syncwarp();                       // the .aligned wait needs the whole warp
         tmem_wait_ld(raw_acc);
         // Normalise the accumulator to fp32 bit patterns once per chunk (uniform
@@ -710,17 +874,19 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           // The whole accumulator stage has been read: hand it back to the MMA warp.
           tc_fence_before_sync();
           __syncwarp();
-          if (lane == 0) {
+          if (lead) {
             if constexpr (CG == 1) mbar_arrive(tempty0 + 8u * acc);
             else mbar_arrive_cluster(map_to_rank(tempty0 + 8u * acc, pair_leader));
           }
-          __syncwarp();
         }
-        // Every thread has read the slot (and agrees whether to go on) before any
-        // thread overwrites it with D and Y.
-        __syncwarp();
-        ok = named_barrier_and(kEpiBarrier, 128, got);
+        ok = got;
         if (!ok) break;
+        // No store still reads the sub-slot D and Y go into (with C/X loads,
+        // the load that filled it was issued after that), and every lane has
+        // read its C/X row before any lane overwrites the sub-slot (a narrower
+        // D packs rows differently from a wider C).
+        if (lead && !loads) bulk_wait_group_read<1>();
+        __syncwarp();
         // D from the accumulator, C (zero when not read) and X; the branches
         // are uniform and outside the element loops.
         float dv[kEpiChunk];
@@ -746,37 +912,42 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
               dv[i] = fmaf(al, __uint_as_float(raw_acc[i]), be * cv[i]);
           }
         }
-        smem_write_row(slot, e.d_dt, e.cd_m_major, r, dv);
+        smem_write_row(slot, e.d_dt, e.cd_m_major, lane, dv);
         if (e.write_y) {
           float yv[kEpiChunk];
 #pragma unroll
           for (int i = 0; i < kEpiChunk; ++i) yv[i] = __uint_as_float(raw_acc[i]);
-          smem_write_row(slot + e.cd_bytes, e.y_dt, e.cd_m_major, r, yv);
+          smem_write_row(slot + cd_sub, e.y_dt, e.cd_m_major, lane, yv);
         }
         fence_proxy_async_smem();
-        // The store of chunk gc-1 has finished reading its slot -- the slot that
-        // chunk gc+E-1 is loaded into, and that chunk gc+1 writes into -- before
-        // anyone passes the barrier below.
-        if (epi_leader) bulk_wait_group_read<0>();
-        named_barrier_sync(kEpiBarrier, 128);
-        if (epi_leader) {
+        __syncwarp();
+        if (lead) {
           const int col0 = ncol0 + j * kEpiChunk;
           const int x0 = e.cd_m_major ? row0 : col0, x1 = e.cd_m_major ? col0 : row0;
-          const uint32_t s_addr = epi0 + (uint32_t)slot_idx * slot_bytes;
-          tma_store_3d(&tmD, s_addr, x0, x1, tl, pol_out);
-          if (e.write_y) tma_store_3d(&tmY, s_addr + e.cd_bytes, x0, x1, tl, pol_out);
+          // (debug build: a store starts at non-negative coordinates, its inner
+          // one a whole 16 bytes of both output types)
+          if (dbg_check(x0 >= 0 && x1 >= 0 && inner_ok(x0, e.d_dt) &&
+                            (!e.write_y || inner_ok(x0, e.y_dt)),
+                        kChkEpiStore, w)) {
+            tma_store_3d(&tmD, s_addr, x0, x1, tl, pol_out);
+            if (e.write_y) tma_store_3d(&tmY, s_addr + cd_sub, x0, x1, tl, pol_out);
+          }
           bulk_commit_group();
-        } else if (epi_loader && loads) {
-          issue_loads();                    // meanwhile, in another warp: C/X of chunk gc+E-1
+          if (loads) {
+            // C/X of chunk gc+E-1 go into the sub-slot of chunk gc-1, once its
+            // store (the one before the store just issued) has read it.
+            bulk_wait_group_read<1>();
+            issue_loads();
+          }
         }
         if (++slot_idx == E) { slot_idx = 0; slot_ph ^= 1u; }
-        __syncwarp();                       // the issuing threads' warps reconverge
+        __syncwarp();
       }
       if (++acc == kAccStages) { acc = 0; aph ^= 1u; }
     }
-    if (epi_leader) bulk_wait_group_all();
+    if (lead) bulk_wait_group_all();
     if constexpr (kRingStats) {
-      if (epi_leader && p.stats) {
+      if (threadIdx.x == kEpiLeader && p.stats) {
         unsigned long long* const o = p.stats + (size_t)blockIdx.x * kStatWords;
         o[kStatEpiTfull] = st_tfull;
         o[kStatEpiCfull] = st_cfull;

@@ -3,30 +3,61 @@
 
 namespace gb300 {
 
-// Kernel entry for 16-bit (ab_bytes = 2), 8-bit (ab_bytes = 1) or tf32
-// (ab_bytes = 4) inputs, CTA
-// group 1 or 2, tile width 128 or 256, and mc CTA groups per cluster sharing B
-// through TMA multicast (1 or 2); nullptr if that variant is not built.
-const void* kernel_ab16_mc1(int cta_group, int tile_n);
-const void* kernel_ab16_mc2(int cta_group, int tile_n);
-const void* kernel_ab8_mc1(int cta_group, int tile_n);
-const void* kernel_ab8_mc2(int cta_group, int tile_n);
-const void* kernel_ab32_mc1(int cta_group, int tile_n);
-const void* kernel_ab32_mc2(int cta_group, int tile_n);
+// A variant is fixed by the input width (ab_bytes: 2 for fp16/bf16, 1 for fp8,
+// 4 for tf32), the CTA group (cta_group 1: single CTAs, 2: CTA pairs), the
+// 128-byte K atoms per ring stage (ka: 1 or 2) and the cluster's CTA groups
+// along M (mc, sharing B) and along N (nc, sharing A), each 1 or 2.  The tile
+// width is a launch parameter.
+//
+// kern_plain.cu, compiled once per input width, holds the clusters of one CTA
+// group; kern_shared.cu, compiled once per input width and (mc, nc), holds
+// the operand-sharing clusters, whose TMA loads multicast.  Only the
+// single-GPU library links the latter (GB300_MULTICAST = 1).
+#define GB300_PLAIN_ENTRIES(X) X(2) X(1) X(4)
+#define GB300_SHARED_ENTRIES(X) \
+  X(2, 2, 1) X(2, 1, 2) X(2, 2, 2) X(1, 2, 1) X(1, 1, 2) X(1, 2, 2) X(4, 2, 1) X(4, 1, 2) X(4, 2, 2)
 
-// 128-byte swizzle atoms along K per ring stage.  Two atoms (8 MMAs per
-// barrier round trip) keep the tensor pipe fed far better than one; the only
-// variant kept at one is the single-CTA 128x256 tile, whose 96 KB two-atom
-// stage would leave room for just two stages.
-constexpr int k_atoms(int cta_group, int tile_n) { return (cta_group == 1 && tile_n == 256) ? 1 : 2; }
+// (two levels, so that macro arguments are expanded before they are pasted)
+#define GB300_PLAIN_NAME_(ab) kernel_plain_ab##ab
+#define GB300_PLAIN_NAME(ab) GB300_PLAIN_NAME_(ab)
+#define GB300_SHARED_NAME_(ab, mc, nc) kernel_shared_ab##ab##_m##mc##_n##nc
+#define GB300_SHARED_NAME(ab, mc, nc) GB300_SHARED_NAME_(ab, mc, nc)
 
-inline const void* kernel_for(int ab_bytes, int cta_group, int tile_n, int mc) {
-  if (ab_bytes == 2) return mc == 1 ? kernel_ab16_mc1(cta_group, tile_n)
-                                    : mc == 2 ? kernel_ab16_mc2(cta_group, tile_n) : nullptr;
-  if (ab_bytes == 1) return mc == 1 ? kernel_ab8_mc1(cta_group, tile_n)
-                                    : mc == 2 ? kernel_ab8_mc2(cta_group, tile_n) : nullptr;
-  if (ab_bytes == 4) return mc == 1 ? kernel_ab32_mc1(cta_group, tile_n)
-                                    : mc == 2 ? kernel_ab32_mc2(cta_group, tile_n) : nullptr;
+#define GB300_DECLARE_PLAIN(ab) const void* GB300_PLAIN_NAME(ab)(int cta_group, int ka);
+#define GB300_DECLARE_SHARED(ab, mc, nc) \
+  const void* GB300_SHARED_NAME(ab, mc, nc)(int cta_group, int ka);
+GB300_PLAIN_ENTRIES(GB300_DECLARE_PLAIN)
+GB300_SHARED_ENTRIES(GB300_DECLARE_SHARED)
+#undef GB300_DECLARE_PLAIN
+#undef GB300_DECLARE_SHARED
+
+#ifndef GB300_MULTICAST
+#define GB300_MULTICAST 0
+#endif
+
+// 128-byte swizzle atoms along K per ring stage the planner gives a single CTA
+// of width tile_n: two atoms (8 MMAs per barrier round trip) keep the tensor
+// pipe fed far better than one, unless a two-atom stage is so large that
+// fewer than three stages fit (128 x 160 and wider single-CTA tiles).
+// CTA pairs always take two.
+constexpr int k_atoms(int cta_group, int tile_n) {
+  return (cta_group == 1 && tile_n > 128) ? 1 : 2;
+}
+
+inline const void* kernel_for(int ab_bytes, int cta_group, int ka, int mc, int nc) {
+  if (mc == 1 && nc == 1) {
+#define GB300_PICK_PLAIN(ab) \
+  if (ab_bytes == ab) return GB300_PLAIN_NAME(ab)(cta_group, ka);
+    GB300_PLAIN_ENTRIES(GB300_PICK_PLAIN)
+#undef GB300_PICK_PLAIN
+    return nullptr;
+  }
+#if GB300_MULTICAST
+#define GB300_PICK_SHARED(ab, m, n) \
+  if (ab_bytes == ab && mc == m && nc == n) return GB300_SHARED_NAME(ab, m, n)(cta_group, ka);
+  GB300_SHARED_ENTRIES(GB300_PICK_SHARED)
+#undef GB300_PICK_SHARED
+#endif
   return nullptr;
 }
 

@@ -168,31 +168,23 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
-// Multicast variants: the box lands at the same shared-memory offset in every
-// CTA of `cta_mask`, and each destination's barrier at the offset of `bar`
-// receives the completion.  With cta_group::2 the completion goes to the
-// barrier in the even (leader) CTA of each destination's pair.
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                               int32_t c0, int32_t c1, int32_t c2,
-                                               uint16_t cta_mask, uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster.L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6, %7;"
-      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2),
-         "h"(cta_mask), "l"(pol)
-      : "memory");
-}
+// TMA load of one operand box for a CTA group of CG CTAs.  kShared = false:
+// into this CTA only (cta_mask unused).  The shared form (kShared = true, one
+// box written into every CTA of cta_mask) is defined in ptx_multicast.cuh,
+// which only the kernel units of operand-sharing clusters include.
+template <int CG, bool kShared>
+struct OperandLoad;
 
-__device__ __forceinline__ void tma_load_3d_pair_mc(uint32_t dst, const CUtensorMap* map,
-                                                    uint32_t cluster_bar, int32_t c0, int32_t c1,
-                                                    int32_t c2, uint16_t cta_mask, uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster.cta_group::2.L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6, %7;"
-      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(c0), "r"(c1),
-         "r"(c2), "h"(cta_mask), "l"(pol)
-      : "memory");
-}
+template <int CG>
+struct OperandLoad<CG, false> {
+  __device__ static __forceinline__ void load(uint32_t dst, const CUtensorMap* map,
+                                              uint32_t bar, int32_t c0, int32_t c1, int32_t c2,
+                                              uint16_t cta_mask, uint64_t pol) {
+    (void)cta_mask;
+    if constexpr (CG == 1) tma_load_3d(dst, map, bar, c0, c1, c2, pol);
+    else tma_load_3d_pair(dst, map, bar, c0, c1, c2, pol);
+  }
+};
 
 // 3-D tiled TMA store from this CTA's shared memory (bulk-group completion).
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int32_t c0,

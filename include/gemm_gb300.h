@@ -54,7 +54,8 @@ typedef enum {
   GEMM_ERR_UNSUPPORTED_ARCH = 4,   /* device is not compute capability 10.3 */
   GEMM_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed */
   GEMM_ERR_DEVICE_TIMEOUT = 6,     /* a kernel pipeline wait exceeded its limit */
-  GEMM_ERR_UNSUPPORTED_CONFIG = 7  /* a forced kernel configuration cannot run this problem */
+  GEMM_ERR_UNSUPPORTED_CONFIG = 7, /* a forced kernel configuration cannot run this problem */
+  GEMM_ERR_DEVICE_CHECK = 8        /* debug library only: a device-side bounds check failed */
 } gemm_status_t;
 
 /* GEMM_TF32: fp32 storage read by the tensor core at tf32 precision (sign,
@@ -105,29 +106,41 @@ typedef struct {
  *   cta_group   1: each CTA owns a 128 x tile_n output tile (tcgen05 cta_group::1)
  *               2: a CTA pair owns a 256 x tile_n tile (tcgen05 cta_group::2);
  *                  each CTA stages 128 rows of A and tile_n/2 rows of B.
- *   tile_n      output tile width: 128 or 256.
+ *   tile_n      output tile width of one CTA group: 64 to 256 in steps of 32
+ *               (the custom-epilogue example's "Constraints": MMA tile N a
+ *               multiple of 32 up to 256; 32 itself is not offered).
  *   stages      depth of the shared-memory A/B ring (0 = as deep as fits).
  *   group_m     tile rasterisation: tiles are walked in column strips
  *               group_m tiles high, odd strips from the last column back;
  *               odd waves of tiles also walk K from the last k-block down
  *               (fp32 accumulators), so each wave starts on the operand
  *               blocks the previous one read last (0 = automatic: 12).
- *   cluster_m   CTA groups per thread-block cluster, stacked along M, that share
- *               their B tile through TMA multicast: 1 or 2 (0 = automatic).  The
- *               cluster holds cta_group * cluster_m CTAs.
+ *   cluster_m   CTA groups per thread-block cluster stacked along M, sharing
+ *               their B columns through TMA multicast: 1 or 2.
+ *   cluster_n   (after tail_split) CTA groups per cluster side by side along N,
+ *               sharing their A rows through TMA multicast: 1 or 2.  The
+ *               cluster holds cta_group * cluster_m * cluster_n CTAs.  As an
+ *               input, both 0 = automatic; either non-zero fixes the shape (0
+ *               counting as 1).  Multicast clusters are built only into the
+ *               single-GPU library (libgemm_gb300.so); the library for
+ *               processes that drive several GPUs (libgemm_gb300_nomc.so)
+ *               returns GEMM_ERR_UNSUPPORTED_CONFIG for them.
  *   epi_slots   (also an input) epilogue slots, 2..6 (0 = automatic).
- *   l2_hints    (also an input) L2 eviction priority of the TMA copies, 2 bits
+ *   Fields marked "diagnostic" are for tuning and testing the kernel, not
+ *   part of the GEMM contract; leave them 0.
+ *   l2_hints    (diagnostic; also an input) L2 eviction priority of the TMA
+ *               copies, 2 bits
  *               each (0 normal, 1 evict-last, 2 evict-first): bits 0-1 A/B
  *               loads, 2-3 C/X loads, 4-5 D/Y stores.  As an input it applies
  *               only with bit 8 set (0 = automatic).
- *   epi_wait_ns (also an input) suspend-time hint, in ns, of the epilogue's
+ *   epi_wait_ns (diagnostic; also an input) suspend-time hint, in ns, of the epilogue's
  *               wait for a finished accumulator; as an input, value + 1
  *               (0 = automatic, 1 = no hint).
  *   tail_split  tiles of the last, partial wave run as two half-width (tile_n/2)
  *               items each, so that wave takes about half as long; reports how
  *               many tiles were split.  As an input: 0 = automatic (split when the
  *               partial wave fills at most half the clusters), 1 = never.
- *   inject_stall  (input, tests of the watchdog only) non-zero: the MMA warp
+ *   inject_stall  (diagnostic input, tests of the watchdog only) non-zero: the MMA warp
  *               first waits on a barrier nothing ever arrives at, so every launch
  *               ends through the watchdog with GEMM_ERR_DEVICE_TIMEOUT (role 6 in
  *               the status word) after the configured timeout.
@@ -135,7 +148,7 @@ typedef struct {
  *   tile_m      128 * cta_group (rows of one CTA group's tile).
  *   tile_k      K elements per ring stage: one or two 128-byte swizzle atoms (64
  *               or 128 K for 16-bit inputs, 128 or 256 for 8-bit); two unless the
- *               tile is a single CTA's 128 x 256.
+ *               tile is a single CTA's and wider than 128.
  *   acc_stages  tensor-memory accumulator stages (2: double buffered).
  *   ring_bytes  ring bytes per CTA: stages*(A stage + B stage) + 8 bytes per
  *               mbarrier (2 per stage, 2 per accumulator stage) + 4 bytes of
@@ -159,6 +172,7 @@ typedef struct {
   int epi_wait_ns;
   int inject_stall;
   int tail_split;
+  int cluster_n;
 } gemm_config_t;
 
 /* Every argument of one gemm_run call, for the host-only planning calls. */
@@ -229,8 +243,8 @@ gemm_status_t gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K, in
                             float alpha, float beta, float x_factor,
                             const gemm_dtypes_t* dtypes, struct CUstream_st* stream);
 
-/* Ring statistics, for studying the kernel's pipeline (no counterpart on the
- * pages).  Only the statistics build of the library (libgemm_gb300_stats.so,
+/* Diagnostic, not part of the GEMM contract.  Ring statistics, for studying
+ * the kernel's pipeline (no counterpart on the pages).  Only the statistics build of the library (libgemm_gb300_stats.so,
  * compiled with GB300_RING_STATS=1; the product library returns
  * GEMM_ERR_UNSUPPORTED_CONFIG) counts, in each CTA of the last launch, the
  * clock cycles its roles spend waiting on the pipeline's barriers.  The call
@@ -248,8 +262,16 @@ gemm_status_t gemm_ring_stats(gemm_handle_t h, struct CUstream_st* stream, uint6
 
 /* Synchronise `stream`, then read and clear the handle's device status word.
  * Returns GEMM_ERR_DEVICE_TIMEOUT if any kernel since the last call hit its
- * watchdog, GEMM_ERR_CUDA if the stream reported an error, else GEMM_OK.
- * *detail (optional) receives the raw status word (0 when clean). */
+ * watchdog, GEMM_ERR_DEVICE_CHECK if (debug library, libgemm_gb300_debug.so,
+ * built with GB300_DEBUG=1) a device-side bounds check failed -- a TMA box
+ * outside its shared-memory slot, a TMA coordinate that is not 16-byte
+ * aligned or a store starting below zero, a tensor-memory column range past
+ * its accumulator stage; the access was skipped and the status word holds
+ * 0xD0CCBBBB, CC the check -- GEMM_ERR_CUDA if the stream reported an error,
+ * else GEMM_OK.
+ * *detail (optional; may be NULL) receives the raw status word (0 when
+ * clean): an extension of the two-argument call, carrying the watchdog's
+ * record 0xE0RRBBBB (RR the waiting role, BBBB the low bits of the block). */
 gemm_status_t gemm_sync_status(gemm_handle_t h, struct CUstream_st* stream, uint32_t* detail);
 
 /* Human-readable name of a status code (static storage). */

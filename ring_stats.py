@@ -1,6 +1,6 @@
 """Per-role pipeline statistics of the GEMM kernel on a workload.
 
-    python -m dense_gemm_epilogue_persistent_gb300.ring_stats [WORKLOAD ...] [--launches N] [--json]
+    python ring_stats.py [WORKLOAD ...] [--launches N] [--json]
 
 Builds (if needed) and loads the ring-statistics library -- the product
 sources compiled with per-role wait counters -- runs each named workload
@@ -12,15 +12,19 @@ reports, for the last launch, the share of each role's loop spent waiting:
   producer     waiting for a stage to drain (a full ring);
   epilogue     waiting for a finished accumulator and for C/X to land.
 
-Run from the repository root (it reads the workload definitions there).
+A measurement tool beside bench.py: it draws the workloads' inputs with
+workloads.py, as the benchmark does.
 """
 from __future__ import annotations
 
 import argparse
 import json
+import os
 import sys
 
-from . import build as _build
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+
+from dense_gemm_epilogue_persistent_gb300 import build as _build  # noqa: E402
 
 
 def _device_inputs(G, W, w, torch):
@@ -75,7 +79,8 @@ def measure(names, launches=30):
             out.append({
                 "workload": name,
                 "kernel": f"{cfg.tile_m}x{cfg.tile_n} cta_group={cfg.cta_group} "
-                          f"cluster_m={cfg.cluster_m} stages={cfg.stages} "
+                          f"cluster_m={cfg.cluster_m} cluster_n={cfg.cluster_n} "
+                          f"stages={cfg.stages} "
                           f"epi_slots={cfg.epi_slots} grid={cfg.grid_ctas}",
                 "tflops_with_counters": round(w.flops / ms / 1e9, 1),
                 "mma_wait_stage_pct": round(100 * share(mma, 0, 2), 2),

@@ -51,7 +51,7 @@ def test_library_links_no_driver_library():
 
 
 def test_status_strings(lib):
-    for code in range(8):
+    for code in range(9):
         assert G.gemm_status_string(code).startswith("GEMM_")
     assert G.gemm_status_string(99) == "GEMM_ERR_UNKNOWN"
 
@@ -202,24 +202,31 @@ def test_plan_every_workload(lib, name):
     assert G.gemm_check(p) == G.GEMM_OK
     st, cfg = G.gemm_plan(p, 152, 232448)
     assert st == G.GEMM_OK
-    assert cfg.cta_group in (1, 2) and cfg.tile_n in (128, 256)
+    assert cfg.cta_group in (1, 2) and cfg.tile_n in range(128, 257, 32)
     atom_k = 128 // W.ELEM_BYTES[w.ab]                 # K of one 128-byte swizzle atom
-    k_atoms = 1 if (cfg.cta_group, cfg.tile_n) == (1, 256) else 2
+    k_atoms = 1 if (cfg.cta_group == 1 and cfg.tile_n > 128) else 2
     assert cfg.tile_k == atom_k * k_atoms
     assert 2 <= cfg.stages and cfg.smem_bytes <= 232448
     rows = cfg.tile_m * cfg.cluster_m                  # output rows per cluster tile
-    assert cfg.tiles == (-(-w.M // rows)) * (-(-w.N // cfg.tile_n)) * w.L
-    assert cfg.cluster_m in (1, 2)
-    assert cfg.grid_ctas % (cfg.cta_group * cfg.cluster_m) == 0 and cfg.grid_ctas <= 152
+    cols = cfg.tile_n * cfg.cluster_n                  # output columns per cluster tile
+    assert cfg.tiles == (-(-w.M // rows)) * (-(-w.N // cols)) * w.L
+    assert cfg.cluster_m in (1, 2) and cfg.cluster_n in (1, 2)
+    csize = cfg.cta_group * cfg.cluster_m * cfg.cluster_n
+    assert cfg.grid_ctas % csize == 0 and cfg.grid_ctas <= 152
     assert 2 * G.gemm_tmem_columns(128, cfg.tile_n) <= 512
 
 
 def test_plan_forced_and_rejected(lib):
     p = _p(M=1024, N=1024, K=512, lda=512, ldb=512)
     for cg in (1, 2):
-        for bn in (128, 256):
+        for bn in range(64, 257, 32):
             st, cfg = G.gemm_plan(p, 152, 232448, G.gemm_config_t(cta_group=cg, tile_n=bn))
             assert st == 0 and (cfg.cta_group, cfg.tile_n) == (cg, bn)
+            assert cfg.tiles == (1024 // (128 * cg)) * -(-1024 // bn)
+            assert cfg.smem_bytes <= 232448 and cfg.stages >= 2
+    for bn in (0, 32, 80, 288):              # only multiples of 32 from 64 to 256
+        st, _ = G.gemm_plan(p, 152, 232448, G.gemm_config_t(tile_n=bn))
+        assert (st == 0) == (bn == 0)
     st, _ = G.gemm_plan(p, 152, 232448, G.gemm_config_t(cta_group=1, tile_n=256, stages=9))
     assert st == G.GEMM_ERR_UNSUPPORTED_CONFIG                 # 9 x 48 KiB does not fit
     # fp8 with N-major B needs 128 B rows per CTA: not with tile_n/cta_group = 64
@@ -311,3 +318,94 @@ def test_plan_group_m_default_and_clamp(lib):
     st, cfg = G.gemm_plan(small, 152, 232448)
     tiles_m = -(-1024 // cfg.tile_m)
     assert st == 0 and cfg.group_m == min(12, tiles_m)
+
+
+def test_plan_clusters_sharing_a(lib):
+    """Clusters of two CTA groups side by side along N (A shared by
+    multicast): a cluster tile covers 2 x tile_n columns, the last wave is
+    never split, and an MN-major 8-bit A cannot be shared (its 128 rows are a
+    single 128-byte atom)."""
+    p = _p(M=8192, N=8192, K=8192, lda=8192, ldb=8192, dtypes=G.make_dtypes("f16", "f16", "f16"))
+    for cm, cn in ((1, 2), (2, 2), (2, 1)):
+        st, cfg = G.gemm_plan(p, 152, 232448, G.gemm_config_t(cta_group=2, tile_n=256,
+                                                              cluster_m=cm, cluster_n=cn))
+        assert st == 0 and (cfg.cluster_m, cfg.cluster_n) == (cm, cn)
+        assert cfg.tiles == (8192 // (256 * cm)) * (8192 // (256 * cn)) and cfg.tail_split == 0
+        assert cfg.grid_ctas % (2 * cm * cn) == 0
+    st, cfg = G.gemm_plan(p, 152, 232448, G.gemm_config_t(cluster_n=2))
+    assert st == 0 and (cfg.cluster_m, cfg.cluster_n) == (1, 2)
+    dt8 = G.make_dtypes("e4m3", "f16", "f16")
+    p8 = _p(M=1024, N=1024, K=512, lda=1024, ldb=512, layoutA=G.GEMM_MN_MAJOR, dtypes=dt8)
+    st, _ = G.gemm_plan(p8, 152, 232448, G.gemm_config_t(cluster_n=2))
+    assert st == G.GEMM_ERR_UNSUPPORTED_CONFIG
+    st, _ = G.gemm_plan(p8, 152, 232448, G.gemm_config_t(cluster_m=2))
+    assert st == 0
+
+
+def _includes(path, seen):
+    """Every in-tree file `path` includes, transitively."""
+    import re
+    d = os.path.dirname(path)
+    seen.add(path)
+    with open(path) as f:
+        for m in re.finditer(r'#include\s+"([^"]+)"', f.read()):
+            for cand in (os.path.join(d, m.group(1)), os.path.join(ROOT, "include", m.group(1))):
+                if os.path.exists(cand) and cand not in seen:
+                    _includes(cand, seen)
+    return seen
+
+
+def test_multi_gpu_library_sources_have_no_multicast_load():
+    """The library for processes that drive several GPUs is built only from
+    files that name no multicast TMA load: its translation units and every
+    header they include."""
+    from dense_gemm_epilogue_persistent_gb300 import build as B
+    csrc = os.path.join(ROOT, "dense_gemm_epilogue_persistent_gb300", "csrc")
+    files = set()
+    for _, src, _ in B.units("nomc"):
+        _includes(os.path.join(csrc, src), files)
+    names = {os.path.basename(f) for f in files}
+    assert names <= set(B.NOMC_FILES) | {"gemm_gb300.h"}, names
+    for f in files:
+        with open(f) as fh:
+            text = fh.read()
+        assert "multicast::cluster" not in text.replace(
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster",
+            "").replace(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster",
+            ""), f
+        assert '#include "ptx_multicast.cuh"' not in text, f
+    # the single-GPU library does hold them
+    with open(os.path.join(csrc, "ptx_multicast.cuh")) as fh:
+        assert "cp.async.bulk.tensor" in fh.read()
+
+
+def test_multi_gpu_library_exports_and_rejects_multicast():
+    """libgemm_gb300_nomc.so exports every symbol the header declares and its
+    planner refuses operand-sharing clusters."""
+    import ctypes
+    from dense_gemm_epilogue_persistent_gb300 import build as B
+    lib = ctypes.CDLL(B.build(kind="nomc"))
+    for name in _header_symbols():
+        assert hasattr(lib, name), name
+    lib.gemm_plan.argtypes = [ctypes.POINTER(G.gemm_problem_t), ctypes.c_int, ctypes.c_int,
+                              ctypes.POINTER(G.gemm_config_t), ctypes.POINTER(G.gemm_config_t)]
+    p = _p(M=4096, N=4096, K=4096, lda=4096, ldb=4096, dtypes=G.make_dtypes("f16", "f16", "f16"))
+    out = G.gemm_config_t()
+    for cm, cn in ((2, 1), (1, 2), (2, 2)):
+        forced = G.gemm_config_t(cluster_m=cm, cluster_n=cn)
+        assert lib.gemm_plan(ctypes.byref(p), 152, 232448, ctypes.byref(forced),
+                             ctypes.byref(out)) == G.GEMM_ERR_UNSUPPORTED_CONFIG
+    assert lib.gemm_plan(ctypes.byref(p), 152, 232448, None, ctypes.byref(out)) == 0
+    assert (out.cluster_m, out.cluster_n) == (1, 1)
+
+
+def test_debug_library_builds_and_maps_device_checks():
+    """The debug library (device-side bounds checks) compiles from the same
+    sources, exports the header's symbols, and its status code has a name."""
+    import ctypes
+    from dense_gemm_epilogue_persistent_gb300 import build as B
+    lib = ctypes.CDLL(B.build(kind="debug"))
+    for name in _header_symbols():
+        assert hasattr(lib, name), name
+    assert G.gemm_status_string(G.GEMM_ERR_DEVICE_CHECK) == "GEMM_ERR_DEVICE_CHECK"

@@ -17,10 +17,31 @@ from gemm_cases import (Case, assert_within, compare_full, compare_sampled, logi
 
 pytestmark = pytest.mark.gpu
 
-# (cta_group, tile_n, cluster_m): single CTAs and CTA pairs, 128- and
-# 256-wide tiles, without and with B shared by TMA multicast across the cluster.
+# (cta_group, tile_n, cluster_m[, cluster_n]): single CTAs and CTA pairs, 128-
+# and 256-wide tiles, alone and in clusters whose groups share B (stacked
+# along M) or A (side by side along N) through TMA multicast.
 VARIANTS = [(1, 128, 1), (1, 256, 1), (2, 128, 1), (2, 256, 1),
-            (1, 128, 2), (1, 256, 2), (2, 128, 2), (2, 256, 2)]
+            (1, 128, 2), (1, 256, 2), (2, 128, 2), (2, 256, 2),
+            (1, 128, 1, 2), (2, 256, 1, 2), (2, 192, 1, 2), (2, 256, 2, 2)]
+# The other tile widths (multiples of 32 from 64 to 256), alone and in a few
+# cluster shapes.
+WIDTH_VARIANTS = [(1, 64, 1), (1, 96, 1), (1, 160, 1), (1, 192, 1), (1, 224, 1),
+                  (2, 64, 1), (2, 96, 1), (2, 160, 1), (2, 192, 1), (2, 224, 1),
+                  (1, 96, 2), (2, 160, 2), (1, 224, 1, 2), (1, 64, 2, 2)]
+
+
+def stageable(case, variant):
+    """Whether a variant can stage the case's MN-major operands: a CTA's part
+    of B (tile_n / cta_group / cluster_m rows) and of A (128 / cluster_n rows)
+    must be whole 128-byte atoms."""
+    cg, bn, mc = variant[:3]
+    nc = variant[3] if len(variant) > 3 else 1
+    atom = 128 // W.ELEM_BYTES[case.ab]
+    if case.b_mn and (bn // cg // mc) % atom != 0:
+        return False
+    if case.a_mn and (128 // nc) % atom != 0:
+        return False
+    return True
 
 
 @pytest.fixture(scope="module")
@@ -32,8 +53,8 @@ def gemm():
     g.close()
 
 
-def _force(gemm, cg, bn, mc=1, stages=0):
-    gemm.set_config(cta_group=cg, tile_n=bn, cluster_m=mc, stages=stages)
+def _force(gemm, cg, bn, mc=1, nc=1, stages=0):
+    gemm.set_config(cta_group=cg, tile_n=bn, cluster_m=mc, cluster_n=nc, stages=stages)
 
 
 def _finish(gemm):
@@ -59,7 +80,7 @@ def test_int256_bit_exact(gemm, variant):
     gemm.set_config(None)
 
 
-@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("variant", VARIANTS + WIDTH_VARIANTS)
 def test_integer_exact_ragged_all_outputs(gemm, variant):
     """Ragged shape, integer inputs, f32 C/X/D/Y: still exact (|acc| < 2^24)."""
     _force(gemm, *variant)
@@ -84,7 +105,7 @@ def test_many_tiles_per_cluster(gemm, variant):
     D, Y = run_gpu(gemm, prep)
     _finish(gemm)
     cfg = gemm.last_config()
-    clusters = cfg.grid_ctas // (cfg.cta_group * cfg.cluster_m)
+    clusters = cfg.grid_ctas // (cfg.cta_group * cfg.cluster_m * cfg.cluster_n)
     assert cfg.tiles >= 3 * clusters
     compare_full(prep, D, Y)
     gemm.set_config(None)
@@ -108,15 +129,14 @@ SMALL = {
 }
 
 
-@pytest.mark.parametrize("variant", VARIANTS + [None])
+@pytest.mark.parametrize("variant", VARIANTS + WIDTH_VARIANTS + [None])
 @pytest.mark.parametrize("name", list(SMALL))
 def test_small_workloads(gemm, name, variant):
     case = SMALL[name]
     if variant:
-        cg, bn, mc = variant
         # MN-major operands are staged (and multicast) in 128-byte atoms
-        if case.b_mn and (bn // cg // mc) % (128 // W.ELEM_BYTES[case.ab]) != 0:
-            pytest.skip("variant cannot stage this MN-major B")
+        if not stageable(case, variant):
+            pytest.skip("variant cannot stage this MN-major operand")
         _force(gemm, *variant)
     else:
         gemm.set_config(None)
@@ -161,9 +181,38 @@ def test_layout_equivalence_bitwise(gemm):
                     assert torch.equal(base[0], out[0]) and torch.equal(base[1], out[1])
 
 
+# ------------------------------------------------------------ shared operands
+
+@pytest.mark.parametrize("variant", [(2, 256, 1, 2), (1, 128, 1, 2), (2, 256, 2, 2),
+                                     (2, 128, 2, 1), (1, 192, 2, 2)])
+@pytest.mark.parametrize("ab", ["bf16", "e4m3"])
+@pytest.mark.parametrize("a_mn,b_mn", [(False, False), (True, False), (False, True),
+                                       (True, True)])
+def test_shared_operand_layouts(gemm, variant, ab, a_mn, b_mn):
+    """Clusters that share A (along N) and/or B (along M) by multicast, with
+    K-major and MN-major operands, on a ragged shape whose last cluster tiles
+    have groups entirely outside the output (rows 768.. and columns 768.. of a
+    720 x 704 output)."""
+    case = Case(M=720, N=704, K=400, L=2, ab=ab, c="f16", d="f32", x="bf16", y="f16",
+                a_mn=a_mn, b_mn=b_mn, alpha=-0.75, beta=1.0, xf=0.5,
+                dist="e4m3_pm4" if ab == "e4m3" else "normal1", seed=31)
+    if not stageable(case, variant):
+        pytest.skip("variant cannot stage this MN-major operand")
+    _force(gemm, *variant)
+    prep = prepare(case)
+    D, Y = run_gpu(gemm, prep)
+    _finish(gemm)
+    cfg = gemm.last_config()
+    assert (cfg.cluster_m, cfg.cluster_n) == (variant[2], variant[3])
+    compare_full(prep, D, Y)
+    gemm.set_config(None)
+
+
 # ------------------------------------------------------------ split last wave
 
 @pytest.mark.parametrize("variant,shape", [
+    ((2, 192, 1), (2560, 1920, 192)),      # 100 tiles on 76 pairs: 24 split
+    ((1, 64, 1), (1280, 2048, 128)),       # 320 tiles on 152 CTAs: 16 split
     ((2, 256, 1), (2560, 2560, 192)),      # 100 tiles on 76 pairs: 24 split
     ((1, 256, 1), (2048, 2560, 128)),      # 160 tiles on 152 CTAs: 8 split
     ((1, 128, 1), (2048, 1280, 256)),

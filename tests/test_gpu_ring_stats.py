@@ -18,7 +18,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 def test_ring_stats_tool_accounts_for_every_stage_and_chunk():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    r = subprocess.run([sys.executable, "-m", "dense_gemm_epilogue_persistent_gb300.ring_stats",
+    r = subprocess.run([sys.executable, "ring_stats.py",
                         "int256_f16_f32", "gemm2048_bf16_f32", "ragged_e4m3_f16",
                         "--launches", "5", "--json"],
                        cwd=ROOT, capture_output=True, text=True, timeout=900)
