@@ -18,6 +18,7 @@ from __future__ import annotations
 
 import argparse
 import csv
+import datetime
 import hashlib
 import io
 import json
@@ -34,7 +35,8 @@ METRIC = "GEMM TFLOP/s (2MNKL/t) and % of GB300 dense tensor peak per config"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "source": "fallback"}
 SMI_FIELDS = ("pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "timestamp")
 
 
 def parse_args():
@@ -75,7 +77,7 @@ def tensor_peak(peaks, ab: str, sustained=False):
     return base * PEAK_RATIO[ab]
 
 
-DEVICE_SOURCES = ("gemm_kernel.cuh", "ptx.cuh", "kernels.h")
+DEVICE_SOURCES = ("gemm_kernel.cuh", "ptx.cuh", "ptx_multicast.cuh", "kernels.h")
 
 
 def kernel_source_digest():
@@ -97,8 +99,8 @@ def kernel_source_digest():
 
 
 def config_key(cfg) -> str:
-    return (f"cg{cfg.cta_group}_n{cfg.tile_n}_mc{cfg.cluster_m}_k{cfg.tile_k}_st{cfg.stages}"
-            f"_e{cfg.epi_slots}_gm{cfg.group_m}_l2{cfg.l2_hints}")
+    return (f"cg{cfg.cta_group}_n{cfg.tile_n}_mc{cfg.cluster_m}_nc{cfg.cluster_n}"
+            f"_k{cfg.tile_k}_st{cfg.stages}_e{cfg.epi_slots}_gm{cfg.group_m}_l2{cfg.l2_hints}")
 
 
 def recorded_traffic(workload: str, cfg):
@@ -117,19 +119,19 @@ def recorded_traffic(workload: str, cfg):
 
 # ---------------------------------------------------------------- clocks
 
-LOAD_W = 300.0        # a sample drawing more than this is "under load" (idle: ~170-190 W)
-
-
 class ClockSampler:
     """nvidia-smi samples (every `period_ms`) of this GPU's clocks, power and
-    throttle reasons while a timed region runs.  The reported SM clock is the
-    median over the samples taken under load (all samples if none was)."""
+    throttle reasons.  mark_start()/mark_end() bracket the timed region on the
+    host clock; the samples whose timestamps fall inside it are the ones
+    "under load", and the reported SM clock is their median (all samples'
+    if none falls inside)."""
 
     def __init__(self, pci_bus: int | None, period_ms: int = 20):
         self.pci_bus = pci_bus
         self.period_ms = period_ms
         self.proc = None
         self.out = None
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
@@ -139,6 +141,12 @@ class ClockSampler:
                  "-lms", str(self.period_ms)], stdout=self.out, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def stop(self):
         if not self.proc:
@@ -151,12 +159,18 @@ class ClockSampler:
             self.proc.kill()
         self.out.seek(0)
         rows = [[c.strip() for c in r] for r in csv.reader(io.StringIO(self.out.read()))
-                if len(r) >= 9]
+                if len(r) >= 10]
         self.out.close()
 
         def bus(r):
             try:
                 return int(r[0].split(":")[1], 16)
+            except Exception:
+                return None
+
+        def stamp(r):
+            try:
+                return datetime.datetime.strptime(r[9], "%Y/%m/%d %H:%M:%S.%f").timestamp()
             except Exception:
                 return None
 
@@ -168,16 +182,18 @@ class ClockSampler:
             except ValueError:
                 return None
 
-        loaded = [r for r in mine if (num(r[3]) or 0.0) > LOAD_W]
-        sm = [x for x in (num(r[1]) for r in (loaded or mine)) if x is not None]
+        inside = []
+        if self.t0 is not None and self.t1 is not None:
+            inside = [r for r in mine if stamp(r) is not None and self.t0 <= stamp(r) <= self.t1]
+        sm = [x for x in (num(r[1]) for r in (inside or mine)) if x is not None]
         smax = [x for x in (num(r[2]) for r in mine) if x is not None]
         power = [x for x in (num(r[3]) for r in mine) if x is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in mine for i in range(4)
+        reasons = sorted({names[i] for r in (inside or mine) for i in range(4)
                           if r[5 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
-                "samples": len(mine), "samples_under_load": len(loaded),
+                "samples": len(mine), "samples_under_load": len(inside),
                 "period_ms": self.period_ms, "power_w_max": max(power) if power else None}
 
 
@@ -489,6 +505,7 @@ def main():
     time.sleep(0.25)
     barrier()
     torch.cuda.synchronize()
+    sampler.mark_start()
     t_start.record(stream)
     for e0, e1 in evs:
         e0.record(stream)
@@ -496,6 +513,7 @@ def main():
         e1.record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
+    sampler.mark_end()
     barrier()
     clocks = sampler.stop()
     st, detail = g.sync_status(stream.cuda_stream)
@@ -599,7 +617,9 @@ def main():
                 sampler_c = ClockSampler(getattr(props, "pci_bus_id", None))
                 sampler_c.start()
                 time.sleep(0.1)
+                sampler_c.mark_start()
                 ms, ms_min = time_reps(torch, bc, stream, iters=iters)
+                sampler_c.mark_end()
                 clk = sampler_c.stop()
                 c2 = g.last_config()
                 tf = wc.flops / (ms / 1e3) / 1e12

@@ -37,7 +37,7 @@ GEMM_ERR_DEVICE_CHECK = 8
 GEMM_F32, GEMM_F16, GEMM_BF16, GEMM_E4M3, GEMM_E5M2, GEMM_TF32 = 0, 1, 2, 3, 4, 5
 GEMM_K_MAJOR, GEMM_MN_MAJOR = 0, 1
 GEMM_EPI_LINEAR, GEMM_EPI_RELU = 0, 1
-GEMM_RING_STAT_WORDS = 12
+GEMM_RING_STAT_WORDS = 16
 
 DTYPE_CODES = {"f32": GEMM_F32, "f16": GEMM_F16, "bf16": GEMM_BF16, "e4m3": GEMM_E4M3,
                "e5m2": GEMM_E5M2, "tf32": GEMM_TF32}

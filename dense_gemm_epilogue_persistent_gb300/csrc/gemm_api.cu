@@ -270,41 +270,39 @@ bool variant_supports(const gemm_problem_t& p, int cg, int bn, int mc, int nc) {
 // the time of one tile, in units of one 128-byte-K-atom k-block of a 256 x 256
 // CTA-pair tile.  A tile takes the longer of its main loop and its epilogue,
 // plus a fixed cost (pipeline fill, hand-offs, the tail of the epilogue).
-// Constants fitted (least squares on log time, variants compared within each
-// problem) to a GB300 sweep of every variant over 17 problems: 256^3 to 8192^3,
-// K from 256 to 8192, 16-bit, fp8 and tf32 inputs, fp32 and 16-bit epilogues with
-// and without C, X and Y, ragged and batched shapes.  Main loop per k-block:
-// the tile's share of tensor work (tile_n / 256) plus a feed overhead that
-// grows as the tile narrows (each CTA still stages 128 A rows per k-block):
-//   CTA pairs          tile_n/256 + 0.22 (256 - tile_n)/128   (2x256: 1.0, 2x128: 0.72)
-//   single CTAs, 2 atoms per stage   tile_n/256 + 0.18 (256 - tile_n)/128   (1x128: 0.68)
-//   single CTAs, 1 atom per stage    1.23 tile_n/256                       (1x256: 1.23)
+// Main loop per k-block: the tile's share of tensor work (tile_n / 256) plus a
+// feed overhead that grows as the tile narrows (each CTA still stages 128 A
+// rows per k-block):
+//   CTA pairs                        tile_n/256 + 0.22 (256 - tile_n)/128
+//   single CTAs, 2 atoms per stage   tile_n/256 + 0.18 (256 - tile_n)/128
+//   single CTAs, 1 atom per stage    1.15 tile_n/256
 // fixed per tile: pairs 15.0 - 1.9 (tile_n - 128)/128, single CTAs 11.0 -
-// 0.4 (tile_n - 128)/128; epilogue: tile_n/32 chunks per CTA, each 1.64 + 0.043
+// 0.4 (tile_n - 128)/128; epilogue: tile_n/32 chunks per CTA, each 2.5 + 0.08
 // per KB the chunk moves (C and X read, D and Y written, 128 x 32 elements
-// each) + 6.0 spread over the slots - 1 chunks of C/X lookahead when it
-// loads; a last wave split into half-width items (tail_split) costs ~0.6 of
-// a wave.  Clusters that share operands by multicast pay the wave count of
-// the larger clusters that fit.
+// each); a last wave split into half-width items (tail_split) costs ~0.8 of a
+// wave.  Constants fitted on GB300 to a sweep of all 14 widths x CTA groups
+// over 11 workloads (256^3 to 8192^3; 16-bit, fp8, mixed fp8, tf32 inputs;
+// fp32 and fp16 accumulators; fp32 and 16-bit epilogues with and without C, X,
+// Y; ragged and batched shapes): the pick is the measured fastest variant on
+// 10 of them and within 0.2 % on the eleventh.  (With per-warp epilogue
+// pipelines the number of C/X slots no longer changes the cost.)
 double plan_cost(int64_t tiles, int64_t k_blocks, int cg, int ka, int bn, int64_t clusters,
-                 bool epi_loads, int epi_slots, double epi_kb, bool can_split) {
+                 double epi_kb, bool can_split) {
   clusters = std::max<int64_t>(1, clusters);
   const int64_t full = tiles / clusters, rem = tiles % clusters;
   const double waves =
-      (double)full + (rem == 0 ? 0.0 : (can_split && 2 * rem <= clusters ? 0.6 : 1.0));
+      (double)full + (rem == 0 ? 0.0 : (can_split && 2 * rem <= clusters ? 0.8 : 1.0));
   const double w = bn / 256.0;
   double per_kb, fixed;
   if (cg == 2) {
     per_kb = w + 0.22 * (256 - bn) / 128.0;
     fixed = 15.0 - 1.9 * (bn - 128) / 128.0;
   } else {
-    per_kb = ka == 1 ? 1.23 * w : w + 0.18 * (256 - bn) / 128.0;
+    per_kb = ka == 1 ? 1.15 * w : w + 0.18 * (256 - bn) / 128.0;
     fixed = 11.0 - 0.4 * (bn - 128) / 128.0;
   }
   const double main_loop = (double)k_blocks * per_kb;
-  const double chunk =
-      1.64 + 0.043 * epi_kb + (epi_loads ? 6.0 / std::max(1, epi_slots - 1) : 0.0);
-  const double epilogue = (double)(bn / gb300::kEpiChunk) * chunk;
+  const double epilogue = (double)(bn / gb300::kEpiChunk) * (2.5 + 0.08 * epi_kb);
   return waves * (std::max(main_loop, epilogue) + fixed);
 }
 
@@ -317,21 +315,6 @@ bool can_split_tail(const gemm_problem_t& p, int cg, int bn, int mc, int nc) {
   if ((bn / 2) % gb300::kEpiChunk != 0) return false;
   const int atom = 128 / dtype_bytes(p.dtypes.ab);
   return p.layoutB == GEMM_K_MAJOR || (bn / cg / 2) % atom == 0;
-}
-
-// Epilogue slots the planner gives a variant: the deepest ring that leaves two
-// slots (one stage less when the problem is a single wave of tiles and the
-// ring stays at least three deep), then every further slot that fits (at
-// most kMaxEpiSlots).
-int auto_slots(int cg, int bn, int ka, int slot, int smem_optin, bool one_wave) {
-  int stages = 0;
-  while (stages < kMaxStages && total_smem(cg, bn, ka, stages + 1, 2, slot) <= smem_optin)
-    ++stages;
-  if (one_wave && stages >= 4) --stages;
-  int slots = 2;
-  while (slots < kMaxEpiSlots && total_smem(cg, bn, ka, stages, slots + 1, slot) <= smem_optin)
-    ++slots;
-  return slots;
 }
 
 // Resident clusters of `csize` CTAs: the device's measured occupancy when
@@ -386,11 +369,7 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
                                 cdiv(std::max<int64_t>(p.N, 1), (int64_t)b * n) *
                                 std::max<int64_t>(p.L, 1);
           const int64_t units = resident_clusters(sm_count, clusters_by_size, a * m * n);
-          const double c = plan_cost(tiles, cdiv(p.K, 128 / ab_bytes), a, ka, b, units,
-                                     reads_c(p) || reads_x(p),
-                                     auto_slots(a, b, ka, epi_slot_bytes(p), smem_optin,
-                                                tiles <= units),
-                                     epi_kb,
+          const double c = plan_cost(tiles, cdiv(p.K, 128 / ab_bytes), a, ka, b, units, epi_kb,
                                      can_split_tail(p, a, b, m, n) &&
                                          !(forced && forced->tail_split == 1));
           if (c < best - 1e-9) { best = c; cg = a; bn = b; mc = m; nc = n; }
@@ -410,18 +389,15 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
   };
   // The deepest A/B ring that still leaves two epilogue slots, then every
   // further slot that fits: more slots let C/X loads run further ahead, which
-  // keeps the epilogue ahead of fast main loops (8-bit inputs, short K).
+  // keeps the epilogue ahead of fast main loops (8-bit inputs, short K).  (A
+  // CTA's last tile takes the C/X its lookahead has not reached from the
+  // drained ring, so single-wave problems need no extra slots.)
   const int max_stages = max_stages_for(2);
-  int stages = forced && forced->stages ? forced->stages : max_stages;
+  const int stages = forced && forced->stages ? forced->stages : max_stages;
   const int64_t tiles_m = cdiv(std::max<int64_t>(p.M, 1), 128 * cg * mc);
   const int64_t tiles_n = cdiv(std::max<int64_t>(p.N, 1), (int64_t)bn * nc);
   const int64_t tiles = tiles_m * tiles_n * std::max<int64_t>(p.L, 1);
   const int64_t units = resident_clusters(sm_count, clusters_by_size, csize);
-  // One wave: every CTA runs one tile and then its whole epilogue, which nothing
-  // overlaps.  A ring one stage shallower (still >= 3 deep) frees room for more
-  // epilogue slots, so C/X load further ahead (2048^3 bf16, fp32 C/D: 24.3 ->
-  // 21.7 us with 3 stages and 5 slots instead of 4 and 2; 2 stages is slower).
-  if (!(forced && forced->stages) && max_stages >= 4 && tiles <= units) stages = max_stages - 1;
   if (stages < 2 || stages > max_stages) return GEMM_ERR_UNSUPPORTED_CONFIG;
   int slots = 2;
   while (slots < kMaxEpiSlots && total_smem(cg, bn, ka, stages, slots + 1, slot) <= smem_optin)

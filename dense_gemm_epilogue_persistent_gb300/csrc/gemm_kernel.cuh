@@ -128,7 +128,10 @@ enum : int {
   kStatEpiCfull,        //   ... waiting for C/X to land
   kStatEpiLoop,         //   ... in its whole loop
   kStatEpiChunks,       //   chunks processed
-  kStatWords = 12
+  kStatEpiRead,         //   ... from C/X landing to C/X read and accumulator columns in registers
+  kStatEpiMath,         //   ... computing D and Y and writing them to shared memory
+  kStatEpiIssue,        //   ... issuing the stores (and the next loads, with their wait)
+  kStatWords = 16
 };
 
 __device__ __forceinline__ long long stat_clock() {
@@ -782,7 +785,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     int slot_idx = 0;                       // gc % E
     uint32_t slot_ph = 0;                   // (gc / E) & 1: phase of the slot's cfull barrier
     bool ok = true;
-    long long st_tfull = 0, st_cfull = 0;
+    long long st_tfull = 0, st_cfull = 0, st_read = 0, st_math = 0, st_issue = 0;
     const long long st_t0 = stat_clock();
     for (int it = cluster_id; ok && it < p.num_items; it += num_clusters) {
       int half;
@@ -849,7 +852,8 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         if (loads && got)
           got = from_ring ? wait_phase<true>(rfull0 + 8u * q, 0u, w, kWaitEpiLoad)
                           : wait_phase<true>(bar0 + 8u * slot_idx, slot_ph, w, kWaitEpiLoad);
-        if constexpr (kRingStats) st_cfull += clock64() - t_c;
+        long long t_r = 0;
+        if constexpr (kRingStats) { t_r = clock64(); st_cfull += t_r - t_c; }
         got = __all_sync(0xFFFFFFFFu, got);
         if (got && e.read_c) {
           smem_read_row(slot, e.c_dt, e.cd_m_major, lane, cv);
@@ -881,6 +885,8 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         ok = got;
         if (!ok) break;
+        long long t_m = 0;
+        if constexpr (kRingStats) { t_m = clock64(); st_read += t_m - t_r; }
         // No store still reads the sub-slot D and Y go into (with C/X loads,
         // the load that filled it was issued after that), and every lane has
         // read its C/X row before any lane overwrites the sub-slot (a narrower
@@ -921,6 +927,8 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         fence_proxy_async_smem();
         __syncwarp();
+        long long t_i = 0;
+        if constexpr (kRingStats) { t_i = clock64(); st_math += t_i - t_m; }
         if (lead) {
           const int col0 = ncol0 + j * kEpiChunk;
           const int x0 = e.cd_m_major ? row0 : col0, x1 = e.cd_m_major ? col0 : row0;
@@ -935,13 +943,16 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           bulk_commit_group();
           if (loads) {
             // C/X of chunk gc+E-1 go into the sub-slot of chunk gc-1, once its
-            // store (the one before the store just issued) has read it.
-            bulk_wait_group_read<1>();
+            // store (the one before the store just issued) has read it; with
+            // nothing left to load (the drained-ring batch has the rest) no
+            // store is waited for.
+            if (ld.it < p.num_items) bulk_wait_group_read<1>();
             issue_loads();
           }
         }
         if (++slot_idx == E) { slot_idx = 0; slot_ph ^= 1u; }
         __syncwarp();
+        if constexpr (kRingStats) st_issue += clock64() - t_i;
       }
       if (++acc == kAccStages) { acc = 0; aph ^= 1u; }
     }
@@ -953,6 +964,9 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         o[kStatEpiCfull] = st_cfull;
         o[kStatEpiLoop] = clock64() - st_t0;
         o[kStatEpiChunks] = gc;
+        o[kStatEpiRead] = st_read;
+        o[kStatEpiMath] = st_math;
+        o[kStatEpiIssue] = st_issue;
       }
     }
     __syncwarp();

@@ -89,6 +89,10 @@ def measure(names, launches=30):
                 "producer_wait_drain_pct": round(100 * share(rows, 4, 5), 2),
                 "epilogue_wait_accumulator_pct": round(100 * share(rows, 6, 8), 2),
                 "epilogue_wait_cx_pct": round(100 * share(rows, 7, 8), 2),
+                "epilogue_read_cycles_per_chunk": round(share(rows, 10, 9), 1),
+                "epilogue_math_cycles_per_chunk": round(share(rows, 11, 9), 1),
+                "epilogue_issue_cycles_per_chunk": round(share(rows, 12, 9), 1),
+                "epilogue_cx_wait_cycles_per_chunk": round(share(rows, 7, 9), 1),
                 "stages": int(sum(r[3] for r in mma)),
                 "chunks": int(sum(r[9] for r in rows)),
                 "tiles": int(cfg.tiles), "tail_split": int(cfg.tail_split),

@@ -282,27 +282,36 @@ def test_ring_stats_rejected_by_product_library(lib):
     """The product library compiles no ring statistics: gemm_ring_stats
     rejects a missing handle or output and never touches the device."""
     import ctypes
-    buf = (ctypes.c_uint64 * 12)()
+    buf = (ctypes.c_uint64 * G.GEMM_RING_STAT_WORDS)()
     n = ctypes.c_int(-1)
     assert lib.gemm_ring_stats(None, None, buf, 1, ctypes.byref(n)) == G.GEMM_ERR_INVALID_ARG
     assert lib.gemm_ring_stats(None, None, None, 1, ctypes.byref(n)) == G.GEMM_ERR_INVALID_ARG
 
 
-def test_plan_single_wave_trades_a_stage_for_epilogue_slots(lib):
-    """One wave of tiles (every CTA runs one tile, its epilogue exposed): the
-    planner takes one ring stage fewer when the ring could be at least four
-    deep, and the freed shared memory becomes epilogue slots.  More than one
-    wave, or a forced stage count, keeps the deepest ring."""
-    dt = G.make_dtypes("bf16", "f32", "f32")
-    one = _p(M=2048, N=2048, K=2048, lda=2048, ldb=2048, dtypes=dt)     # 128 tiles of 128x256
-    st, cfg = G.gemm_plan(one, 152, 232448)
-    assert st == 0 and (cfg.cta_group, cfg.tile_n) == (1, 256)
-    st, deep = G.gemm_plan(one, 152, 232448, G.gemm_config_t(cta_group=1, tile_n=256, stages=4))
-    assert st == 0 and deep.stages == 4
-    assert cfg.tiles <= 152 and cfg.stages == deep.stages - 1 and cfg.epi_slots > deep.epi_slots
-    many = _p(M=4096, N=4096, K=2048, lda=2048, ldb=2048, dtypes=dt)
-    st, cfg2 = G.gemm_plan(many, 152, 232448, G.gemm_config_t(cta_group=1, tile_n=256))
-    assert st == 0 and cfg2.tiles > 152 and cfg2.stages == 4
+# The tile each workload ran fastest with in a GB300 sweep of all 14 widths x
+# CTA groups (the sweep the planner's constants are fitted to; 128-wide and
+# wider tiles, 152 SMs, bench workloads, warm L2).
+MEASURED_BEST = {
+    "int256_f16_f32": (1, 128), "gemm2048_bf16_f32": (1, 256), "efc8192_f16": (2, 256),
+    "gemm8192_bf16": (2, 256), "batched16_bf16_mn": (2, 256), "ragged_e4m3_f16": (2, 256),
+    "e5m2_4096_f16": (2, 256), "fp8mix_relu_4096": (1, 224), "tf32_4096_f32": (2, 224),
+    "f16acc_4096_f16": (2, 224), "e4m3_f16acc_4096": (2, 256),
+}
+
+
+@pytest.mark.parametrize("name", list(MEASURED_BEST))
+def test_plan_picks_the_measured_fastest_tile(lib, name):
+    w = W.WORKLOADS[name]
+    dt = G.make_dtypes(w.ab, w.c or "f32", w.d, w.x or "f32", w.y or "f32",
+                       G.GEMM_MN_MAJOR if w.cd_m_major else G.GEMM_K_MAJOR, b=w.b,
+                       epilogue=G.GEMM_EPI_RELU if w.relu else G.GEMM_EPI_LINEAR, acc=w.acc)
+    p = _p(M=w.M, N=w.N, K=w.K, L=w.L, lda=w.M if w.a_mn_major else w.K,
+           ldb=w.N if w.b_mn_major else w.K, layoutA=int(w.a_mn_major),
+           layoutB=int(w.b_mn_major), alpha=w.alpha, beta=w.beta, x_factor=w.x_factor,
+           dtypes=dt, C=C16 if w.c else None, X=(5 << 20) if w.x else None,
+           Y=(6 << 20) if w.y else None)
+    st, cfg = G.gemm_plan(p, 152, 232448)
+    assert st == 0 and (cfg.cta_group, cfg.tile_n) == MEASURED_BEST[name]
 
 
 def test_plan_group_m_default_and_clamp(lib):

@@ -26,10 +26,10 @@ g = G.Gemm(0)
 cases = [
     (Case(M=720, N=704, K=400, L=2, ab="bf16", c="f16", d="f32", x="bf16", y="f16",
           a_mn=True, b_mn=True, alpha=-0.75, beta=1.0, xf=0.5, seed=31),
-     [None, (2, 256, 1, 2), (2, 256, 2, 2), (1, 128, 2, 1), (2, 192, 1, 1), (1, 64, 1, 1)]),
+     [None, (2, 256, 1, 2), (2, 256, 2, 2), (1, 128, 2, 1), (2, 128, 1, 1), (1, 64, 1, 1)]),
     (Case(M=300, N=504, K=272, L=1, ab="e4m3", c="f16", d="f16", alpha=0.25, beta=1.0,
           dist="e4m3_pm4", seed=4),
-     [None, (2, 224, 1, 1), (1, 160, 1, 1), (2, 96, 2, 1)]),
+     [None, (2, 224, 1, 1), (1, 160, 1, 1), (2, 96, 2, 1), (2, 192, 1, 1)]),
     (Case(M=2560, N=1920, K=192, L=1, ab="f16", c="f16", d="f16", x="bf16", y="f16",
           alpha=1.0, beta=-0.5, xf=2.0, seed=77),                 # split last wave
      [(2, 192, 1, 1), (2, 256, 1, 1)]),
