@@ -49,8 +49,8 @@ constexpr int kMaxEpiSlots = 6;
 constexpr int kDefaultL2Hints = 2 | (2 << 2) | (2 << 4);
 constexpr int kDefaultEpiWaitNs = 0;
 // base alignment + abort flag + watchdog-test barrier + the epilogue warps'
-// ring-batch barriers
-constexpr int kSmemSlack = 1024 + 16 + 32;
+// ring-batch barriers (one per warp and chunk of a tile)
+constexpr int kSmemSlack = 1024 + 16 + 8 * 4 * gb300::kMaxChunks;
 
 struct VariantState {
   bool smem_attr_set = false;  // max dynamic smem attribute raised to the opt-in limit

@@ -145,6 +145,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kEpiChunk = 32;          // columns per epilogue chunk
 constexpr int kEpiLeader = 64;         // epilogue thread that records the ring statistics
 constexpr int kSubRows = 32;           // rows of one epilogue warp's sub-tiles
+constexpr int kMaxChunks = 8;          // 32-column epilogue chunks of the widest tile
 
 constexpr uint32_t kAccStride = 256;   // tensor-memory columns between accumulator stages
 
@@ -473,7 +474,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 
   // [B ring][A ring][epilogue slots][full x S][empty x S][tfull x 2][tempty x 2]
   // [cfull x 4E (per epilogue warp and slot)][tmem address][abort flag][never]
-  // [rfull x 4 (per epilogue warp)]  ("never": a barrier nothing
+  // [rfull x 4 x 8 (per epilogue warp and chunk)]  ("never": a barrier nothing
   // arrives at, waited on only when a stall is injected to test the watchdog)
   const uint32_t b_ring = base;
   const uint32_t a_ring = b_ring + S * T.b_stage;
@@ -486,7 +487,8 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   volatile uint32_t* const holder_ptr = reinterpret_cast<volatile uint32_t*>(gbase + (holder - base));
   volatile uint32_t* const abort_ptr = holder_ptr + 1;
   const uint32_t never_bar = holder + 8u;
-  const uint32_t rfull0 = never_bar + 8u;           // a ring-batch barrier per epilogue warp
+  // a ring-batch barrier per epilogue warp and chunk of a tile
+  const uint32_t rfull0 = never_bar + 8u;
   const uint32_t ring_bytes = (uint32_t)S * ((uint32_t)G::A_STAGE + (uint32_t)T.b_stage);
 
   if (threadIdx.x == 0) {
@@ -500,7 +502,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     }
     for (int s = 0; s < 4 * E; ++s) mbar_init(cfull0 + 8u * s, 1);
     mbar_init(never_bar, 1);
-    for (int q = 0; q < 4; ++q) mbar_init(rfull0 + 8u * q, 1);
+    for (int q = 0; q < 4 * kMaxChunks; ++q) mbar_init(rfull0 + 8u * q, 1);
     *abort_ptr = 0u;
     fence_barrier_init();
     if (p.k_blocks > 0) {                    // A and B are encoded only when K > 0
@@ -811,14 +813,15 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       if (loads && it + num_clusters >= p.num_items) {
         if (lead && ld.it == it && (uint32_t)(nchunks - ld.j) * 4u * sub <= ring_bytes) {
           batch0 = ld.j;
-          mbar_arrive_expect_tx(rfull0 + 8u * q, (uint32_t)(nchunks - batch0) * load_tx);
           for (int c = 0; c < nchunks - batch0; ++c) {
             int x0, x1;
             cursor_xy(ld, x0, x1);
             const uint32_t dst = b_ring + (uint32_t)(c * 4 + q) * sub;
+            const uint32_t rb = rfull0 + 8u * (uint32_t)(q * kMaxChunks + c);
             if (!dbg_check(load_ok(dst, x0), kChkEpiLoad, w)) break;
-            if (e.read_c) tma_load_3d(dst, &tmC, rfull0 + 8u * q, x0, x1, ld.tl, pol_in);
-            if (e.read_x) tma_load_3d(dst + cd_sub, &tmX, rfull0 + 8u * q, x0, x1, ld.tl, pol_in);
+            mbar_arrive_expect_tx(rb, load_tx);
+            if (e.read_c) tma_load_3d(dst, &tmC, rb, x0, x1, ld.tl, pol_in);
+            if (e.read_x) tma_load_3d(dst + cd_sub, &tmX, rb, x0, x1, ld.tl, pol_in);
             cursor_next(ld);
           }
           ld.it = p.num_items;               // the cursor has nothing left to load
@@ -850,7 +853,8 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                              kChkEpiSmem, w);
         const long long t_c = stat_clock();
         if (loads && got)
-          got = from_ring ? wait_phase<true>(rfull0 + 8u * q, 0u, w, kWaitEpiLoad)
+          got = from_ring ? wait_phase<true>(rfull0 + 8u * (uint32_t)(q * kMaxChunks + j - batch0),
+                                             0u, w, kWaitEpiLoad)
                           : wait_phase<true>(bar0 + 8u * slot_idx, slot_ph, w, kWaitEpiLoad);
         long long t_r = 0;
         if constexpr (kRingStats) { t_r = clock64(); st_cfull += t_r - t_c; }
@@ -956,7 +960,9 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       }
       if (++acc == kAccStages) { acc = 0; aph ^= 1u; }
     }
-    if (lead) bulk_wait_group_all();
+    // The stores must have read their shared memory before the CTA exits; their
+    // writes to global memory complete with the grid.
+    if (lead) bulk_wait_group_read<0>();
     if constexpr (kRingStats) {
       if (threadIdx.x == kEpiLeader && p.stats) {
         unsigned long long* const o = p.stats + (size_t)blockIdx.x * kStatWords;
