@@ -51,7 +51,20 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--config", default="",
+                    help="force a kernel configuration for the benchmark workload, e.g. "
+                         "cta_group=2,tile_n=256,cluster_n=2 (gemm_config_t fields; for "
+                         "profiling and comparisons: the default is the planner's choice)")
     return ap.parse_args()
+
+
+def parse_config(text: str) -> dict:
+    """'k=v,k=v' -> {k: int(v)} (gemm_config_t fields)."""
+    out = {}
+    for kv in filter(None, (t.strip() for t in text.split(","))):
+        k, v = kv.split("=")
+        out[k.strip()] = int(v, 0)
+    return out
 
 
 def load_peaks():
@@ -478,6 +491,9 @@ def main():
     w = W.WORKLOADS[args.workload]
     inp = W.make_inputs(w)
     g = G.Gemm(device)
+    forced = parse_config(args.config)
+    if forced:
+        g.set_config(G.gemm_config_t(**forced))
     bound = Bound(G, g, w, inp, device)
     stream = torch.cuda.current_stream()
 
@@ -600,6 +616,8 @@ def main():
 
     per_config = None
     cpu_baseline = None
+    if forced:
+        g.set_config(None)                   # the per-config table uses the planner's choices
     if rank == 0:
         if not args.no_per_config:
             per_config = {}
@@ -682,7 +700,9 @@ def main():
                        "epilogue": (f"Y=AB, D=relu({w.alpha}*AB+{w.beta}*C)+{w.x_factor}*X"
                                     if w.relu else
                                     f"Y=AB, D={w.alpha}*AB+{w.beta}*C+{w.x_factor}*X"),
+                       "forced_config": forced or None,
                        "kernel": {"cta_group": cfg.cta_group, "tile": f"{cfg.tile_m}x{cfg.tile_n}",
+                                  "cluster": f"{cfg.cluster_m}x{cfg.cluster_n}",
                                   "tile_k": cfg.tile_k, "stages": cfg.stages,
                                   "grid_ctas": cfg.grid_ctas, "group_m": cfg.group_m},
                        "l2": "no flush: inputs larger than L2 "

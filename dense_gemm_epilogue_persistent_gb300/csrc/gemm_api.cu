@@ -409,11 +409,13 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
       return GEMM_ERR_UNSUPPORTED_CONFIG;
   }
 
-  // Strips of 12 tile rows: with the serpentine strip order and the K
-  // direction alternating per wave, 8192^3 reads 1.206 GB from DRAM per launch
-  // at 12 (1.235 GB at 8, 1.514 GB at 4, 1.307 GB at 16) and runs 0.5-0.8 %
-  // faster than at 8; other shapes measured the same at 8 and 12.
-  int group_m = forced && forced->group_m ? forced->group_m : 12;
+  // Strips of 12 CTA-group tile rows: with the serpentine strip order and the
+  // K direction alternating per wave, 8192^3 reads 1.206 GB from DRAM per
+  // launch at 12 (1.235 GB at 8, 1.514 GB at 4, 1.307 GB at 16) and runs 0.5-0.8 %
+  // faster than at 8; other shapes measured the same at 8 and 12.  A cluster
+  // tile stacks cluster_m group tiles, so the strip counts 12 / cluster_m of
+  // them (B shared along M, 8192^3: 1.29 GB read at 6 against 1.58 GB at 12).
+  int group_m = forced && forced->group_m ? forced->group_m : std::max(1, 12 / mc);
   group_m = (int)std::max<int64_t>(1, std::min<int64_t>(group_m, tiles_m));
 
   gemm_config_t c{};

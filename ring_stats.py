@@ -43,14 +43,17 @@ def _device_inputs(G, W, w, torch):
     return A, B, C, X, D, Y, dt
 
 
-def measure(names, launches=30):
-    """Run each workload `launches` times with the statistics library; return
-    one summary dict per workload."""
+def measure(names, launches=30, config=None):
+    """Run each workload `launches` times with the statistics library (and a
+    forced configuration, if given: gemm_config_t fields); return one summary
+    dict per workload."""
     import dense_gemm_epilogue_persistent_gb300 as G
     G.select_library(_build.build(ring_stats=True))
     import torch
     import workloads as W
     g = G.Gemm(0)
+    if config:
+        g.set_config(G.gemm_config_t(**config))
     out = []
     try:
         for name in names:
@@ -110,8 +113,13 @@ def main(argv=None):
     ap.add_argument("workloads", nargs="*", default=["efc8192_f16"])
     ap.add_argument("--launches", type=int, default=30)
     ap.add_argument("--json", action="store_true")
+    ap.add_argument("--config", default="", help="forced configuration, e.g. cta_group=2,tile_n=256")
     args = ap.parse_args(argv)
-    res = measure(args.workloads, args.launches)
+    config = {}
+    for kv in filter(None, args.config.split(",")):
+        k, v = kv.split("=")
+        config[k] = int(v, 0)
+    res = measure(args.workloads, args.launches, config)
     for r in res:
         print(json.dumps(r) if args.json else
               f"{r['workload']}: {r['kernel']}  {r['tflops_with_counters']} TFLOP/s | MMA waits: "

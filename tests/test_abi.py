@@ -418,3 +418,13 @@ def test_debug_library_builds_and_maps_device_checks():
     for name in _header_symbols():
         assert hasattr(lib, name), name
     assert G.gemm_status_string(G.GEMM_ERR_DEVICE_CHECK) == "GEMM_ERR_DEVICE_CHECK"
+
+
+def test_nvtx_ranges_compiled_in(lib):
+    """The entry points open NVTX ranges in the gemm_gb300 domain (their names
+    are in the library, and the NVTX entry points it resolves at run time)."""
+    data = open(G.LIB_PATH, "rb").read()
+    for name in (b"gemm_gb300", b"gemm_run", b"gemm_run_host", b"gemm_run_noalloc",
+                 b"gemm_run:plan_and_encode"):
+        assert name + b"\0" in data, name
+    assert b"NVTX_INJECTION64_PATH" in data
