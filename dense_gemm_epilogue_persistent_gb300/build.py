@@ -24,8 +24,9 @@ neither a GPU nor libcuda):
                            range, reported as GEMM_ERR_DEVICE_CHECK; built
                            only on request.
 
-Each kernel unit is compiled once per input width (and, for kern_shared.cu,
-per cluster shape) with -D flags, so the units compile in parallel.
+Each kernel unit is compiled once per input width (and per epilogue warp
+count for kern_plain.cu, per cluster shape for kern_shared.cu) with -D flags,
+so the units compile in parallel.
 """
 from __future__ import annotations
 
@@ -54,8 +55,10 @@ DEBUG_LIB = LIBS["debug"]
 EXTRA_DEFINES = {"stats": ["-DGB300_RING_STATS=1"], "debug": ["-DGB300_DEBUG=1"]}
 
 # (object name, source, -D flags).  Input widths: 2 bytes (fp16/bf16), 1 (fp8),
-# 4 (tf32); operand-sharing cluster shapes (groups along M, along N).
-PLAIN_UNITS = [(f"kern_plain_ab{ab}", "kern_plain.cu", [f"-DGB300_AB={ab}"]) for ab in (2, 1, 4)]
+# 4 (tf32); epilogue warps per tensor-memory lane quarter (1 or 2);
+# operand-sharing cluster shapes (groups along M, along N).
+PLAIN_UNITS = [(f"kern_plain_ab{ab}_e{epw}", "kern_plain.cu", [f"-DGB300_AB={ab}", f"-DGB300_EPW={epw}"])
+               for ab in (2, 1, 4) for epw in (1, 2)]
 SHARED_UNITS = [(f"kern_shared_ab{ab}_m{mc}_n{nc}", "kern_shared.cu",
                  [f"-DGB300_AB={ab}", f"-DGB300_MC={mc}", f"-DGB300_NC={nc}"])
                 for ab in (2, 1, 4) for mc, nc in ((2, 1), (1, 2), (2, 2))]

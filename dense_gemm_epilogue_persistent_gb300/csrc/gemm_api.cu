@@ -50,7 +50,7 @@ constexpr int kDefaultL2Hints = 2 | (2 << 2) | (2 << 4);
 constexpr int kDefaultEpiWaitNs = 0;
 // base alignment + abort flag + watchdog-test barrier + the epilogue warps'
 // ring-batch barriers (one per warp and chunk of a tile)
-constexpr int kSmemSlack = 1024 + 16 + 8 * 4 * gb300::kMaxChunks;
+constexpr int kSmemSlack = 1024 + 16 + 8 * gb300::kMaxEpiWarps * gb300::kMaxChunks;
 
 struct VariantState {
   bool smem_attr_set = false;  // max dynamic smem attribute raised to the opt-in limit
@@ -115,7 +115,7 @@ struct gemm_handle {
   gemm_config_t forced_cfg{};
   gemm_config_t last{};
   uint64_t timeout_ns = kDefaultTimeoutNs;
-  VariantState variants[3][2][2][2][2];   // [ab 16/8/32][cta_group][k atoms][mc][nc]
+  VariantState variants[3][2][2][2][2][2];   // [ab 16/8/32][cta_group][k atoms][mc][nc][epw]
   int clusters_by_size[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};   // resident clusters of 1, 2, 4, 8 CTAs
   uint64_t config_gen = 0;
   LaunchEntry cache[kLaunchCacheEntries];
@@ -426,6 +426,8 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
   c.tile_m = 128 * cg;
   c.cluster_m = mc;
   c.cluster_n = nc;
+  c.epi_warps = forced && forced->epi_warps ? forced->epi_warps : 1;
+  if (c.epi_warps == 2 && csize != cg) return GEMM_ERR_UNSUPPORTED_CONFIG;
   c.l2_hints = forced && (forced->l2_hints & 0x100) ? (forced->l2_hints & 0x3F) : kDefaultL2Hints;
   c.epi_wait_ns = forced && forced->epi_wait_ns > 0 ? forced->epi_wait_ns - 1 : kDefaultEpiWaitNs;
   c.inject_stall = forced && forced->inject_stall ? 1 : 0;
@@ -549,15 +551,16 @@ gemm_status_t prepare_launch(gemm_handle* h, const gemm_problem_t& p, LaunchEntr
   const int ab_bytes = dtype_bytes(dtypes->ab);
   const int csize = cfg.cta_group * cfg.cluster_m * cfg.cluster_n;
   const int ka = gb300::k_atoms(cfg.cta_group, cfg.tile_n);
-  const void* kern =
-      gb300::kernel_for(ab_bytes, cfg.cta_group, ka, cfg.cluster_m, cfg.cluster_n);
+  const void* kern = gb300::kernel_for(ab_bytes, cfg.cta_group, ka, cfg.cluster_m,
+                                       cfg.cluster_n, cfg.epi_warps);
   if (!kern) return GEMM_ERR_UNSUPPORTED_CONFIG;
   VariantState& vs = h->variants[ab_bytes == 2 ? 0 : ab_bytes == 1 ? 1 : 2][cfg.cta_group - 1]
-                                [ka - 1][cfg.cluster_m - 1][cfg.cluster_n - 1];
+                                [ka - 1][cfg.cluster_m - 1][cfg.cluster_n - 1]
+                                [cfg.epi_warps - 1];
 
   cudaLaunchConfig_t lc{};
   cudaLaunchAttribute attr[1];
-  lc.blockDim = dim3(gb300::kThreads);
+  lc.blockDim = dim3(gb300::threads_for(cfg.epi_warps));
   lc.dynamicSmemBytes = (size_t)cfg.smem_bytes;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)csize;
@@ -839,7 +842,7 @@ GEMM_API gemm_status_t gemm_set_config(gemm_handle_t h, const gemm_config_t* cfg
       (cfg->cluster_m && cfg->cluster_m != 1 && cfg->cluster_m != 2) ||
       (cfg->cluster_n && cfg->cluster_n != 1 && cfg->cluster_n != 2) ||
       cfg->epi_slots < 0 || cfg->epi_slots > kMaxEpiSlots || cfg->epi_wait_ns < 0 ||
-      cfg->tail_split < 0 || cfg->tail_split > 1 ||
+      cfg->tail_split < 0 || cfg->tail_split > 1 || cfg->epi_warps < 0 || cfg->epi_warps > 2 ||
       cfg->epi_wait_ns > 1000001 ||
       cfg->stages > kMaxStages || cfg->group_m < 0)
     return GEMM_ERR_INVALID_ARG;
@@ -912,7 +915,7 @@ GEMM_API gemm_status_t gemm_run(gemm_handle_t h, int64_t M, int64_t N, int64_t K
   cudaLaunchConfig_t lc{};
   cudaLaunchAttribute attr[2];
   lc.gridDim = dim3((unsigned)ent->cfg.grid_ctas);
-  lc.blockDim = dim3(gb300::kThreads);
+  lc.blockDim = dim3(gb300::threads_for(ent->cfg.epi_warps));
   lc.dynamicSmemBytes = (size_t)ent->cfg.smem_bytes;
   lc.stream = reinterpret_cast<cudaStream_t>(stream);
   attr[0].id = cudaLaunchAttributeClusterDimension;

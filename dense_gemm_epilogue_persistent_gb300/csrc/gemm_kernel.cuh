@@ -16,21 +16,24 @@
 // follow the cuBLASDx "API Card: Blackwell Pipeline (tcgen05)", host-side and
 // "Depth and shared memory" bullets.
 //
-// Block = 6 warps:
+// Block = 6 warps (10 with EPW = 2):
 //   warp 0      TMA producer: one lane streams A and B k-blocks into a ring of
 //               `stages` shared-memory slots, each guarded by full/empty mbarriers.
 //   warp 1      tensor-memory allocator + MMA issuer: one lane of the leader CTA
 //               issues tcgen05.mma into one of two accumulator stages in tensor
 //               memory, frees ring slots with tcgen05.commit, and hands finished
 //               accumulators to the epilogue with another commit.
-//   warps 2..5  epilogue: warp w owns TMEM lanes 32*(w%4)..+31 (= tile rows).  The
-//               tile is processed in 32-column chunks through a ring of `slots`
-//               shared-memory slots: C and X sub-tiles are TMA-loaded `slots-1`
-//               chunks ahead (across tile boundaries, so the next tile's C/X arrive
-//               during its main loop) by one thread; each thread requests its
-//               accumulator columns, reads its C/X row while they load, computes
-//               in fp32, writes D and Y back into the slot, and a thread of another
-//               warp TMA-stores them.
+//   warps 2..   epilogue: warp w owns TMEM lanes 32*(w%4)..+31 (= 32 tile rows)
+//               and runs its own pipeline over them, in 32-column chunks through
+//               its share of the `slots` shared-memory slots: its lane 0
+//               TMA-loads the C and X sub-tiles ahead (across tile boundaries, so
+//               the next tile's C/X arrive during its main loop); each lane
+//               requests its accumulator columns, reads its C/X row while they
+//               load, computes in fp32 and writes D and Y back into the sub-slot,
+//               and lane 0 TMA-stores them.  With EPW = 2 two warps own each
+//               lane quarter and take its chunks alternately, so the per-chunk
+//               latency chain (accumulator load, shared-memory traffic, store
+//               issue) of one warp overlaps the other's.
 // Every cluster walks the same static persistent tile sequence
 // t = cluster_id, cluster_id + num_clusters, ...; with two accumulator stages the
 // epilogue of tile i overlaps the main loop of tile i+1.  Tiles are ordered in
@@ -139,13 +142,17 @@ __device__ __forceinline__ long long stat_clock() {
   else return 0;
 }
 
-constexpr int kThreads = 192;
+// Threads of a CTA: the TMA warp, the MMA warp and four (or eight, with two
+// epilogue warps per tensor-memory lane quarter) epilogue warps.
+constexpr int threads_for(int epi_warps_per_quarter) { return 64 + 128 * epi_warps_per_quarter; }
+constexpr int kThreads = threads_for(1);
 constexpr int kAccStages = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kEpiChunk = 32;          // columns per epilogue chunk
 constexpr int kEpiLeader = 64;         // epilogue thread that records the ring statistics
 constexpr int kSubRows = 32;           // rows of one epilogue warp's sub-tiles
 constexpr int kMaxChunks = 8;          // 32-column epilogue chunks of the widest tile
+constexpr int kMaxEpiWarps = 8;        // epilogue warps of the largest CTA
 
 constexpr uint32_t kAccStride = 256;   // tensor-memory columns between accumulator stages
 
@@ -415,8 +422,8 @@ __device__ __forceinline__ uint32_t sub_bytes(int dt) {
 
 // ------------------------------------------------------------------ the kernel
 
-template <int CG, int AB_BYTES, int KA, int MC, int NC>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int CG, int AB_BYTES, int KA, int MC, int NC, int EPW>
+__global__ void __launch_bounds__(threads_for(EPW), 1)
 persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmC,
@@ -474,7 +481,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 
   // [B ring][A ring][epilogue slots][full x S][empty x S][tfull x 2][tempty x 2]
   // [cfull x 4E (per epilogue warp and slot)][tmem address][abort flag][never]
-  // [rfull x 4 x 8 (per epilogue warp and chunk)]  ("never": a barrier nothing
+  // [rfull x 8 x 8 (per epilogue warp and chunk)]  ("never": a barrier nothing
   // arrives at, waited on only when a stall is injected to test the watchdog)
   const uint32_t b_ring = base;
   const uint32_t a_ring = b_ring + S * T.b_stage;
@@ -498,11 +505,11 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     }
     for (int a = 0; a < kAccStages; ++a) {
       mbar_init(tfull0 + 8u * a, 1);
-      mbar_init(tempty0 + 8u * a, 4 * CG);   // every epilogue warp of the CTA (pair)
+      mbar_init(tempty0 + 8u * a, 4 * EPW * CG);   // every epilogue warp of the CTA (pair)
     }
     for (int s = 0; s < 4 * E; ++s) mbar_init(cfull0 + 8u * s, 1);
     mbar_init(never_bar, 1);
-    for (int q = 0; q < 4 * kMaxChunks; ++q) mbar_init(rfull0 + 8u * q, 1);
+    for (int q = 0; q < kMaxEpiWarps * kMaxChunks; ++q) mbar_init(rfull0 + 8u * q, 1);
     *abort_ptr = 0u;
     fence_barrier_init();
     if (p.k_blocks > 0) {                    // A and B are encoded only when K > 0
@@ -700,43 +707,53 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   } else {
     // ---------------------------------------------------------- epilogue
     // Each epilogue warp runs its own pipeline over the 32 tile rows whose
-    // accumulator lanes it may read, through its own ring of `slots`
-    // shared-memory sub-slots (32 rows x 32 columns of C/D and of X/Y): lane 0
-    // TMA-loads the C/X sub-tiles E - 1 chunks ahead (across tile
-    // boundaries), every lane reads its row, computes D and Y and writes them
-    // back in place, and lane 0 TMA-stores them.  The four warps never wait on
-    // one another; they meet only in the accumulator stage's release count.
+    // accumulator lanes it may read, through its own ring of shared-memory
+    // sub-slots (32 rows x 32 columns of C/D and of X/Y): lane 0 TMA-loads the
+    // C/X sub-tiles ahead (across tile boundaries), every lane reads its row,
+    // computes D and Y and writes them back in place, and lane 0 TMA-stores
+    // them.  With EPW = 2 two warps share each lane quarter and take its
+    // chunks alternately (stream 0 the even, stream 1 the odd ones), each
+    // with half the sub-slots.  The warps never wait on one another; they
+    // meet only in the accumulator stage's release count.
     const int q = warp & 3;                 // TMEM lane quarter this warp may read
+    const int ew = warp - 2;                // epilogue warp index, 0 .. 4 * EPW - 1
+    const int strm = ew >> 2;               // which of the quarter's EPW chunk streams
     const bool lead = lane == 0;
     const bool loads = e.read_c || e.read_x;
     const uint32_t load_tx = (e.read_c ? sub_bytes(e.c_dt) : 0u) + (e.read_x ? sub_bytes(e.x_dt) : 0u);
     const uint32_t sub = slot_bytes / 4;               // one warp's share of a slot
     const uint32_t cd_sub = e.cd_bytes / 4;            // ... of which C/D
-    const uint32_t ring0 = epi0 + (uint32_t)(q * E) * sub;
-    const uint32_t bar0 = cfull0 + 8u * (uint32_t)(q * E);
+    // sub-slots of this warp: all E with one warp per quarter, else E / 2
+    const int Ew = EPW == 1 ? E : max(1, E / EPW);
+    const uint32_t ring0 = epi0 + (uint32_t)(ew * Ew) * sub;
+    const uint32_t bar0 = cfull0 + 8u * (uint32_t)(ew * Ew);
     const uint64_t pol_in = make_l2_policy((p.l2_hints >> 2) & 3u);
     const uint64_t pol_out = make_l2_policy((p.l2_hints >> 4) & 3u);
 
-    // Lane 0 walks this CTA's stream of chunks (BN / 32 per whole tile, half
-    // that per half-width item, in item order) with a cursor that issues the
-    // TMA loads of its rows' C/X into the warp's sub-slots.  The cursor
-    // computes an item's coordinates once, when it enters the item.  TMA
-    // coordinates are (column, row, batch) for row-major C/D/X/Y and (row,
-    // column, batch) for column-major ones.
+    // Lane 0 walks this warp's stream of chunks (of BN / 32 per whole tile,
+    // half that per half-width item, in item order: the chunks j = strm,
+    // strm + EPW, ...) with a cursor that issues the TMA loads of its rows'
+    // C/X into the warp's sub-slots.  The cursor computes an item's
+    // coordinates once, when it enters the item.  TMA coordinates are
+    // (column, row, batch) for row-major C/D/X/Y and (row, column, batch) for
+    // column-major ones.
     struct Cursor { int it, j, nch, row0, col0, tl; };
     auto cursor_enter = [&](Cursor& cc) {
-      if (cc.it >= p.num_items) return;
-      int half;
-      const int t = item_tile(cc.it, p, half);
-      int tm, tn;
-      tile_coords(t, p, tm, tn, cc.tl);
-      cc.nch = half < 0 ? T.chunks : T.chunks / 2;
-      cc.row0 = tm * G::CM + (int)gm * (G::BM * CG) + (int)rank * G::BM + q * kSubRows;
-      cc.col0 = tn * (BN * NC) + (int)gn * BN + (half > 0 ? BN / 2 : 0);
+      for (; cc.it < p.num_items; cc.it += num_clusters) {
+        int half;
+        const int t = item_tile(cc.it, p, half);
+        cc.nch = half < 0 ? T.chunks : T.chunks / 2;
+        if (strm >= cc.nch) continue;       // no chunk of this item in this stream
+        int tm, tn;
+        tile_coords(t, p, tm, tn, cc.tl);
+        cc.j = strm;
+        cc.row0 = tm * G::CM + (int)gm * (G::BM * CG) + (int)rank * G::BM + q * kSubRows;
+        cc.col0 = tn * (BN * NC) + (int)gn * BN + (half > 0 ? BN / 2 : 0);
+        return;
+      }
     };
     auto cursor_next = [&](Cursor& cc) {
-      if (cc.it < p.num_items && ++cc.j == cc.nch) {
-        cc.j = 0;
+      if (cc.it < p.num_items && (cc.j += EPW) >= cc.nch) {
         cc.it += num_clusters;
         cursor_enter(cc);
       }
@@ -751,7 +768,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     const uint32_t slots_end = epi0 + (uint32_t)E * slot_bytes;
     auto inner_ok = [&](int x, int dt) { return ((long long)x * (dt == DT_F32 ? 4 : 2)) % 16 == 0; };
     auto load_ok = [&](uint32_t dst, int x0) {
-      const bool in_slots = in_range(dst, sub, ring0, ring0 + (uint32_t)E * sub) &&
+      const bool in_slots = in_range(dst, sub, ring0, ring0 + (uint32_t)Ew * sub) &&
                             dst + sub <= slots_end;
       const bool in_ring = in_range(dst, sub, b_ring, b_ring + ring_bytes);
       return (in_slots || in_ring) && (!e.read_c || inner_ok(x0, e.c_dt)) &&
@@ -771,21 +788,23 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           if (e.read_x) tma_load_3d(slot + cd_sub, &tmX, bar, x0, x1, ld.tl, pol_in);
         }
       }
-      if (++ld_slot == E) ld_slot = 0;
+      if (++ld_slot == Ew) ld_slot = 0;
       cursor_next(ld);
     };
 
+    // Loads run Ew - 1 chunks ahead (one sub-slot: the next chunk's load is
+    // issued once the current chunk's store has read the sub-slot).
     if (lead && loads) {
       cursor_enter(ld);
-      for (int c = 0; c < E - 1; ++c) issue_loads();
+      for (int c = 0; c < max(1, Ew - 1); ++c) issue_loads();
     }
     __syncwarp();
 
     int acc = 0;
     uint32_t aph = 0;
-    int gc = 0;                             // chunk counter of this CTA's stream
-    int slot_idx = 0;                       // gc % E
-    uint32_t slot_ph = 0;                   // (gc / E) & 1: phase of the slot's cfull barrier
+    int gc = 0;                             // chunk counter of this warp's stream
+    int slot_idx = 0;                       // gc % Ew
+    uint32_t slot_ph = 0;                   // (gc / Ew) & 1: phase of the slot's cfull barrier
     bool ok = true;
     long long st_tfull = 0, st_cfull = 0, st_read = 0, st_math = 0, st_issue = 0;
     const long long st_t0 = stat_clock();
@@ -802,6 +821,22 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       ok = __all_sync(0xFFFFFFFFu, ready);
       if (!ok) break;
       tc_fence_after_sync();
+      // The accumulator stage is handed back to the MMA warp after this
+      // warp's last chunk of the item; a warp with no chunk in the item does
+      // so at once.
+      auto release_acc = [&]() {
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lead) {
+          if constexpr (CG == 1) mbar_arrive(tempty0 + 8u * acc);
+          else mbar_arrive_cluster(map_to_rank(tempty0 + 8u * acc, pair_leader));
+        }
+      };
+      if (strm >= nchunks) {
+        release_acc();
+        if (++acc == kAccStages) { acc = 0; aph ^= 1u; }
+        continue;
+      }
       // This CTA's last item: once its accumulator is ready the operand ring
       // has been drained for good (no main loop follows), so the C/X chunks
       // the lookahead has not loaded yet all go into the ring at once, and
@@ -811,13 +846,14 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       // Only lane 0 keeps the cursor; it decides and tells the warp.
       int batch0 = nchunks;
       if (loads && it + num_clusters >= p.num_items) {
-        if (lead && ld.it == it && (uint32_t)(nchunks - ld.j) * 4u * sub <= ring_bytes) {
+        const int nb = ld.it == it ? (nchunks - ld.j + EPW - 1) / EPW : 0;   // this warp's
+        if (lead && nb > 0 && (uint32_t)nb * (4u * EPW) * sub <= ring_bytes) {
           batch0 = ld.j;
-          for (int c = 0; c < nchunks - batch0; ++c) {
+          for (int c = 0; c < nb; ++c) {
             int x0, x1;
             cursor_xy(ld, x0, x1);
-            const uint32_t dst = b_ring + (uint32_t)(c * 4 + q) * sub;
-            const uint32_t rb = rfull0 + 8u * (uint32_t)(q * kMaxChunks + c);
+            const uint32_t dst = b_ring + (uint32_t)(c * 4 * EPW + ew) * sub;
+            const uint32_t rb = rfull0 + 8u * (uint32_t)(ew * kMaxChunks + c);
             if (!dbg_check(load_ok(dst, x0), kChkEpiLoad, w)) break;
             mbar_arrive_expect_tx(rb, load_tx);
             if (e.read_c) tma_load_3d(dst, &tmC, rb, x0, x1, ld.tl, pol_in);
@@ -831,7 +867,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       const int row0 = tm * G::CM + (int)gm * (G::BM * CG) + (int)rank * G::BM + q * kSubRows;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * kAccStride;
 #pragma unroll 1
-      for (int j = 0; j < nchunks; ++j, ++gc) {
+      for (int j = strm; j < nchunks; j += EPW, ++gc) {
         // The accumulator columns are requested first: their latency overlaps
         // the wait for C/X and the shared-memory reads below.
         uint32_t raw_acc[32];
@@ -843,18 +879,19 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         else
           for (int i = 0; i < 32; ++i) raw_acc[i] = 0u;
         const bool from_ring = j >= batch0;
-        const uint32_t s_addr = from_ring ? b_ring + (uint32_t)((j - batch0) * 4 + q) * sub
+        const int bc = (j - batch0) / EPW;  // index in this warp's ring batch
+        const uint32_t s_addr = from_ring ? b_ring + (uint32_t)(bc * 4 * EPW + ew) * sub
                                           : ring0 + (uint32_t)slot_idx * sub;
         uint8_t* const slot = gbase + (s_addr - base);
         float cv[kEpiChunk], xv[kEpiChunk];
         bool got = dbg_check(from_ring ? in_range(s_addr, sub, b_ring, b_ring + ring_bytes)
-                                       : in_range(s_addr, sub, ring0, ring0 + (uint32_t)E * sub) &&
+                                       : in_range(s_addr, sub, ring0, ring0 + (uint32_t)Ew * sub) &&
                                              s_addr + sub <= slots_end,
                              kChkEpiSmem, w);
         const long long t_c = stat_clock();
         if (loads && got)
-          got = from_ring ? wait_phase<true>(rfull0 + 8u * (uint32_t)(q * kMaxChunks + j - batch0),
-                                             0u, w, kWaitEpiLoad)
+          got = from_ring ? wait_phase<true>(rfull0 + 8u * (uint32_t)(ew * kMaxChunks + bc), 0u, w,
+                                             kWaitEpiLoad)
                           : wait_phase<true>(bar0 + 8u * slot_idx, slot_ph, w, kWaitEpiLoad);
         long long t_r = 0;
         if constexpr (kRingStats) { t_r = clock64(); st_cfull += t_r - t_c; }
@@ -878,15 +915,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           for (int i = 0; i < 32; ++i)
             raw_acc[i] = __float_as_uint(__half2float(__ushort_as_half((uint16_t)raw_acc[i])));
         }
-        if (j == nchunks - 1) {
-          // The whole accumulator stage has been read: hand it back to the MMA warp.
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lead) {
-            if constexpr (CG == 1) mbar_arrive(tempty0 + 8u * acc);
-            else mbar_arrive_cluster(map_to_rank(tempty0 + 8u * acc, pair_leader));
-          }
-        }
+        if (j + EPW >= nchunks) release_acc();   // this warp's last chunk of the stage
         ok = got;
         if (!ok) break;
         long long t_m = 0;
@@ -895,7 +924,10 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         // the load that filled it was issued after that), and every lane has
         // read its C/X row before any lane overwrites the sub-slot (a narrower
         // D packs rows differently from a wider C).
-        if (lead && !loads) bulk_wait_group_read<1>();
+        if (lead && !loads) {
+          if (Ew >= 2) bulk_wait_group_read<1>();
+          else bulk_wait_group_read<0>();
+        }
         __syncwarp();
         // D from the accumulator, C (zero when not read) and X; the branches
         // are uniform and outside the element loops.
@@ -946,15 +978,19 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           }
           bulk_commit_group();
           if (loads) {
-            // C/X of chunk gc+E-1 go into the sub-slot of chunk gc-1, once its
-            // store (the one before the store just issued) has read it; with
-            // nothing left to load (the drained-ring batch has the rest) no
-            // store is waited for.
-            if (ld.it < p.num_items) bulk_wait_group_read<1>();
+            // C/X of chunk gc+Ew-1 go into the sub-slot of chunk gc-1, once its
+            // store (the one before the store just issued) has read it (with
+            // one sub-slot: chunk gc+1 into chunk gc's, once its store has);
+            // with nothing left to load (the drained-ring batch has the rest)
+            // no store is waited for.
+            if (ld.it < p.num_items) {
+              if (Ew >= 2) bulk_wait_group_read<1>();
+              else bulk_wait_group_read<0>();
+            }
             issue_loads();
           }
         }
-        if (++slot_idx == E) { slot_idx = 0; slot_ph ^= 1u; }
+        if (++slot_idx == Ew) { slot_idx = 0; slot_ph ^= 1u; }
         __syncwarp();
         if constexpr (kRingStats) st_issue += clock64() - t_i;
       }

@@ -126,6 +126,12 @@ typedef struct {
  *               processes that drive several GPUs (libgemm_gb300_nomc.so)
  *               returns GEMM_ERR_UNSUPPORTED_CONFIG for them.
  *   epi_slots   (also an input) epilogue slots, 2..6 (0 = automatic).
+ *   epi_warps   (after cluster_n; also an input) epilogue warps per 32-lane
+ *               quarter of the tensor-memory accumulator: 1 (4 epilogue warps,
+ *               192 threads a CTA) or 2 (8 warps, 320 threads; the two warps
+ *               of a quarter take its 32-column chunks alternately, each with
+ *               half the epilogue slots; clusters of one CTA group only).
+ *               0 = automatic.
  *   Fields marked "diagnostic" are for tuning and testing the kernel, not
  *   part of the GEMM contract; leave them 0.
  *   l2_hints    (diagnostic; also an input) L2 eviction priority of the TMA
@@ -173,6 +179,7 @@ typedef struct {
   int inject_stall;
   int tail_split;
   int cluster_n;
+  int epi_warps;
 } gemm_config_t;
 
 /* Every argument of one gemm_run call, for the host-only planning calls. */

@@ -351,6 +351,22 @@ def test_plan_clusters_sharing_a(lib):
     assert st == 0
 
 
+def test_plan_epilogue_warps(lib):
+    """Eight epilogue warps (two per accumulator lane quarter) only when
+    forced, and only for clusters of one CTA group; out-of-range values are
+    rejected by gemm_set_config's checks."""
+    p = _p(M=4096, N=4096, K=4096, lda=4096, ldb=4096, dtypes=G.make_dtypes("f16", "f16", "f16"))
+    st, cfg = G.gemm_plan(p, 152, 232448)
+    assert st == 0 and cfg.epi_warps == 1
+    for cg, bn in ((1, 128), (2, 256), (1, 96)):
+        st, cfg = G.gemm_plan(p, 152, 232448, G.gemm_config_t(cta_group=cg, tile_n=bn, epi_warps=2))
+        assert st == 0 and cfg.epi_warps == 2 and cfg.epi_slots >= 2
+    for cm, cn in ((2, 1), (1, 2)):
+        st, _ = G.gemm_plan(p, 152, 232448, G.gemm_config_t(cta_group=2, tile_n=256, cluster_m=cm,
+                                                            cluster_n=cn, epi_warps=2))
+        assert st == G.GEMM_ERR_UNSUPPORTED_CONFIG
+
+
 def _includes(path, seen):
     """Every in-tree file `path` includes, transitively."""
     import re

@@ -17,17 +17,21 @@ from gemm_cases import (Case, assert_within, compare_full, compare_sampled, logi
 
 pytestmark = pytest.mark.gpu
 
-# (cta_group, tile_n, cluster_m[, cluster_n]): single CTAs and CTA pairs, 128-
-# and 256-wide tiles, alone and in clusters whose groups share B (stacked
-# along M) or A (side by side along N) through TMA multicast.
+# (cta_group, tile_n, cluster_m[, cluster_n[, epi_warps]]): single CTAs and CTA
+# pairs, 128- and 256-wide tiles, alone and in clusters whose groups share B
+# (stacked along M) or A (side by side along N) through TMA multicast, and
+# with two epilogue warps per accumulator lane quarter.
 VARIANTS = [(1, 128, 1), (1, 256, 1), (2, 128, 1), (2, 256, 1),
             (1, 128, 2), (1, 256, 2), (2, 128, 2), (2, 256, 2),
-            (1, 128, 1, 2), (2, 256, 1, 2), (2, 192, 1, 2), (2, 256, 2, 2)]
-# The other tile widths (multiples of 32 from 64 to 256), alone and in a few
-# cluster shapes.
+            (1, 128, 1, 2), (2, 256, 1, 2), (2, 192, 1, 2), (2, 256, 2, 2),
+            (1, 128, 1, 1, 2), (2, 256, 1, 1, 2)]
+# The other tile widths (multiples of 32 from 64 to 256), alone, in a few
+# cluster shapes and with two epilogue warps per lane quarter (odd chunk
+# counts: 96 and 224 wide tiles have 3 and 7 chunks).
 WIDTH_VARIANTS = [(1, 64, 1), (1, 96, 1), (1, 160, 1), (1, 192, 1), (1, 224, 1),
                   (2, 64, 1), (2, 96, 1), (2, 160, 1), (2, 192, 1), (2, 224, 1),
-                  (1, 96, 2), (2, 160, 2), (1, 224, 1, 2), (1, 64, 2, 2)]
+                  (1, 96, 2), (2, 160, 2), (1, 224, 1, 2), (1, 64, 2, 2),
+                  (1, 96, 1, 1, 2), (2, 64, 1, 1, 2), (1, 224, 1, 1, 2), (2, 160, 1, 1, 2)]
 
 
 def stageable(case, variant):
@@ -53,8 +57,9 @@ def gemm():
     g.close()
 
 
-def _force(gemm, cg, bn, mc=1, nc=1, stages=0):
-    gemm.set_config(cta_group=cg, tile_n=bn, cluster_m=mc, cluster_n=nc, stages=stages)
+def _force(gemm, cg, bn, mc=1, nc=1, epw=0, stages=0, slots=0):
+    gemm.set_config(cta_group=cg, tile_n=bn, cluster_m=mc, cluster_n=nc, epi_warps=epw,
+                    stages=stages, epi_slots=slots)
 
 
 def _finish(gemm):
@@ -208,6 +213,45 @@ def test_shared_operand_layouts(gemm, variant, ab, a_mn, b_mn):
     gemm.set_config(None)
 
 
+# ------------------------------------------------------- two epilogue warps per lane quarter
+
+@pytest.mark.parametrize("cg,bn", [(1, 128), (2, 256), (1, 224)])
+@pytest.mark.parametrize("slots", [2, 3, 4, 6])
+@pytest.mark.parametrize("loads", [True, False])
+def test_two_epilogue_warps_per_quarter(gemm, cg, bn, slots, loads):
+    """Eight epilogue warps, the two of each lane quarter taking alternate
+    32-column chunks with half the slots each (one slot each at 2 and 3
+    slots: loads wait for the previous store), over many tiles per CTA; with
+    and without C/X loads.  All outputs against the oracle."""
+    case = Case(M=4608, N=2080, K=96, L=1, ab="bf16", c="f16" if loads else None, d="f16",
+                x="bf16" if loads else None, y="f16", alpha=1.5, beta=-0.5 if loads else 0.0,
+                xf=2.0 if loads else 0.0, seed=slots * 7 + bn + cg)
+    _force(gemm, cg, bn, 1, 1, 2, 2 if slots > 2 else 0, slots)   # short ring: room for slots
+    prep = prepare(case)
+    try:
+        D, Y = run_gpu(gemm, prep)
+    except G.GemmError:
+        gemm.set_config(None)
+        pytest.skip("that many slots do not fit beside the ring")
+    _finish(gemm)
+    cfg = gemm.last_config()
+    assert (cfg.epi_warps, cfg.epi_slots, cfg.tile_n) == (2, slots, bn)
+    clusters = cfg.grid_ctas // cfg.cta_group
+    assert cfg.tiles >= 2 * clusters
+    compare_full(prep, D, Y)
+    gemm.set_config(None)
+
+
+def test_two_epilogue_warps_need_one_group_clusters(gemm):
+    """Two epilogue warps per quarter exist only for clusters of one CTA group."""
+    case = SMALL["efc_f16"]
+    prep = prepare(case)
+    gemm.set_config(cta_group=2, tile_n=256, cluster_m=2, epi_warps=2)
+    with pytest.raises(G.GemmError):
+        run_gpu(gemm, prep)
+    gemm.set_config(None)
+
+
 # ------------------------------------------------------------ split last wave
 
 @pytest.mark.parametrize("variant,shape", [
@@ -219,6 +263,9 @@ def test_shared_operand_layouts(gemm, variant, ab, a_mn, b_mn):
     ((2, 128, 1), (2048, 1408, 128)),
     ((2, 256, 1), (2500, 2552, 200)),      # ragged
     ((1, 256, 1), (2000, 2560, 136)),
+    ((1, 64, 1, 1, 2), (1280, 2048, 128)),    # half items of one chunk: one warp idle
+    ((2, 192, 1, 1, 2), (2560, 1920, 192)),   # half items of three chunks
+    ((2, 256, 1, 1, 2), (2500, 2552, 200)),
 ])
 def test_split_last_wave(gemm, variant, shape):
     """Tiles of the last, partial wave run as two half-width items each."""

@@ -16,12 +16,13 @@ pytestmark = pytest.mark.gpu
 AB = [("f16", None), ("bf16", None), ("e4m3", None), ("e5m2", None), ("e4m3", "e5m2"),
       ("e5m2", "e4m3"), ("tf32", None)]
 OUT = ["f32", "f16", "bf16"]
-# (cta_group, tile_n, cluster_m, cluster_n), None = automatic
+# (cta_group, tile_n, cluster_m, cluster_n[, epi_warps]), None = automatic
 VARIANTS = [None, (1, 128, 1, 1), (1, 256, 1, 1), (2, 128, 1, 1), (2, 256, 1, 1),
             (1, 128, 2, 1), (1, 256, 2, 1), (2, 128, 2, 1), (2, 256, 2, 1),
             (1, 64, 1, 1), (1, 96, 1, 1), (1, 160, 1, 1), (1, 192, 1, 1), (1, 224, 1, 1),
             (2, 64, 1, 1), (2, 96, 1, 1), (2, 160, 1, 1), (2, 192, 1, 1), (2, 224, 1, 1),
-            (1, 128, 1, 2), (2, 256, 1, 2), (2, 160, 1, 2), (1, 96, 2, 2), (2, 224, 2, 2)]
+            (1, 128, 1, 2), (2, 256, 1, 2), (2, 160, 1, 2), (1, 96, 2, 2), (2, 224, 2, 2),
+            (1, 128, 1, 1, 2), (2, 256, 1, 1, 2), (1, 96, 1, 1, 2), (2, 192, 1, 1, 2)]
 N_CASES = 80
 
 
@@ -89,8 +90,9 @@ def gemm():
 def test_random_problem(gemm, i):
     case, variant = draw_case(i)
     if variant:
-        cg, bn, mc, nc = variant
-        gemm.set_config(cta_group=cg, tile_n=bn, cluster_m=mc, cluster_n=nc)
+        cg, bn, mc, nc = variant[:4]
+        epw = variant[4] if len(variant) > 4 else 0
+        gemm.set_config(cta_group=cg, tile_n=bn, cluster_m=mc, cluster_n=nc, epi_warps=epw)
     else:
         gemm.set_config(None)
     prep = prepare(case)

@@ -14,10 +14,10 @@ from gemm_cases import Case, compare_full, prepare, run_gpu
 
 pytestmark = pytest.mark.gpu
 
-# (cta_group, tile_n, cluster_m, cluster_n): single CTAs, pairs, and clusters
-# sharing B, A or both through multicast
-VARIANTS = [(1, 256, 1, 1), (2, 256, 1, 1), (2, 256, 2, 1), (1, 128, 2, 1), (2, 256, 1, 2),
-            (2, 160, 2, 2)]
+# (cta_group, tile_n, cluster_m, cluster_n, epi_warps): single CTAs, pairs,
+# clusters sharing B, A or both through multicast, and eight epilogue warps
+VARIANTS = [(1, 256, 1, 1, 1), (2, 256, 1, 1, 1), (2, 256, 2, 1, 1), (1, 128, 2, 1, 1),
+            (2, 256, 1, 2, 1), (2, 160, 2, 2, 1), (1, 128, 1, 1, 2), (2, 256, 1, 1, 2)]
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
@@ -29,10 +29,10 @@ def test_injected_stall_times_out_cleanly_and_context_survives(variant):
         case = Case(M=1024, N=768, K=512, L=1, ab="f16", c="f16", d="f16", x="f16", y="f16",
                     alpha=1.0, beta=1.0, xf=1.0, seed=77)
         prep = prepare(case)
-        cg, bn, mc, nc = variant
+        cg, bn, mc, nc, epw = variant
         G.gemm_set_timeout_ns(g.handle, 50_000_000)           # 50 ms per wait
         g.set_config(G.gemm_config_t(cta_group=cg, tile_n=bn, cluster_m=mc, cluster_n=nc,
-                                     inject_stall=1))
+                                     epi_warps=epw, inject_stall=1))
         run_gpu(g, prep)
         st, detail = g.sync_status()
         assert st == G.GEMM_ERR_DEVICE_TIMEOUT
@@ -41,7 +41,8 @@ def test_injected_stall_times_out_cleanly_and_context_survives(variant):
         assert st == G.GEMM_OK and detail == 0
         # the same handle, stream and context run a normal GEMM correctly
         G.gemm_set_timeout_ns(g.handle, 0)
-        g.set_config(G.gemm_config_t(cta_group=cg, tile_n=bn, cluster_m=mc, cluster_n=nc))
+        g.set_config(G.gemm_config_t(cta_group=cg, tile_n=bn, cluster_m=mc, cluster_n=nc,
+                                     epi_warps=epw))
         D, Y = run_gpu(g, prep)
         st, detail = g.sync_status()
         assert st == G.GEMM_OK, hex(detail)
