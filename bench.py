@@ -113,7 +113,8 @@ def kernel_source_digest():
 
 def config_key(cfg) -> str:
     return (f"cg{cfg.cta_group}_n{cfg.tile_n}_mc{cfg.cluster_m}_nc{cfg.cluster_n}"
-            f"_k{cfg.tile_k}_st{cfg.stages}_e{cfg.epi_slots}_gm{cfg.group_m}_l2{cfg.l2_hints}")
+            f"_k{cfg.tile_k}_st{cfg.stages}_e{cfg.epi_slots}_w{cfg.epi_warps}_gm{cfg.group_m}"
+            f"_l2{cfg.l2_hints}")
 
 
 def recorded_traffic(workload: str, cfg):

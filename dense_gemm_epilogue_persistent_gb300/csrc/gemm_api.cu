@@ -286,24 +286,50 @@ bool variant_supports(const gemm_problem_t& p, int cg, int bn, int mc, int nc) {
 // Y; ragged and batched shapes): the pick is the measured fastest variant on
 // 10 of them and within 0.2 % on the eleventh.  (With per-warp epilogue
 // pipelines the number of C/X slots no longer changes the cost.)
-double plan_cost(int64_t tiles, int64_t k_blocks, int cg, int ka, int bn, int64_t clusters,
-                 double epi_kb, bool can_split) {
+//
+// Two epilogue warps per accumulator lane quarter (epw = 2) run two chunk
+// chains per quarter side by side: in a GB300 sweep of the same widths with
+// the two epilogues alternating, the 10-warp CTAs took 0.85-0.95 of the time
+// where the epilogue is the longer side or stands alone (fp8 with 16-bit C, X
+// and D; single-wave 2048^3 and 256^3) and 1.00-1.02 where the main loop
+// dominates (8192^3, tf32, fp16 accumulators, batched).  Modelled as the
+// epilogue x 0.55, the fixed part x 0.9 and the main loop x 1.015, offered
+// only where it pays (two_epilogue_warps_pay).
+struct TileCost {
+  double waves, main_loop, epilogue, fixed;
+};
+
+TileCost tile_cost(int64_t tiles, int64_t k_blocks, int cg, int ka, int bn, int64_t clusters,
+                   double epi_kb, bool can_split) {
   clusters = std::max<int64_t>(1, clusters);
   const int64_t full = tiles / clusters, rem = tiles % clusters;
-  const double waves =
-      (double)full + (rem == 0 ? 0.0 : (can_split && 2 * rem <= clusters ? 0.8 : 1.0));
+  TileCost t;
+  t.waves = (double)full + (rem == 0 ? 0.0 : (can_split && 2 * rem <= clusters ? 0.8 : 1.0));
   const double w = bn / 256.0;
-  double per_kb, fixed;
+  double per_kb;
   if (cg == 2) {
     per_kb = w + 0.22 * (256 - bn) / 128.0;
-    fixed = 15.0 - 1.9 * (bn - 128) / 128.0;
+    t.fixed = 15.0 - 1.9 * (bn - 128) / 128.0;
   } else {
     per_kb = ka == 1 ? 1.15 * w : w + 0.18 * (256 - bn) / 128.0;
-    fixed = 11.0 - 0.4 * (bn - 128) / 128.0;
+    t.fixed = 11.0 - 0.4 * (bn - 128) / 128.0;
   }
-  const double main_loop = (double)k_blocks * per_kb;
-  const double epilogue = (double)(bn / gb300::kEpiChunk) * (2.5 + 0.08 * epi_kb);
-  return waves * (std::max(main_loop, epilogue) + fixed);
+  t.main_loop = (double)k_blocks * per_kb;
+  t.epilogue = (double)(bn / gb300::kEpiChunk) * (2.5 + 0.08 * epi_kb);
+  return t;
+}
+
+// Whether the automatic choice offers two epilogue warps per lane quarter: the
+// tiles fit in one wave (each CTA's epilogue runs after its only main loop,
+// with nothing to hide it), or the epilogue is at least 0.8 of the main loop.
+bool two_epilogue_warps_pay(const TileCost& t, int64_t tiles, int64_t clusters) {
+  return tiles <= std::max<int64_t>(1, clusters) || t.epilogue >= 0.8 * t.main_loop;
+}
+
+double plan_cost(const TileCost& t, int epw) {
+  if (epw == 2)
+    return t.waves * (std::max(1.015 * t.main_loop, 0.55 * t.epilogue) + 0.9 * t.fixed);
+  return t.waves * (std::max(t.main_loop, t.epilogue) + t.fixed);
 }
 
 // Whether the last wave of a variant may run as half-width items: clusters of
@@ -338,7 +364,8 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
   const int fbn = forced ? forced->tile_n : 0;
   const int fmc = forced ? forced->cluster_m : 0;
   const int fnc = forced ? forced->cluster_n : 0;
-  int cg = 0, bn = 0, mc = 0, nc = 0;
+  const int fepw = forced ? forced->epi_warps : 0;
+  int cg = 0, bn = 0, mc = 0, nc = 0, epw = 0;
   double best = 1e300;
   // KB an epilogue chunk (128 x 32 elements of each tensor) moves per CTA.
   const double epi_kb =
@@ -369,10 +396,18 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
                                 cdiv(std::max<int64_t>(p.N, 1), (int64_t)b * n) *
                                 std::max<int64_t>(p.L, 1);
           const int64_t units = resident_clusters(sm_count, clusters_by_size, a * m * n);
-          const double c = plan_cost(tiles, cdiv(p.K, 128 / ab_bytes), a, ka, b, units, epi_kb,
-                                     can_split_tail(p, a, b, m, n) &&
-                                         !(forced && forced->tail_split == 1));
-          if (c < best - 1e-9) { best = c; cg = a; bn = b; mc = m; nc = n; }
+          const TileCost tc = tile_cost(tiles, cdiv(p.K, 128 / ab_bytes), a, ka, b, units, epi_kb,
+                                        can_split_tail(p, a, b, m, n) &&
+                                            !(forced && forced->tail_split == 1));
+          // Epilogue warps per lane quarter: forced, or 1 and (where it pays,
+          // for clusters of one CTA group) 2.
+          for (int e : {1, 2}) {
+            if (fepw ? e != fepw
+                     : e == 2 && (m != 1 || n != 1 || !two_epilogue_warps_pay(tc, tiles, units)))
+              continue;
+            const double c = plan_cost(tc, e);
+            if (c < best - 1e-9) { best = c; cg = a; bn = b; mc = m; nc = n; epw = e; }
+          }
         }
   if (!cg) return GEMM_ERR_UNSUPPORTED_CONFIG;
   if (gemm_tmem_columns(128, bn) > (int)gb300::kAccStride) return GEMM_ERR_UNSUPPORTED_CONFIG;
@@ -426,7 +461,7 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
   c.tile_m = 128 * cg;
   c.cluster_m = mc;
   c.cluster_n = nc;
-  c.epi_warps = forced && forced->epi_warps ? forced->epi_warps : 1;
+  c.epi_warps = epw;
   if (c.epi_warps == 2 && csize != cg) return GEMM_ERR_UNSUPPORTED_CONFIG;
   c.l2_hints = forced && (forced->l2_hints & 0x100) ? (forced->l2_hints & 0x3F) : kDefaultL2Hints;
   c.epi_wait_ns = forced && forced->epi_wait_ns > 0 ? forced->epi_wait_ns - 1 : kDefaultEpiWaitNs;

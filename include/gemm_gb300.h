@@ -131,7 +131,8 @@ typedef struct {
  *               192 threads a CTA) or 2 (8 warps, 320 threads; the two warps
  *               of a quarter take its 32-column chunks alternately, each with
  *               half the epilogue slots; clusters of one CTA group only).
- *               0 = automatic.
+ *               0 = automatic: 2 where the tiles fit in one wave or the
+ *               epilogue takes about as long as the main loop, else 1.
  *   Fields marked "diagnostic" are for tuning and testing the kernel, not
  *   part of the GEMM contract; leave them 0.
  *   l2_hints    (diagnostic; also an input) L2 eviction priority of the TMA
@@ -160,8 +161,10 @@ typedef struct {
  *               mbarrier (2 per stage, 2 per accumulator stage) + 4 bytes of
  *               tensor-memory address.
  *   epi_slots   epilogue shared-memory slots: C/X sub-tiles (128 rows x 32
- *               columns) are TMA-loaded epi_slots-1 chunks ahead; D/Y are staged
- *               in the same slot and TMA-stored.
+ *               columns) are TMA-loaded epi_slots-1 chunks ahead (with two
+ *               epilogue warps per quarter each warp has epi_slots/2 of them and
+ *               loads that many minus one of its own chunks ahead, at least
+ *               one); D/Y are staged in the same slot and TMA-stored.
  *   epi_slot_bytes  bytes of one epilogue slot.
  *   smem_bytes  dynamic shared memory per CTA (ring + epilogue slots + their
  *               barriers + alignment slack).
