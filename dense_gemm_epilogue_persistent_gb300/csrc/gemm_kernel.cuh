@@ -130,10 +130,11 @@ enum : int {
   kStatEpiTfull,        // epilogue store thread: cycles waiting for an accumulator
   kStatEpiCfull,        //   ... waiting for C/X to land
   kStatEpiLoop,         //   ... in its whole loop
-  kStatEpiChunks,       //   chunks processed
+  kStatEpiChunks,       //   chunks the CTA processed (all epilogue warps of a lane quarter)
   kStatEpiRead,         //   ... from C/X landing to C/X read and accumulator columns in registers
   kStatEpiMath,         //   ... computing D and Y and writing them to shared memory
   kStatEpiIssue,        //   ... issuing the stores (and the next loads, with their wait)
+  kStatEpiOwnChunks,    //   chunks the recording warp processed (the three above are its own)
   kStatWords = 16
 };
 
@@ -807,6 +808,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     uint32_t slot_ph = 0;                   // (gc / Ew) & 1: phase of the slot's cfull barrier
     bool ok = true;
     long long st_tfull = 0, st_cfull = 0, st_read = 0, st_math = 0, st_issue = 0;
+    long long st_chunks = 0;
     const long long st_t0 = stat_clock();
     for (int it = cluster_id; ok && it < p.num_items; it += num_clusters) {
       int half;
@@ -821,6 +823,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       ok = __all_sync(0xFFFFFFFFu, ready);
       if (!ok) break;
       tc_fence_after_sync();
+      if constexpr (kRingStats) st_chunks += nchunks;
       // The accumulator stage is handed back to the MMA warp after this
       // warp's last chunk of the item; a warp with no chunk in the item does
       // so at once.
@@ -1005,7 +1008,8 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         o[kStatEpiTfull] = st_tfull;
         o[kStatEpiCfull] = st_cfull;
         o[kStatEpiLoop] = clock64() - st_t0;
-        o[kStatEpiChunks] = gc;
+        o[kStatEpiChunks] = st_chunks;
+        o[kStatEpiOwnChunks] = gc;
         o[kStatEpiRead] = st_read;
         o[kStatEpiMath] = st_math;
         o[kStatEpiIssue] = st_issue;

@@ -264,10 +264,13 @@ gemm_status_t gemm_run_host(gemm_handle_t h, int64_t M, int64_t N, int64_t K, in
  * waiting for a free accumulator stage, its whole loop, stages issued (these
  * four are zero in the non-leader CTA of a pair); producer waiting for a
  * stage to drain, its whole loop; epilogue store thread waiting for a
- * finished accumulator, waiting for C/X to land, its whole loop, chunks
- * processed, then three parts of its chunk loop: from C/X landing to C/X and
- * accumulator columns in registers, computing D and Y into shared memory,
- * issuing the stores and next loads (with their wait); three spare words. */
+ * finished accumulator, waiting for C/X to land, its whole loop, the CTA's
+ * epilogue chunks, then three parts of the store thread's chunk loop: from
+ * C/X landing to C/X and accumulator columns in registers, computing D and Y
+ * into shared memory, issuing the stores and next loads (with their wait);
+ * the chunks the store thread's warp processed (the CTA's chunks with one
+ * epilogue warp per lane quarter, about half of them with two); two spare
+ * words. */
 #define GEMM_RING_STAT_WORDS 16
 gemm_status_t gemm_ring_stats(gemm_handle_t h, struct CUstream_st* stream, uint64_t* out,
                               int max_ctas, int* n_ctas);

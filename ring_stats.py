@@ -84,7 +84,8 @@ def measure(names, launches=30, config=None):
                 "kernel": f"{cfg.tile_m}x{cfg.tile_n} cta_group={cfg.cta_group} "
                           f"cluster_m={cfg.cluster_m} cluster_n={cfg.cluster_n} "
                           f"stages={cfg.stages} "
-                          f"epi_slots={cfg.epi_slots} grid={cfg.grid_ctas}",
+                          f"epi_slots={cfg.epi_slots} epi_warps={cfg.epi_warps} "
+                          f"grid={cfg.grid_ctas}",
                 "tflops_with_counters": round(w.flops / ms / 1e9, 1),
                 "mma_wait_stage_pct": round(100 * share(mma, 0, 2), 2),
                 "mma_wait_accumulator_pct": round(100 * share(mma, 1, 2), 2),
@@ -92,10 +93,10 @@ def measure(names, launches=30, config=None):
                 "producer_wait_drain_pct": round(100 * share(rows, 4, 5), 2),
                 "epilogue_wait_accumulator_pct": round(100 * share(rows, 6, 8), 2),
                 "epilogue_wait_cx_pct": round(100 * share(rows, 7, 8), 2),
-                "epilogue_read_cycles_per_chunk": round(share(rows, 10, 9), 1),
-                "epilogue_math_cycles_per_chunk": round(share(rows, 11, 9), 1),
-                "epilogue_issue_cycles_per_chunk": round(share(rows, 12, 9), 1),
-                "epilogue_cx_wait_cycles_per_chunk": round(share(rows, 7, 9), 1),
+                "epilogue_read_cycles_per_chunk": round(share(rows, 10, 13), 1),
+                "epilogue_math_cycles_per_chunk": round(share(rows, 11, 13), 1),
+                "epilogue_issue_cycles_per_chunk": round(share(rows, 12, 13), 1),
+                "epilogue_cx_wait_cycles_per_chunk": round(share(rows, 7, 13), 1),
                 "stages": int(sum(r[3] for r in mma)),
                 "chunks": int(sum(r[9] for r in rows)),
                 "tiles": int(cfg.tiles), "tail_split": int(cfg.tail_split),
