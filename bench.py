@@ -649,7 +649,7 @@ def main():
                        "kernel": f"{c2.tile_m}x{c2.tile_n} cta_group={c2.cta_group}"
                                  f" cluster={c2.cluster_m}x{c2.cluster_n}"
                                  f" stages={c2.stages} slots={c2.epi_slots}"
-                                 f" grid={c2.grid_ctas}",
+                                 f" epi_warps={c2.epi_warps} grid={c2.grid_ctas}",
                        "clock": {"sm_mhz": clk["sm_mhz"], "samples": clk["samples"],
                                  "samples_under_load": clk["samples_under_load"],
                                  "reasons": clk["reasons"]}}
@@ -705,7 +705,8 @@ def main():
                        "kernel": {"cta_group": cfg.cta_group, "tile": f"{cfg.tile_m}x{cfg.tile_n}",
                                   "cluster": f"{cfg.cluster_m}x{cfg.cluster_n}",
                                   "tile_k": cfg.tile_k, "stages": cfg.stages,
-                                  "grid_ctas": cfg.grid_ctas, "group_m": cfg.group_m},
+                                  "grid_ctas": cfg.grid_ctas, "group_m": cfg.group_m,
+                                  "epi_warps": cfg.epi_warps},
                        "l2": "no flush: inputs larger than L2 "
                              f"({bound.nbytes_in() / 2**20:.0f} MiB of A,B,C,X vs 129 MB)",
                        "parallelism": f"replicas x{world}"},
