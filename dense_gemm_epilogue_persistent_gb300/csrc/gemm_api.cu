@@ -291,12 +291,20 @@ bool variant_supports(const gemm_problem_t& p, int cg, int bn, int mc, int nc) {
 // chains per quarter side by side: in a GB300 sweep of the same widths with
 // the two epilogues alternating, the 10-warp CTAs took 0.85-0.95 of the time
 // where the epilogue is the longer side or stands alone (fp8 with 16-bit C, X
-// and D; single-wave 2048^3 and 256^3) and 1.00-1.02 where the main loop
-// dominates (8192^3, tf32, fp16 accumulators, batched).  Modelled as the
-// epilogue x 0.55, the fixed part x 0.9 and the main loop x 1.015, offered
-// only where it pays (two_epilogue_warps_pay).
+// and D; single-wave 2048^3 and 256^3), about 1.0 (0.98-1.03 between runs)
+// where the two sides are close (fp8 with 16-bit C and D) and 1.00-1.02 where
+// the main loop dominates (8192^3, tf32, fp16 accumulators, batched).
+// Modelled as the epilogue x 0.55, the fixed part x 0.9 and the main loop x
+// 1.015, offered only where it pays (two_epilogue_warps_pay).
+//
+// When every cluster runs one tile at most (a single partial wave), a CTA
+// pair costs a further 4 units (2048^3: 128 x 256 single-CTA tiles 19.4-19.5
+// us against 19.5-20.2 us for 256 x 256 pairs with ten warps, 21.3 against
+// 21.6 us with six).
 struct TileCost {
   double waves, main_loop, epilogue, fixed;
+  bool single_wave;
+  int cta_group;
 };
 
 TileCost tile_cost(int64_t tiles, int64_t k_blocks, int cg, int ka, int bn, int64_t clusters,
@@ -305,6 +313,8 @@ TileCost tile_cost(int64_t tiles, int64_t k_blocks, int cg, int ka, int bn, int6
   const int64_t full = tiles / clusters, rem = tiles % clusters;
   TileCost t;
   t.waves = (double)full + (rem == 0 ? 0.0 : (can_split && 2 * rem <= clusters ? 0.8 : 1.0));
+  t.single_wave = tiles <= clusters;
+  t.cta_group = cg;
   const double w = bn / 256.0;
   double per_kb;
   if (cg == 2) {
@@ -321,15 +331,18 @@ TileCost tile_cost(int64_t tiles, int64_t k_blocks, int cg, int ka, int bn, int6
 
 // Whether the automatic choice offers two epilogue warps per lane quarter: the
 // tiles fit in one wave (each CTA's epilogue runs after its only main loop,
-// with nothing to hide it), or the epilogue is at least 0.8 of the main loop.
-bool two_epilogue_warps_pay(const TileCost& t, int64_t tiles, int64_t clusters) {
-  return tiles <= std::max<int64_t>(1, clusters) || t.epilogue >= 0.8 * t.main_loop;
+// with nothing to hide it), or the epilogue is at least as long as the main
+// loop.
+bool two_epilogue_warps_pay(const TileCost& t) {
+  return t.single_wave || t.epilogue >= t.main_loop;
 }
 
 double plan_cost(const TileCost& t, int epw) {
-  if (epw == 2)
-    return t.waves * (std::max(1.015 * t.main_loop, 0.55 * t.epilogue) + 0.9 * t.fixed);
-  return t.waves * (std::max(t.main_loop, t.epilogue) + t.fixed);
+  const double main_loop = epw == 2 ? 1.015 * t.main_loop : t.main_loop;
+  const double epilogue = epw == 2 ? 0.55 * t.epilogue : t.epilogue;
+  const double fixed = epw == 2 ? 0.9 * t.fixed : t.fixed;
+  const double pair_single = t.single_wave && t.cta_group == 2 ? 4.0 : 0.0;
+  return t.waves * (std::max(main_loop, epilogue) + fixed) + pair_single;
 }
 
 // Whether the last wave of a variant may run as half-width items: clusters of
@@ -403,7 +416,7 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
           // for clusters of one CTA group) 2.
           for (int e : {1, 2}) {
             if (fepw ? e != fepw
-                     : e == 2 && (m != 1 || n != 1 || !two_epilogue_warps_pay(tc, tiles, units)))
+                     : e == 2 && (m != 1 || n != 1 || !two_epilogue_warps_pay(tc)))
               continue;
             const double c = plan_cost(tc, e);
             if (c < best - 1e-9) { best = c; cg = a; bn = b; mc = m; nc = n; epw = e; }

@@ -132,7 +132,7 @@ typedef struct {
  *               of a quarter take its 32-column chunks alternately, each with
  *               half the epilogue slots; clusters of one CTA group only).
  *               0 = automatic: 2 where the tiles fit in one wave or the
- *               epilogue takes about as long as the main loop, else 1.
+ *               epilogue takes at least as long as the main loop, else 1.
  *   Fields marked "diagnostic" are for tuning and testing the kernel, not
  *   part of the GEMM contract; leave them 0.
  *   l2_hints    (diagnostic; also an input) L2 eviction priority of the TMA

@@ -291,21 +291,22 @@ def test_ring_stats_rejected_by_product_library(lib):
 # The tile each workload ran fastest with in a GB300 sweep of all 14 widths x
 # CTA groups (the sweep the planner's constants are fitted to; 128-wide and
 # wider tiles, 152 SMs, bench workloads, warm L2), and the epilogue warps per
-# lane quarter a sweep alternating 1 and 2 on every tile favoured (2 where it
-# took at most 0.98 of the time).  fp8mix_relu_4096 moved from 128 x 224 to
-# 256 x 256 tiles, which with two epilogue warps ran 52-56 us against 58-59.
+# lane quarter that two sweeps alternating 1 and 2 on the same tiles favoured
+# (2 where it took at most 0.98 of the time on average).  fp8mix_relu_4096
+# moved from 128 x 224 to 256 x 256 tiles, which with two epilogue warps ran
+# 53-57 us against 58-65 us.
 MEASURED_BEST = {
     "int256_f16_f32": (1, 128, 2), "gemm2048_bf16_f32": (1, 256, 2),
     "efc8192_f16": (2, 256, 1), "gemm8192_bf16": (2, 256, 1), "batched16_bf16_mn": (2, 256, 1),
-    "ragged_e4m3_f16": (2, 256, 1), "e5m2_4096_f16": (2, 256, 2),
+    "ragged_e4m3_f16": (2, 256, 1), "e5m2_4096_f16": (2, 256, 1),
     "fp8mix_relu_4096": (2, 256, 2), "tf32_4096_f32": (2, 224, 1),
     "f16acc_4096_f16": (2, 224, 1), "e4m3_f16acc_4096": (2, 256, 2),
 }
 # Where the planner's pick differs, and what that costs in the same sweeps:
-# 2048^3 takes 256 x 256 pair tiles (19.46 us against 18.97 us for 128 x 256
-# single-CTA tiles, both with two epilogue warps); the ragged fp8 shape takes
-# two epilogue warps (time ratio 1.002 to one).
-PLANNER_EXCEPTIONS = {"gemm2048_bf16_f32": (2, 256, 2), "ragged_e4m3_f16": (2, 256, 2)}
+# the fp8 GEMM with an fp16 accumulator keeps six warps (two took 0.95 and
+# 0.98 of the time in the two sweeps; the other fp8 shapes whose epilogue is as
+# long as theirs measured 0.98-1.03, so the rule does not separate them).
+PLANNER_EXCEPTIONS = {"e4m3_f16acc_4096": (2, 256, 1)}
 
 
 @pytest.mark.parametrize("name", list(MEASURED_BEST))
