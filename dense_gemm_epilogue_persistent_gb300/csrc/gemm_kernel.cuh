@@ -319,65 +319,65 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t w) {
 // Lane r touches only row r; the swizzles make each 8-row group of a warp hit
 // distinct banks.  The type and layout branches are uniform and sit outside the
 // element loops, and 16-bit values convert two at a time.
-__device__ __forceinline__ void smem_read_row(const uint8_t* sub, int dt, int m_major, int r,
-                                              float (&v)[kEpiChunk]) {
+// Calls f(i, value) for the 32 values of row r, in pieces as they are loaded,
+// so that a caller folding them into another array keeps only a few of them
+// in registers at a time.
+template <bool BF16, typename F>
+__device__ __forceinline__ void smem_row_each_16(const uint8_t* sub, int m_major, int r, F&& f) {
+  auto unpack = [](uint32_t w) { return BF16 ? unpack_bf16x2(w) : unpack_f16x2(w); };
   if (!m_major) {
-    if (dt == DT_F32) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float4 q = *reinterpret_cast<const float4*>(sub + r * 128 + ((j ^ (r & 7)) << 4));
-        v[4 * j] = q.x; v[4 * j + 1] = q.y; v[4 * j + 2] = q.z; v[4 * j + 3] = q.w;
-      }
-    } else {
-      uint32_t w[16];
+    for (int j = 0; j < 4; ++j) {
+      const uint4 q = *reinterpret_cast<const uint4*>(sub + r * 64 + ((j ^ ((r >> 1) & 3)) << 4));
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint4 q =
-            *reinterpret_cast<const uint4*>(sub + r * 64 + ((j ^ ((r >> 1) & 3)) << 4));
-        w[4 * j] = q.x; w[4 * j + 1] = q.y; w[4 * j + 2] = q.z; w[4 * j + 3] = q.w;
-      }
-      if (dt == DT_BF16) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 f = unpack_bf16x2(w[i]);
-          v[2 * i] = f.x; v[2 * i + 1] = f.y;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 f = unpack_f16x2(w[i]);
-          v[2 * i] = f.x; v[2 * i + 1] = f.y;
-        }
+      for (int k = 0; k < 4; ++k) {
+        const float2 v = unpack(w[k]);
+        f(8 * j + 2 * k, v.x);
+        f(8 * j + 2 * k + 1, v.y);
       }
     }
   } else {
-    if (dt == DT_F32) {
 #pragma unroll
-      for (int c = 0; c < kEpiChunk; ++c)
-        v[c] = *reinterpret_cast<const float*>(sub + (c * kSubRows + r) * 4);
-    } else {
-      uint32_t w[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint32_t lo = *reinterpret_cast<const uint16_t*>(sub + (2 * i * kSubRows + r) * 2);
-        const uint32_t hi = *reinterpret_cast<const uint16_t*>(sub + ((2 * i + 1) * kSubRows + r) * 2);
-        w[i] = lo | (hi << 16);
-      }
-      if (dt == DT_BF16) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 f = unpack_bf16x2(w[i]);
-          v[2 * i] = f.x; v[2 * i + 1] = f.y;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 f = unpack_f16x2(w[i]);
-          v[2 * i] = f.x; v[2 * i + 1] = f.y;
-        }
-      }
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t lo = *reinterpret_cast<const uint16_t*>(sub + (2 * i * kSubRows + r) * 2);
+      const uint32_t hi = *reinterpret_cast<const uint16_t*>(sub + ((2 * i + 1) * kSubRows + r) * 2);
+      const float2 v = unpack(lo | (hi << 16));
+      f(2 * i, v.x);
+      f(2 * i + 1, v.y);
     }
   }
+}
+
+// Calls f(i, value) for the 32 values of row r, in pieces as they are loaded,
+// so that a caller folding them into another array keeps only a few of them
+// in registers at a time.
+template <typename F>
+__device__ __forceinline__ void smem_row_each(const uint8_t* sub, int dt, int m_major, int r,
+                                              F&& f) {
+  if (dt == DT_BF16) {
+    smem_row_each_16<true>(sub, m_major, r, f);
+  } else if (dt != DT_F32) {
+    smem_row_each_16<false>(sub, m_major, r, f);
+  } else if (!m_major) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float4 q = *reinterpret_cast<const float4*>(sub + r * 128 + ((j ^ (r & 7)) << 4));
+      f(4 * j, q.x);
+      f(4 * j + 1, q.y);
+      f(4 * j + 2, q.z);
+      f(4 * j + 3, q.w);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < kEpiChunk; ++c)
+      f(c, *reinterpret_cast<const float*>(sub + (c * kSubRows + r) * 4));
+  }
+}
+
+__device__ __forceinline__ void smem_read_row(const uint8_t* sub, int dt, int m_major, int r,
+                                              float (&v)[kEpiChunk]) {
+  smem_row_each(sub, dt, m_major, r, [&](int i, float x) { v[i] = x; });
 }
 
 __device__ __forceinline__ void smem_write_row(uint8_t* sub, int dt, int m_major, int r,
@@ -899,13 +899,17 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         long long t_r = 0;
         if constexpr (kRingStats) { t_r = clock64(); st_cfull += t_r - t_c; }
         got = __all_sync(0xFFFFFFFFu, got);
-        if (got && e.read_c) {
-          smem_read_row(slot, e.c_dt, e.cd_m_major, lane, cv);
-        } else {
+        if constexpr (EPW == 1) {
+          // One warp per lane quarter: the C/X rows are read while the
+          // accumulator load is in flight.
+          if (got && e.read_c) {
+            smem_read_row(slot, e.c_dt, e.cd_m_major, lane, cv);
+          } else {
 #pragma unroll
-          for (int i = 0; i < kEpiChunk; ++i) cv[i] = 0.f;
+            for (int i = 0; i < kEpiChunk; ++i) cv[i] = 0.f;
+          }
+          if (got && e.read_x) smem_read_row(slot + cd_sub, e.x_dt, e.cd_m_major, lane, xv);
         }
-        if (got && e.read_x) smem_read_row(slot + cd_sub, e.x_dt, e.cd_m_major, lane, xv);
         __syncwarp();                       // the .aligned wait needs the whole warp
         tmem_wait_ld(raw_acc);
         // Normalise the accumulator to fp32 bit patterns once per chunk (uniform
@@ -936,7 +940,44 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         // are uniform and outside the element loops.
         float dv[kEpiChunk];
         const float al = e.alpha, be = e.beta, xf = e.x_factor;
-        if (e.read_x) {
+        if constexpr (EPW == 2) {
+          // Two warps per lane quarter (a 168-register budget): C and X are
+          // folded into D as their pieces are read, after the accumulator
+          // load, so no whole C or X row is held; the same operations in the
+          // same order as below, so both forms give the same bits.
+          auto fold_c = [&](bool first) {   // first: dv = be * c, else dv = fma(be, c, dv)
+            if (e.read_c) {
+              if (first)
+                smem_row_each(slot, e.c_dt, e.cd_m_major, lane, [&](int i, float c) { dv[i] = be * c; });
+              else
+                smem_row_each(slot, e.c_dt, e.cd_m_major, lane,
+                              [&](int i, float c) { dv[i] = fmaf(be, c, dv[i]); });
+            } else {
+#pragma unroll
+              for (int i = 0; i < kEpiChunk; ++i) dv[i] = first ? be * 0.f : fmaf(be, 0.f, dv[i]);
+            }
+          };
+          if (e.read_x && !e.relu) {
+            // fmaf(al, acc, fmaf(be, c, xf * x))
+            smem_row_each(slot + cd_sub, e.x_dt, e.cd_m_major, lane, [&](int i, float x) { dv[i] = xf * x; });
+            fold_c(false);
+#pragma unroll
+            for (int i = 0; i < kEpiChunk; ++i) dv[i] = fmaf(al, __uint_as_float(raw_acc[i]), dv[i]);
+          } else {
+            // fmaf(al, acc, be * c), then relu, then fmaf(xf, x, .)
+            fold_c(true);
+#pragma unroll
+            for (int i = 0; i < kEpiChunk; ++i) dv[i] = fmaf(al, __uint_as_float(raw_acc[i]), dv[i]);
+            if (e.relu) {
+#pragma unroll
+              for (int i = 0; i < kEpiChunk; ++i) dv[i] = fmaxf(dv[i], 0.f);
+            }
+            if (e.read_x)
+              smem_row_each(slot + cd_sub, e.x_dt, e.cd_m_major, lane,
+                            [&](int i, float x) { dv[i] = fmaf(xf, x, dv[i]); });
+          }
+          __syncwarp();                     // every lane has read its C/X row
+        } else if (e.read_x) {
           if (e.relu) {
 #pragma unroll
             for (int i = 0; i < kEpiChunk; ++i)

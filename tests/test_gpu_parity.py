@@ -242,6 +242,38 @@ def test_two_epilogue_warps_per_quarter(gemm, cg, bn, slots, loads):
     gemm.set_config(None)
 
 
+@pytest.mark.parametrize("epi", [
+    dict(c="f16", x="bf16", y="f16", d="f16", beta=-0.75, xf=1.5, relu=False),
+    dict(c="f16", x="bf16", y=None, d="bf16", beta=0.5, xf=-2.0, relu=True),
+    dict(c="f32", x=None, y="f32", d="f32", beta=1.0, xf=0.0, relu=False),
+    dict(c="bf16", x=None, y=None, d="f16", beta=0.25, xf=0.0, relu=True),
+    dict(c=None, x="f16", y="bf16", d="f32", beta=0.0, xf=0.5, relu=False),
+    dict(c=None, x=None, y=None, d="bf16", beta=0.0, xf=0.0, relu=False),
+])
+@pytest.mark.parametrize("cd_m", [False, True])
+def test_epilogue_warp_forms_bitwise_equal(gemm, epi, cd_m):
+    """The ten-warp form folds C and X into D piece by piece after the
+    accumulator load; the six-warp form reads whole rows first.  Both apply the
+    same operations in the same order, so on the same tile their D and Y are
+    bit-identical (real-valued inputs, every epilogue shape)."""
+    case = Case(M=640, N=544, K=264, L=2, ab="bf16", c=epi["c"], d=epi["d"], x=epi["x"],
+                y=epi["y"], cd_m=cd_m, alpha=0.875, beta=epi["beta"], xf=epi["xf"],
+                relu=epi["relu"], seed=77 + cd_m)
+    prep = prepare(case)
+    outs = []
+    for epw in (1, 2):
+        _force(gemm, 2, 224, 1, 1, epw)
+        D, Y = run_gpu(gemm, prep)
+        _finish(gemm)
+        assert gemm.last_config().epi_warps == epw
+        outs.append((D.clone(), None if Y is None else Y.clone()))
+    gemm.set_config(None)
+    assert torch.equal(outs[0][0].view(torch.uint8), outs[1][0].view(torch.uint8))
+    if outs[0][1] is not None:
+        assert torch.equal(outs[0][1].view(torch.uint8), outs[1][1].view(torch.uint8))
+    compare_full(prep, *outs[1])
+
+
 def test_two_epilogue_warps_need_one_group_clusters(gemm):
     """Two epilogue warps per quarter exist only for clusters of one CTA group."""
     case = SMALL["efc_f16"]
