@@ -948,7 +948,8 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           auto fold_c = [&](bool first) {   // first: dv = be * c, else dv = fma(be, c, dv)
             if (e.read_c) {
               if (first)
-                smem_row_each(slot, e.c_dt, e.cd_m_major, lane, [&](int i, float c) { dv[i] = be * c; });
+                smem_row_each(slot, e.c_dt, e.cd_m_major, lane,
+                              [&](int i, float c) { dv[i] = be * c; });
               else
                 smem_row_each(slot, e.c_dt, e.cd_m_major, lane,
                               [&](int i, float c) { dv[i] = fmaf(be, c, dv[i]); });
@@ -959,15 +960,18 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           };
           if (e.read_x && !e.relu) {
             // fmaf(al, acc, fmaf(be, c, xf * x))
-            smem_row_each(slot + cd_sub, e.x_dt, e.cd_m_major, lane, [&](int i, float x) { dv[i] = xf * x; });
+            smem_row_each(slot + cd_sub, e.x_dt, e.cd_m_major, lane,
+                          [&](int i, float x) { dv[i] = xf * x; });
             fold_c(false);
 #pragma unroll
-            for (int i = 0; i < kEpiChunk; ++i) dv[i] = fmaf(al, __uint_as_float(raw_acc[i]), dv[i]);
+            for (int i = 0; i < kEpiChunk; ++i)
+              dv[i] = fmaf(al, __uint_as_float(raw_acc[i]), dv[i]);
           } else {
             // fmaf(al, acc, be * c), then relu, then fmaf(xf, x, .)
             fold_c(true);
 #pragma unroll
-            for (int i = 0; i < kEpiChunk; ++i) dv[i] = fmaf(al, __uint_as_float(raw_acc[i]), dv[i]);
+            for (int i = 0; i < kEpiChunk; ++i)
+              dv[i] = fmaf(al, __uint_as_float(raw_acc[i]), dv[i]);
             if (e.relu) {
 #pragma unroll
               for (int i = 0; i < kEpiChunk; ++i) dv[i] = fmaxf(dv[i], 0.f);
