@@ -251,14 +251,16 @@ def test_two_epilogue_warps_per_quarter(gemm, cg, bn, slots, loads):
     dict(c=None, x=None, y=None, d="bf16", beta=0.0, xf=0.0, relu=False),
 ])
 @pytest.mark.parametrize("cd_m", [False, True])
-def test_epilogue_warp_forms_bitwise_equal(gemm, epi, cd_m):
+@pytest.mark.parametrize("ab,acc", [("bf16", "f32"), ("e4m3", "f16"), ("tf32", "f32")])
+def test_epilogue_warp_forms_bitwise_equal(gemm, epi, cd_m, ab, acc):
     """The ten-warp form folds C and X into D piece by piece after the
     accumulator load; the six-warp form reads whole rows first.  Both apply the
     same operations in the same order, so on the same tile their D and Y are
     bit-identical (real-valued inputs, every epilogue shape)."""
-    case = Case(M=640, N=544, K=264, L=2, ab="bf16", c=epi["c"], d=epi["d"], x=epi["x"],
-                y=epi["y"], cd_m=cd_m, alpha=0.875, beta=epi["beta"], xf=epi["xf"],
-                relu=epi["relu"], seed=77 + cd_m)
+    case = Case(M=640, N=544, K=264 if ab != "e4m3" else 256, L=2, ab=ab, c=epi["c"],
+                d=epi["d"], x=epi["x"], y=epi["y"], cd_m=cd_m, alpha=0.875, beta=epi["beta"],
+                xf=epi["xf"], relu=epi["relu"], acc=acc,
+                dist="e4m3_pm4" if ab == "e4m3" else "normal1", seed=77 + cd_m)
     prep = prepare(case)
     outs = []
     for epw in (1, 2):
