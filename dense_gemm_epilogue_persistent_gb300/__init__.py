@@ -59,7 +59,8 @@ class gemm_config_t(ctypes.Structure):
                 ("l2_hints", ctypes.c_int), ("epi_wait_ns", ctypes.c_int),
                 ("inject_stall", ctypes.c_int), ("tail_split", ctypes.c_int),
                 ("cluster_n", ctypes.c_int),
-                ("epi_warps", ctypes.c_int)]
+                ("epi_warps", ctypes.c_int),
+                ("stream_k", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

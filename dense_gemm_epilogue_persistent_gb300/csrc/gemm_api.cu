@@ -49,8 +49,9 @@ constexpr int kMaxEpiSlots = 6;
 constexpr int kDefaultL2Hints = 2 | (2 << 2) | (2 << 4);
 constexpr int kDefaultEpiWaitNs = 0;
 // base alignment + abort flag + watchdog-test barrier + the epilogue warps'
-// ring-batch barriers (one per warp and chunk of a tile)
-constexpr int kSmemSlack = 1024 + 16 + 8 * gb300::kMaxEpiWarps * gb300::kMaxChunks;
+// ring-batch barriers (one per warp and chunk of a tile) + the two stream-K
+// barriers
+constexpr int kSmemSlack = 1024 + 16 + 8 * gb300::kMaxEpiWarps * gb300::kMaxChunks + 16;
 
 struct VariantState {
   bool smem_attr_set = false;  // max dynamic smem attribute raised to the opt-in limit
@@ -125,6 +126,10 @@ struct gemm_handle {
   size_t ws_bytes = 0;
   std::mutex ws_mu;
   unsigned long long* d_stats = nullptr;   // ring statistics (statistics build only)
+  // Stream-K workspace: one 128 x 256 fp32 partial slot and one flag per SM
+  // (null: stream-K is never planned for this handle).
+  float* sk_partials = nullptr;
+  uint32_t* sk_flags = nullptr;
 };
 
 namespace {
@@ -345,6 +350,21 @@ double plan_cost(const TileCost& t, int epw) {
   return t.waves * (std::max(main_loop, epilogue) + fixed) + pair_single;
 }
 
+// Whether the automatic choice splits k-blocks across clusters (stream-K) for
+// a single partial wave of `tiles` tiles on `units` clusters.  Never: on GB300
+// the 2048^3 bf16 GEMM with fp32 C/D ran 26.2-26.7 us with stream-K on all 152
+// SMs (128 x 256 tiles or 256 x 256 pairs) against 20.5-20.9 us without, in
+// alternating runs; each cluster issues 16 % fewer k-blocks, but its MMA
+// issuer's cycles per stage rose from ~785 to ~1020 (ring statistics) while
+// the partial sums were stored and read, and a copy that skipped the partial
+// stores still took 23.0-24.7 us.  A single wave of 152 tiles (2432 x 2048 x
+// 2048) runs in the same ~21 us as 128, so the 24 idle SMs are not what the
+// single wave loses.  Forced (stream_k = 2) it runs, with its parity tests.
+bool stream_k_pays(int64_t tiles, int64_t k_blocks, int64_t units) {
+  (void)tiles; (void)k_blocks; (void)units;
+  return false;
+}
+
 // Whether the last wave of a variant may run as half-width items: clusters of
 // one CTA group (groups of a larger cluster share operands), half tiles that
 // are whole epilogue chunks, and B staged in whole 128-byte atoms at half
@@ -366,7 +386,7 @@ int64_t resident_clusters(int sm_count, const int* clusters_by_size, int csize) 
 
 gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
                    const gemm_config_t* forced, gemm_config_t* out,
-                   const int* clusters_by_size = nullptr) {
+                   const int* clusters_by_size = nullptr, bool stream_k_ok = true) {
   gemm_status_t st = validate(pp);
   if (st != GEMM_OK) return st;
   if (!out || sm_count <= 0 || smem_optin <= 0) return GEMM_ERR_INVALID_ARG;
@@ -488,13 +508,25 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
   // contend for the 512 tensor-memory columns each allocates.
   c.smem_bytes = std::max(total_smem(cg, bn, ka, stages, slots, slot), smem_optin / 2 + 1024);
   c.tiles = tiles;
+  // Stream-K: when the tiles fill less than one wave of clusters, every
+  // resident cluster takes an equal contiguous share of all the tiles'
+  // k-blocks (fp32 accumulators, clusters of one CTA group, at least one
+  // k-block per cluster); a tile's earlier k-blocks come back to its owner as
+  // fp32 partial sums, added in cluster order.
+  const int64_t k_blocks = cdiv(p.K, (int64_t)c.tile_k);
+  const int fsk = forced ? forced->stream_k : 0;
+  const bool sk_possible = stream_k_ok && mc == 1 && nc == 1 && p.dtypes.acc != GEMM_F16 &&
+                           p.K > 0 && tiles < units && tiles * k_blocks >= units &&
+                           bn / gb300::kEpiChunk >= 2 && units * cg <= sm_count;
+  const bool sk = sk_possible && (fsk == 2 || (fsk == 0 && stream_k_pays(tiles, k_blocks, units)));
+  c.stream_k = sk ? (int)units : 0;
   int64_t split = 0;
-  if (can_split_tail(p, cg, bn, mc, nc) && !(forced && forced->tail_split == 1)) {
+  if (!sk && can_split_tail(p, cg, bn, mc, nc) && !(forced && forced->tail_split == 1)) {
     const int64_t rem = tiles % units;
     if (rem > 0 && 2 * rem <= units) split = rem;
   }
   c.tail_split = (int)split;
-  c.grid_ctas = (int)(std::min<int64_t>(tiles + split, units) * csize);
+  c.grid_ctas = (int)((sk ? units : std::min<int64_t>(tiles + split, units)) * csize);
   *out = c;
   return GEMM_OK;
 }
@@ -593,7 +625,7 @@ gemm_status_t prepare_launch(gemm_handle* h, const gemm_problem_t& p, LaunchEntr
   const gemm_dtypes_t* dtypes = &p.dtypes;
   gemm_config_t cfg{};
   const gemm_status_t st = plan(&p, h->sm_count, h->smem_optin, h->forced ? &h->forced_cfg : nullptr, &cfg,
-            h->clusters_by_size);
+            h->clusters_by_size, h->sk_partials != nullptr && h->sk_flags != nullptr);
   if (st != GEMM_OK) return st;
 
   const int ab_bytes = dtype_bytes(dtypes->ab);
@@ -637,7 +669,19 @@ gemm_status_t prepare_launch(gemm_handle* h, const gemm_problem_t& p, LaunchEntr
     vs.occ_smem = cfg.smem_bytes;
     vs.max_clusters = nclusters;
   }
-  const int64_t clusters = std::min<int64_t>(cfg.tiles + cfg.tail_split, vs.max_clusters);
+  int64_t clusters = std::min<int64_t>(cfg.tiles + cfg.tail_split, vs.max_clusters);
+  if (cfg.stream_k > 0) {
+    // Stream-K runs one item pair on every cluster the kernel can keep
+    // resident; the k-block ranges are cut for exactly that many clusters.
+    const int64_t k_blocks = cdiv(K, (int64_t)cfg.tile_k);
+    clusters = std::min<int64_t>(cfg.stream_k, vs.max_clusters);
+    if (clusters <= cfg.tiles || cfg.tiles * k_blocks < clusters) {
+      clusters = std::min<int64_t>(cfg.tiles, vs.max_clusters);   // not worth it here: off
+      cfg.stream_k = 0;
+    } else {
+      cfg.stream_k = (int)clusters;
+    }
+  }
   cfg.grid_ctas = (int)(clusters * csize);
 
   const bool a_mn = layoutA == GEMM_MN_MAJOR, b_mn = layoutB == GEMM_MN_MAJOR;
@@ -684,12 +728,21 @@ gemm_status_t prepare_launch(gemm_handle* h, const gemm_problem_t& p, LaunchEntr
                              a_mn, b_mn);
   kp.split_start = (int)(cfg.tiles - cfg.tail_split);
   kp.num_items = (int)(cfg.tiles + cfg.tail_split);
+  if (cfg.stream_k > 0) {
+    // every resident cluster takes an equal share of all k-blocks, as up to
+    // two items (the head of one tile, the tail of the previous one)
+    kp.sk_units = cfg.stream_k;
+    kp.sk_iters = cfg.tiles * (long long)kp.k_blocks;
+    kp.num_items = 2 * cfg.stream_k;
+    kp.sk_partials = h->sk_partials;
+    kp.sk_flags = h->sk_flags;
+  }
   kp.l2_hints = (uint32_t)cfg.l2_hints;
   kp.epi_wait_ns = (uint32_t)cfg.epi_wait_ns;
   kp.inject_stall = cfg.inject_stall;
   // fp16 accumulators keep increasing K: their rounding points are defined on
   // running sums from k = 0.
-  kp.k_alternate = acc_f16 ? 0 : 1;
+  kp.k_alternate = acc_f16 || cfg.stream_k > 0 ? 0 : 1;
   kp.status = h->d_status;
   kp.timeout_ns = h->timeout_ns;
   kp.epi.c_dt = dtypes->c;
@@ -860,6 +913,21 @@ GEMM_API gemm_status_t gemm_create(gemm_handle_t* out, int device) {
     }
     cudaSetDevice(prev);
   }
+  // Stream-K workspace (20 MB on 152 SMs), allocated once here so that no
+  // launch allocates; without it the planner never chooses stream-K.
+  if (cudaSetDevice(device) == cudaSuccess) {
+    const size_t pbytes = (size_t)sms * 128 * 256 * sizeof(float);
+    if (cudaMalloc(&h->sk_partials, pbytes) != cudaSuccess ||
+        cudaMalloc(&h->sk_flags, (size_t)sms * sizeof(uint32_t)) != cudaSuccess ||
+        cudaMemset(h->sk_flags, 0, (size_t)sms * sizeof(uint32_t)) != cudaSuccess) {
+      cudaGetLastError();
+      if (h->sk_partials) cudaFree(h->sk_partials);
+      if (h->sk_flags) cudaFree(h->sk_flags);
+      h->sk_partials = nullptr;
+      h->sk_flags = nullptr;
+    }
+  }
+  cudaSetDevice(prev);
   *out = h;
   return GEMM_OK;
 }
@@ -872,6 +940,8 @@ GEMM_API gemm_status_t gemm_destroy(gemm_handle_t h) {
   cudaFree(h->d_status);
   if (h->ws) cudaFree(h->ws);
   if (h->d_stats) cudaFree(h->d_stats);
+  if (h->sk_partials) cudaFree(h->sk_partials);
+  if (h->sk_flags) cudaFree(h->sk_flags);
   cudaSetDevice(prev);
   delete h;
   return GEMM_OK;
@@ -891,6 +961,7 @@ GEMM_API gemm_status_t gemm_set_config(gemm_handle_t h, const gemm_config_t* cfg
       (cfg->cluster_n && cfg->cluster_n != 1 && cfg->cluster_n != 2) ||
       cfg->epi_slots < 0 || cfg->epi_slots > kMaxEpiSlots || cfg->epi_wait_ns < 0 ||
       cfg->tail_split < 0 || cfg->tail_split > 1 || cfg->epi_warps < 0 || cfg->epi_warps > 2 ||
+      cfg->stream_k < 0 || cfg->stream_k > 2 ||
       cfg->epi_wait_ns > 1000001 ||
       cfg->stages > kMaxStages || cfg->group_m < 0)
     return GEMM_ERR_INVALID_ARG;
@@ -1104,6 +1175,8 @@ GEMM_API gemm_status_t gemm_sync_status(gemm_handle_t h, struct CUstream_st* str
   if (detail) *detail = word;
   if (word != 0) {
     cudaMemsetAsync(h->d_status, 0, sizeof(uint32_t), s);
+    // A launch that ended early may leave stream-K flags raised.
+    if (h->sk_flags) cudaMemsetAsync(h->sk_flags, 0, (size_t)h->sm_count * sizeof(uint32_t), s);
     cudaStreamSynchronize(s);
     return status_of_word(word);
   }

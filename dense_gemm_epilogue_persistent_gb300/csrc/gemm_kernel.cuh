@@ -108,6 +108,14 @@ struct KernelParams {
   uint32_t* status;          // device status word (watchdog)
   unsigned long long timeout_ns;
   unsigned long long* stats; // ring statistics (statistics build only; else unused)
+  // Stream-K (tiles fewer than resident clusters): sk_units clusters split the
+  // sk_iters = num_tiles * k_blocks k-blocks of all tiles into equal contiguous
+  // ranges; a tile's k-blocks held by several clusters are summed in fp32
+  // through sk_partials (one 128 x bn slot per CTA) and sk_flags.  0: off.
+  int sk_units;
+  long long sk_iters;
+  float* sk_partials;
+  uint32_t* sk_flags;
   EpiParams epi;
 };
 
@@ -192,7 +200,7 @@ struct TileN {
 // Watchdog codes: 0xE0RRBBBB, RR = role, BBBB = low 16 bits of blockIdx.x.
 enum : uint32_t {
   kWaitProducer = 1, kWaitMmaFull = 2, kWaitMmaAcc = 3, kWaitEpilogue = 4, kWaitEpiLoad = 5,
-  kWaitInjected = 6
+  kWaitInjected = 6, kWaitPartial = 7
 };
 
 struct Watch {
@@ -289,6 +297,72 @@ __device__ __forceinline__ int item_tile(int it, const KernelParams& p, int& hal
   const int r = it - p.split_start;
   half = r & 1;
   return p.split_start + (r >> 1);
+}
+
+// One work item of a cluster: k-blocks [kb0, kb1) of tile `tile` (half as in
+// item_tile).  owner: the item ends at the tile's last k-block, so its
+// epilogue writes the tile; otherwise (stream-K only) it publishes a partial
+// sum.  empty: no work (stream-K only: a cluster whose range is one segment
+// has nothing at its second item position).  Without stream-K, K = 0 gives
+// items of no k-block whose epilogue still writes D = beta C + x_factor X.
+struct Work {
+  int tile, half, kb0, kb1;
+  bool owner, empty;
+};
+
+// Stream-K: the cluster whose range holds k-block i of the flattened
+// (tile, k-block) space, ranges [u T / U, (u + 1) T / U).
+__device__ __forceinline__ int sk_unit_of(long long i, const KernelParams& p) {
+  return (int)(((i + 1) * p.sk_units - 1) / p.sk_iters);
+}
+
+// Item `it` of the static walk (it = cluster + n * clusters).  Without stream-K
+// every item is a whole tile (or half tile) over all k-blocks.  With stream-K
+// each cluster has two item positions: a range that crosses a tile boundary is
+// the tail of tile t0 (which it owns) and the head of tile t0 + 1 (a partial
+// for that tile's owner); the head comes first, so that its partial is
+// published while the owned tail is computed, and no cluster ever waits for a
+// partial that is computed after a wait of its own.
+__device__ __forceinline__ Work work_item(int it, const KernelParams& p, int num_clusters) {
+  Work w;
+  if (!p.sk_units) {
+    w.tile = item_tile(it, p, w.half);
+    w.kb0 = 0;
+    w.kb1 = p.k_blocks;
+    w.owner = true;
+    w.empty = false;
+    return w;
+  }
+  w.half = -1;
+  const int u = it % num_clusters, pos = it / num_clusters;
+  const long long T = p.sk_iters, U = p.sk_units, kb = p.k_blocks;
+  const long long b = u * T / U, e = (u + 1) * T / U;
+  const long long t0 = b / kb, t1 = (e - 1) / kb;
+  w.tile = 0;
+  w.kb0 = w.kb1 = 0;
+  w.owner = false;
+  w.empty = true;
+  if (u >= U || pos > 1 || b >= e) return w;     // (the grid has exactly U clusters)
+  w.empty = false;
+  if (t0 == t1) {
+    if (pos != 0) {
+      w.empty = true;
+      return w;
+    }
+    w.tile = (int)t0;
+    w.kb0 = (int)(b - t0 * kb);
+    w.kb1 = (int)(e - t0 * kb);
+    w.owner = e == (t0 + 1) * kb;
+  } else if (pos == 0) {                  // head of tile t1: a partial
+    w.tile = (int)t1;
+    w.kb1 = (int)(e - t1 * kb);
+  } else {                                // tail of tile t0: owned
+    w.tile = (int)t0;
+    w.kb0 = (int)(b - t0 * kb);
+    w.kb1 = (int)kb;
+    w.owner = true;
+  }
+  return w;
 }
 
 // ------------------------------------------------------------------ epilogue smem
@@ -482,8 +556,9 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 
   // [B ring][A ring][epilogue slots][full x S][empty x S][tfull x 2][tempty x 2]
   // [cfull x 4E (per epilogue warp and slot)][tmem address][abort flag][never]
-  // [rfull x 8 x 8 (per epilogue warp and chunk)]  ("never": a barrier nothing
-  // arrives at, waited on only when a stall is injected to test the watchdog)
+  // [rfull x 8 x 8 (per epilogue warp and chunk)][pdone][pread]  ("never": a
+  // barrier nothing arrives at, waited on only when a stall is injected to
+  // test the watchdog)
   const uint32_t b_ring = base;
   const uint32_t a_ring = b_ring + S * T.b_stage;
   const uint32_t epi0 = a_ring + S * G::A_STAGE;
@@ -497,6 +572,10 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   const uint32_t never_bar = holder + 8u;
   // a ring-batch barrier per epilogue warp and chunk of a tile
   const uint32_t rfull0 = never_bar + 8u;
+  // stream-K: every epilogue warp has stored its partial rows (pdone) / read
+  // the partials it adds (pread)
+  const uint32_t pdone = rfull0 + 8u * (uint32_t)(kMaxEpiWarps * kMaxChunks);
+  const uint32_t pread = pdone + 8u;
   const uint32_t ring_bytes = (uint32_t)S * ((uint32_t)G::A_STAGE + (uint32_t)T.b_stage);
 
   if (threadIdx.x == 0) {
@@ -511,6 +590,8 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     for (int s = 0; s < 4 * E; ++s) mbar_init(cfull0 + 8u * s, 1);
     mbar_init(never_bar, 1);
     for (int q = 0; q < kMaxEpiWarps * kMaxChunks; ++q) mbar_init(rfull0 + 8u * q, 1);
+    mbar_init(pdone, 4 * EPW);
+    mbar_init(pread, 4 * EPW);
     *abort_ptr = 0u;
     fence_barrier_init();
     if (p.k_blocks > 0) {                    // A and B are encoded only when K > 0
@@ -549,10 +630,11 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       long long st_empty = 0;
       const long long st_t0 = stat_clock();
       for (int it = cluster_id; ok && it < p.num_items; it += num_clusters) {
-        int half;
-        const int t = item_tile(it, p, half);
+        const Work wk = work_item(it, p, num_clusters);
+        if (wk.empty) continue;
+        const int half = wk.half;
         int tm, tn, tl;
-        tile_coords(t, p, tm, tn, tl);
+        tile_coords(wk.tile, p, tm, tn, tl);
         // A half-width item covers columns [half * BN/2, +BN/2) of its tile: its
         // CTAs load full B boxes from that origin and the MMA reads their first
         // half.  m0: this CTA's 128 A rows; n0: the first of its B rows, plus
@@ -566,7 +648,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         // still in L2.  The MMA side only counts stages, so the order is the
         // producer's alone.
         const bool k_down = p.k_alternate && ((it / num_clusters) & 1);
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = wk.kb0; kb < wk.kb1; ++kb) {
           const long long t_w = stat_clock();
           if (!wait_phase(empty0 + 8u * s, ph ^ 1u, w, kWaitProducer)) { ok = false; break; }
           if constexpr (kRingStats) st_empty += clock64() - t_w;
@@ -637,18 +719,20 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       const long long st_t0 = stat_clock();
       bool ok = !p.inject_stall || wait_phase(never_bar, 0u, w, kWaitInjected);
       for (int it = cluster_id; ok && it < p.num_items; it += num_clusters) {
+        const Work wk = work_item(it, p, num_clusters);
+        if (wk.empty) continue;
         const long long t_a = stat_clock();
         if (!wait_phase(tempty0 + 8u * acc, aph ^ 1u, w, kWaitMmaAcc)) break;
         if constexpr (kRingStats) st_acc += clock64() - t_a;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + (uint32_t)acc * kAccStride;
-        const uint32_t idesc = it < p.split_start ? p.idesc : p.idesc_half;
+        const uint32_t idesc = wk.half < 0 ? p.idesc : p.idesc_half;
         // (debug build: the item's accumulator columns inside its stage)
-        if (!dbg_check((uint32_t)(it < p.split_start ? BN : BN / 2) <= kAccStride &&
+        if (!dbg_check((uint32_t)(wk.half < 0 ? BN : BN / 2) <= kAccStride &&
                            (uint32_t)acc * kAccStride + kAccStride <= kTmemCols,
                        kChkMmaTmem, w))
           break;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = wk.kb0; kb < wk.kb1; ++kb) {
           const long long t_f = stat_clock();
           if (!wait_phase(full0 + 8u * s, ph, w, kWaitMmaFull)) { ok = false; break; }
           if constexpr (kRingStats) { st_full += clock64() - t_f; ++st_stages; }
@@ -680,7 +764,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
               ok = false;
               break;
             }
-            umma<CG, KIND>(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            umma<CG, KIND>(d_tmem, ad, bd, idesc, (kb != wk.kb0 || k != 0) ? 1u : 0u);
           }
           if (kDebug && !ok) break;
           umma_commit<CG, MULTI>(empty0 + 8u * s, all_mask);   // slot drained: tell every loader
@@ -741,12 +825,13 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     struct Cursor { int it, j, nch, row0, col0, tl; };
     auto cursor_enter = [&](Cursor& cc) {
       for (; cc.it < p.num_items; cc.it += num_clusters) {
-        int half;
-        const int t = item_tile(cc.it, p, half);
+        const Work wk = work_item(cc.it, p, num_clusters);
+        if (wk.empty || !wk.owner) continue;   // no C/X: nothing, or a stream-K partial
+        const int half = wk.half;
         cc.nch = half < 0 ? T.chunks : T.chunks / 2;
         if (strm >= cc.nch) continue;       // no chunk of this item in this stream
         int tm, tn;
-        tile_coords(t, p, tm, tn, cc.tl);
+        tile_coords(wk.tile, p, tm, tn, cc.tl);
         cc.j = strm;
         cc.row0 = tm * G::CM + (int)gm * (G::BM * CG) + (int)rank * G::BM + q * kSubRows;
         cc.col0 = tn * (BN * NC) + (int)gn * BN + (half > 0 ? BN / 2 : 0);
@@ -811,10 +896,11 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     long long st_chunks = 0;
     const long long st_t0 = stat_clock();
     for (int it = cluster_id; ok && it < p.num_items; it += num_clusters) {
-      int half;
-      const int t = item_tile(it, p, half);
+      const Work wk = work_item(it, p, num_clusters);
+      if (wk.empty) continue;
+      const int half = wk.half;
       int tm, tn, tl;
-      tile_coords(t, p, tm, tn, tl);
+      tile_coords(wk.tile, p, tm, tn, tl);
       const int nchunks = half < 0 ? T.chunks : T.chunks / 2;
       const int ncol0 = tn * (BN * NC) + (int)gn * BN + (half > 0 ? BN / 2 : 0);
       const long long t_t = stat_clock();
@@ -835,8 +921,43 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           else mbar_arrive_cluster(map_to_rank(tempty0 + 8u * acc, pair_leader));
         }
       };
-      if (strm >= nchunks) {
+      if (strm >= nchunks) {                // (never with stream-K: whole tiles, >= 2 chunks)
         release_acc();
+        if (++acc == kAccStages) { acc = 0; aph ^= 1u; }
+        continue;
+      }
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * kAccStride;
+      // Stream-K partial sums: this CTA's slot of 128 x BN fp32 values, laid
+      // out [chunk][16-byte piece][row] so that a warp's 32 rows of one piece
+      // are 512 contiguous bytes.
+      auto partial_rows = [&](int slot_cluster) {
+        return reinterpret_cast<float4*>(p.sk_partials) +
+               (size_t)(slot_cluster * CG + (int)rank) * (size_t)(BN * 32) + q * kSubRows + lane;
+      };
+      if (!wk.owner) {
+        // ---- stream-K: the head of a tile another cluster owns.  Its
+        // accumulator goes to this CTA's partial slot; once every epilogue
+        // warp's stores are ordered, one thread publishes the slot's flag.
+        float4* const dst = partial_rows(cluster_id);
+        for (int j = strm; j < nchunks; j += EPW) {
+          uint32_t raw[32];
+          tmem_load_32cols(tbase + 32u * j, raw);
+          tmem_wait_ld(raw);
+          if (j + EPW >= nchunks) release_acc();
+#pragma unroll
+          for (int pc = 0; pc < 8; ++pc)
+            __stcg(dst + (size_t)(j * 8 + pc) * 128,
+                   make_float4(__uint_as_float(raw[4 * pc]), __uint_as_float(raw[4 * pc + 1]),
+                               __uint_as_float(raw[4 * pc + 2]), __uint_as_float(raw[4 * pc + 3])));
+        }
+        fence_acq_rel_gpu();
+        __syncwarp();
+        if (lead) mbar_arrive(pdone);
+        if (ew == 0) {
+          const bool all = wait_phase<true>(pdone, 0u, w, kWaitPartial);
+          if (lead && all) st_release_gpu(p.sk_flags + cluster_id * CG + (int)rank, 1u);
+          ok = __all_sync(0xFFFFFFFFu, all);
+        }
         if (++acc == kAccStages) { acc = 0; aph ^= 1u; }
         continue;
       }
@@ -848,7 +969,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       // none).
       // Only lane 0 keeps the cursor; it decides and tells the warp.
       int batch0 = nchunks;
-      if (loads && it + num_clusters >= p.num_items) {
+      if (loads && (it + num_clusters >= p.num_items || p.sk_units)) {   // (stream-K: owned items come last)
         const int nb = ld.it == it ? (nchunks - ld.j + EPW - 1) / EPW : 0;   // this warp's
         if (lead && nb > 0 && (uint32_t)nb * (4u * EPW) * sub <= ring_bytes) {
           batch0 = ld.j;
@@ -867,8 +988,30 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         batch0 = __shfl_sync(0xFFFFFFFFu, batch0, 0);
       }
+      // Stream-K owner: the clusters sk_first .. cluster_id - 1 hold the tile's
+      // earlier k-blocks; wait until each has published its partial (after the C/X loads
+      // above are under way).
+      int sk_first = cluster_id;
+      if (p.sk_units) {
+        sk_first = sk_unit_of((long long)wk.tile * p.k_blocks, p);
+        bool got = true;
+        for (int c = sk_first; got && c < cluster_id; ++c) {
+          const uint32_t* f = p.sk_flags + c * CG + (int)rank;
+          const uint64_t t0 = globaltimer_ns();
+          while (ld_acquire_gpu(f) == 0u) {
+            if (*w.abort) { got = false; break; }
+            if (globaltimer_ns() - t0 > w.timeout_ns) {
+              *w.abort = 1u;
+              atomicCAS(w.status, 0u, 0xE0000000u | (kWaitPartial << 16) | (blockIdx.x & 0xFFFFu));
+              got = false;
+              break;
+            }
+          }
+        }
+        ok = __all_sync(0xFFFFFFFFu, got);
+        if (!ok) break;
+      }
       const int row0 = tm * G::CM + (int)gm * (G::BM * CG) + (int)rank * G::BM + q * kSubRows;
-      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * kAccStride;
 #pragma unroll 1
       for (int j = strm; j < nchunks; j += EPW, ++gc) {
         // The accumulator columns are requested first: their latency overlaps
@@ -921,6 +1064,19 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             raw_acc[i] = __float_as_uint(__half2float(__ushort_as_half((uint16_t)raw_acc[i])));
+        }
+        // Stream-K owner: add the earlier k-blocks' partial sums, in the
+        // order of the clusters that hold them (fp32 accumulators only).
+        for (int c = sk_first; c < cluster_id; ++c) {
+          const float4* const src = partial_rows(c) + (size_t)j * 8 * 128;
+#pragma unroll
+          for (int pc = 0; pc < 8; ++pc) {
+            const float4 v = __ldcg(src + pc * 128);
+            raw_acc[4 * pc] = __float_as_uint(__uint_as_float(raw_acc[4 * pc]) + v.x);
+            raw_acc[4 * pc + 1] = __float_as_uint(__uint_as_float(raw_acc[4 * pc + 1]) + v.y);
+            raw_acc[4 * pc + 2] = __float_as_uint(__uint_as_float(raw_acc[4 * pc + 2]) + v.z);
+            raw_acc[4 * pc + 3] = __float_as_uint(__uint_as_float(raw_acc[4 * pc + 3]) + v.w);
+          }
         }
         if (j + EPW >= nchunks) release_acc();   // this warp's last chunk of the stage
         ok = got;
@@ -1041,6 +1197,18 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         if (++slot_idx == Ew) { slot_idx = 0; slot_ph ^= 1u; }
         __syncwarp();
         if constexpr (kRingStats) st_issue += clock64() - t_i;
+      }
+      if (p.sk_units && sk_first < cluster_id && ok) {
+        // Every epilogue warp has read the partials: clear their flags for
+        // the next launch (which reads nothing before this grid completes).
+        __syncwarp();
+        if (lead) mbar_arrive(pread);
+        if (ew == 0) {
+          const bool all = wait_phase<true>(pread, 0u, w, kWaitPartial);
+          if (lead && all)
+            for (int c = sk_first; c < cluster_id; ++c) p.sk_flags[c * CG + (int)rank] = 0u;
+          ok = __all_sync(0xFFFFFFFFu, all);
+        }
       }
       if (++acc == kAccStages) { acc = 0; aph ^= 1u; }
     }

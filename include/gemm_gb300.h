@@ -133,6 +133,16 @@ typedef struct {
  *               half the epilogue slots; clusters of one CTA group only).
  *               0 = automatic: 2 where the tiles fit in one wave or the
  *               epilogue takes at least as long as the main loop, else 1.
+ *   stream_k    (after epi_warps) when the tiles fill less than one wave of
+ *               resident clusters, every cluster takes an equal contiguous
+ *               share of all the tiles' k-blocks; the owner of a tile (the
+ *               cluster holding its last k-block) adds the fp32 partial sums of
+ *               its earlier k-blocks, in cluster order, before its epilogue.
+ *               fp32 accumulators and clusters of one CTA group only; the
+ *               partials go through a workspace the handle allocates at
+ *               creation (gemm_run_noalloc never uses it).  As an input:
+ *               0 = automatic, 1 = never, 2 = wherever allowed.  As an output:
+ *               the number of clusters sharing the k-blocks (0 = off).
  *   Fields marked "diagnostic" are for tuning and testing the kernel, not
  *   part of the GEMM contract; leave them 0.
  *   l2_hints    (diagnostic; also an input) L2 eviction priority of the TMA
@@ -183,6 +193,7 @@ typedef struct {
   int tail_split;
   int cluster_n;
   int epi_warps;
+  int stream_k;
 } gemm_config_t;
 
 /* Every argument of one gemm_run call, for the host-only planning calls. */
@@ -286,7 +297,11 @@ gemm_status_t gemm_ring_stats(gemm_handle_t h, struct CUstream_st* stream, uint6
  * else GEMM_OK.
  * *detail (optional; may be NULL) receives the raw status word (0 when
  * clean): an extension of the two-argument call, carrying the watchdog's
- * record 0xE0RRBBBB (RR the waiting role, BBBB the low bits of the block). */
+ * record 0xE0RRBBBB (RR the waiting role: 1 producer, 2 MMA waiting for
+ * operands, 3 MMA waiting for an accumulator, 4 epilogue waiting for an
+ * accumulator, 5 epilogue waiting for C/X, 6 injected stall, 7 stream-K
+ * partial sums; BBBB the low bits of the block).  After an error the call
+ * also clears the handle's stream-K flags. */
 gemm_status_t gemm_sync_status(gemm_handle_t h, struct CUstream_st* stream, uint32_t* detail);
 
 /* Human-readable name of a status code (static storage). */

@@ -378,6 +378,33 @@ def test_plan_epilogue_warps(lib):
         assert st == G.GEMM_ERR_UNSUPPORTED_CONFIG
 
 
+def test_plan_stream_k(lib):
+    """Stream-K only when forced (it measured slower on GB300), only for a
+    single partial wave with fp32 accumulators, and 'never' turns it off."""
+    dt = G.make_dtypes("bf16", "f32", "f32")
+    single = _p(M=2048, N=2048, K=2048, lda=2048, ldb=2048, dtypes=dt)
+    st, cfg = G.gemm_plan(single, 152, 232448)
+    assert st == 0 and cfg.stream_k == 0
+    for cg, bn, units in ((1, 256, 152), (2, 256, 76)):
+        st, cfg = G.gemm_plan(single, 152, 232448,
+                              G.gemm_config_t(cta_group=cg, tile_n=bn, stream_k=2))
+        assert st == 0 and cfg.stream_k == units and cfg.tail_split == 0
+        assert cfg.grid_ctas == units * cg and cfg.tiles < units
+        st, cfg = G.gemm_plan(single, 152, 232448,
+                              G.gemm_config_t(cta_group=cg, tile_n=bn, stream_k=1))
+        assert st == 0 and cfg.stream_k == 0
+    multi = _p(M=8192, N=8192, K=512, lda=512, ldb=512, dtypes=dt)
+    st, cfg = G.gemm_plan(multi, 152, 232448, G.gemm_config_t(stream_k=2))
+    assert st == 0 and cfg.stream_k == 0
+    dt16 = G.make_dtypes("f16", "f16", "f16", acc="f16")
+    acc16 = _p(M=2048, N=2048, K=2048, lda=2048, ldb=2048, dtypes=dt16)
+    st, cfg = G.gemm_plan(acc16, 152, 232448, G.gemm_config_t(cta_group=1, tile_n=256, stream_k=2))
+    assert st == 0 and cfg.stream_k == 0
+    st, cfg = G.gemm_plan(single, 152, 232448,
+                          G.gemm_config_t(cta_group=2, tile_n=256, cluster_m=2, stream_k=2))
+    assert st == 0 and cfg.stream_k == 0
+
+
 def _includes(path, seen):
     """Every in-tree file `path` includes, transitively."""
     import re

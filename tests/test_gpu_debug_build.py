@@ -27,7 +27,7 @@ cases = [
     (Case(M=720, N=704, K=400, L=2, ab="bf16", c="f16", d="f32", x="bf16", y="f16",
           a_mn=True, b_mn=True, alpha=-0.75, beta=1.0, xf=0.5, seed=31),
      [None, (2, 256, 1, 2), (2, 256, 2, 2), (1, 128, 2, 1), (2, 128, 1, 1), (1, 64, 1, 1),
-      (2, 256, 1, 1, 2), (1, 192, 1, 1, 2)]),
+      (2, 256, 1, 1, 2), (1, 192, 1, 1, 2), (1, 256, 1, 1, 2, 2), (2, 128, 1, 1, 1, 2)]),
     (Case(M=300, N=504, K=272, L=1, ab="e4m3", c="f16", d="f16", alpha=0.25, beta=1.0,
           dist="e4m3_pm4", seed=4),
      [None, (2, 224, 1, 1), (1, 160, 1, 1), (2, 96, 2, 1), (2, 192, 1, 1)]),
@@ -44,7 +44,8 @@ for case, variants in cases:
     for v in variants:
         if v:
             g.set_config(cta_group=v[0], tile_n=v[1], cluster_m=v[2], cluster_n=v[3],
-                         epi_warps=v[4] if len(v) > 4 else 0)
+                         epi_warps=v[4] if len(v) > 4 else 0,
+                         stream_k=v[5] if len(v) > 5 else 0)
         else:
             g.set_config(None)
         prep = prepare(case)

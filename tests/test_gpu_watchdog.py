@@ -14,10 +14,12 @@ from gemm_cases import Case, compare_full, prepare, run_gpu
 
 pytestmark = pytest.mark.gpu
 
-# (cta_group, tile_n, cluster_m, cluster_n, epi_warps): single CTAs, pairs,
-# clusters sharing B, A or both through multicast, and eight epilogue warps
-VARIANTS = [(1, 256, 1, 1, 1), (2, 256, 1, 1, 1), (2, 256, 2, 1, 1), (1, 128, 2, 1, 1),
-            (2, 256, 1, 2, 1), (2, 160, 2, 2, 1), (1, 128, 1, 1, 2), (2, 256, 1, 1, 2)]
+# (cta_group, tile_n, cluster_m, cluster_n, epi_warps, stream_k): single CTAs,
+# pairs, clusters sharing B, A or both through multicast, eight epilogue
+# warps, and stream-K (whose owners also wait for partial sums)
+VARIANTS = [(1, 256, 1, 1, 1, 0), (2, 256, 1, 1, 1, 0), (2, 256, 2, 1, 1, 0),
+            (1, 128, 2, 1, 1, 0), (2, 256, 1, 2, 1, 0), (2, 160, 2, 2, 1, 0),
+            (1, 128, 1, 1, 2, 0), (2, 256, 1, 1, 2, 0), (1, 256, 1, 1, 2, 2), (2, 128, 1, 1, 1, 2)]
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
@@ -29,10 +31,10 @@ def test_injected_stall_times_out_cleanly_and_context_survives(variant):
         case = Case(M=1024, N=768, K=512, L=1, ab="f16", c="f16", d="f16", x="f16", y="f16",
                     alpha=1.0, beta=1.0, xf=1.0, seed=77)
         prep = prepare(case)
-        cg, bn, mc, nc, epw = variant
+        cg, bn, mc, nc, epw, sk = variant
         G.gemm_set_timeout_ns(g.handle, 50_000_000)           # 50 ms per wait
         g.set_config(G.gemm_config_t(cta_group=cg, tile_n=bn, cluster_m=mc, cluster_n=nc,
-                                     epi_warps=epw, inject_stall=1))
+                                     epi_warps=epw, stream_k=sk, inject_stall=1))
         run_gpu(g, prep)
         st, detail = g.sync_status()
         assert st == G.GEMM_ERR_DEVICE_TIMEOUT
@@ -42,10 +44,11 @@ def test_injected_stall_times_out_cleanly_and_context_survives(variant):
         # the same handle, stream and context run a normal GEMM correctly
         G.gemm_set_timeout_ns(g.handle, 0)
         g.set_config(G.gemm_config_t(cta_group=cg, tile_n=bn, cluster_m=mc, cluster_n=nc,
-                                     epi_warps=epw))
+                                     epi_warps=epw, stream_k=sk))
         D, Y = run_gpu(g, prep)
         st, detail = g.sync_status()
         assert st == G.GEMM_OK, hex(detail)
+        assert (g.last_config().stream_k > 0) == (sk == 2)
         compare_full(prep, D, Y)
     finally:
         g.close()
