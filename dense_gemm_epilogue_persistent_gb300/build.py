@@ -25,8 +25,8 @@ neither a GPU nor libcuda):
                            only on request.
 
 Each kernel unit is compiled once per input width (and per epilogue warp
-count for kern_plain.cu, per cluster shape for kern_shared.cu) with -D flags,
-so the units compile in parallel.
+count and stream-K form for kern_plain.cu, per cluster shape for
+kern_shared.cu) with -D flags, so the units compile in parallel.
 """
 from __future__ import annotations
 
@@ -55,10 +55,11 @@ DEBUG_LIB = LIBS["debug"]
 EXTRA_DEFINES = {"stats": ["-DGB300_RING_STATS=1"], "debug": ["-DGB300_DEBUG=1"]}
 
 # (object name, source, -D flags).  Input widths: 2 bytes (fp16/bf16), 1 (fp8),
-# 4 (tf32); epilogue warps per tensor-memory lane quarter (1 or 2);
-# operand-sharing cluster shapes (groups along M, along N).
-PLAIN_UNITS = [(f"kern_plain_ab{ab}_e{epw}", "kern_plain.cu", [f"-DGB300_AB={ab}", f"-DGB300_EPW={epw}"])
-               for ab in (2, 1, 4) for epw in (1, 2)]
+# 4 (tf32); epilogue warps per tensor-memory lane quarter (1 or 2); stream-K
+# items or not; operand-sharing cluster shapes (groups along M, along N).
+PLAIN_UNITS = [(f"kern_plain_ab{ab}_e{epw}_s{sk}", "kern_plain.cu",
+                [f"-DGB300_AB={ab}", f"-DGB300_EPW={epw}", f"-DGB300_SK={sk}"])
+               for ab in (2, 1, 4) for epw in (1, 2) for sk in (0, 1)]
 SHARED_UNITS = [(f"kern_shared_ab{ab}_m{mc}_n{nc}", "kern_shared.cu",
                  [f"-DGB300_AB={ab}", f"-DGB300_MC={mc}", f"-DGB300_NC={nc}"])
                 for ab in (2, 1, 4) for mc, nc in ((2, 1), (1, 2), (2, 2))]

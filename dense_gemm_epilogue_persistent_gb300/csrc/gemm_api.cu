@@ -116,7 +116,7 @@ struct gemm_handle {
   gemm_config_t forced_cfg{};
   gemm_config_t last{};
   uint64_t timeout_ns = kDefaultTimeoutNs;
-  VariantState variants[3][2][2][2][2][2];   // [ab 16/8/32][cta_group][k atoms][mc][nc][epw]
+  VariantState variants[3][2][2][2][2][2][2];   // [ab 16/8/32][cta_group][k atoms][mc][nc][epw][sk]
   int clusters_by_size[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};   // resident clusters of 1, 2, 4, 8 CTAs
   uint64_t config_gen = 0;
   LaunchEntry cache[kLaunchCacheEntries];
@@ -631,12 +631,13 @@ gemm_status_t prepare_launch(gemm_handle* h, const gemm_problem_t& p, LaunchEntr
   const int ab_bytes = dtype_bytes(dtypes->ab);
   const int csize = cfg.cta_group * cfg.cluster_m * cfg.cluster_n;
   const int ka = gb300::k_atoms(cfg.cta_group, cfg.tile_n);
+  const int sk = cfg.stream_k > 0 ? 1 : 0;
   const void* kern = gb300::kernel_for(ab_bytes, cfg.cta_group, ka, cfg.cluster_m,
-                                       cfg.cluster_n, cfg.epi_warps);
+                                       cfg.cluster_n, cfg.epi_warps, sk);
   if (!kern) return GEMM_ERR_UNSUPPORTED_CONFIG;
   VariantState& vs = h->variants[ab_bytes == 2 ? 0 : ab_bytes == 1 ? 1 : 2][cfg.cta_group - 1]
                                 [ka - 1][cfg.cluster_m - 1][cfg.cluster_n - 1]
-                                [cfg.epi_warps - 1];
+                                [cfg.epi_warps - 1][sk];
 
   cudaLaunchConfig_t lc{};
   cudaLaunchAttribute attr[1];

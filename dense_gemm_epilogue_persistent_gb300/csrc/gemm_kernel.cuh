@@ -323,9 +323,10 @@ __device__ __forceinline__ int sk_unit_of(long long i, const KernelParams& p) {
 // for that tile's owner); the head comes first, so that its partial is
 // published while the owned tail is computed, and no cluster ever waits for a
 // partial that is computed after a wait of its own.
+template <bool kSK>
 __device__ __forceinline__ Work work_item(int it, const KernelParams& p, int num_clusters) {
   Work w;
-  if (!p.sk_units) {
+  if (!kSK || !p.sk_units) {
     w.tile = item_tile(it, p, w.half);
     w.kb0 = 0;
     w.kb1 = p.k_blocks;
@@ -497,7 +498,7 @@ __device__ __forceinline__ uint32_t sub_bytes(int dt) {
 
 // ------------------------------------------------------------------ the kernel
 
-template <int CG, int AB_BYTES, int KA, int MC, int NC, int EPW>
+template <int CG, int AB_BYTES, int KA, int MC, int NC, int EPW, int SK>
 __global__ void __launch_bounds__(threads_for(EPW), 1)
 persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB,
@@ -518,6 +519,9 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   tn_geo.b_stage = tn_geo.b_atom * KA;
   tn_geo.chunks = BN / kEpiChunk;
   const TileN& T = tn_geo;
+  // Stream-K items (a separate instantiation, so that the other kernels carry
+  // none of its code).
+  constexpr bool kSK = SK != 0;
 
   // The next GEMM of the stream may start its prologue on SMs this grid leaves
   // idle; it touches global memory only after its own dependency wait below.
@@ -630,7 +634,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       long long st_empty = 0;
       const long long st_t0 = stat_clock();
       for (int it = cluster_id; ok && it < p.num_items; it += num_clusters) {
-        const Work wk = work_item(it, p, num_clusters);
+        const Work wk = work_item<kSK>(it, p, num_clusters);
         if (wk.empty) continue;
         const int half = wk.half;
         int tm, tn, tl;
@@ -719,7 +723,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       const long long st_t0 = stat_clock();
       bool ok = !p.inject_stall || wait_phase(never_bar, 0u, w, kWaitInjected);
       for (int it = cluster_id; ok && it < p.num_items; it += num_clusters) {
-        const Work wk = work_item(it, p, num_clusters);
+        const Work wk = work_item<kSK>(it, p, num_clusters);
         if (wk.empty) continue;
         const long long t_a = stat_clock();
         if (!wait_phase(tempty0 + 8u * acc, aph ^ 1u, w, kWaitMmaAcc)) break;
@@ -825,7 +829,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     struct Cursor { int it, j, nch, row0, col0, tl; };
     auto cursor_enter = [&](Cursor& cc) {
       for (; cc.it < p.num_items; cc.it += num_clusters) {
-        const Work wk = work_item(cc.it, p, num_clusters);
+        const Work wk = work_item<kSK>(cc.it, p, num_clusters);
         if (wk.empty || !wk.owner) continue;   // no C/X: nothing, or a stream-K partial
         const int half = wk.half;
         cc.nch = half < 0 ? T.chunks : T.chunks / 2;
@@ -896,7 +900,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     long long st_chunks = 0;
     const long long st_t0 = stat_clock();
     for (int it = cluster_id; ok && it < p.num_items; it += num_clusters) {
-      const Work wk = work_item(it, p, num_clusters);
+      const Work wk = work_item<kSK>(it, p, num_clusters);
       if (wk.empty) continue;
       const int half = wk.half;
       int tm, tn, tl;
@@ -934,7 +938,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         return reinterpret_cast<float4*>(p.sk_partials) +
                (size_t)(slot_cluster * CG + (int)rank) * (size_t)(BN * 32) + q * kSubRows + lane;
       };
-      if (!wk.owner) {
+      if (kSK && !wk.owner) {
         // ---- stream-K: the head of a tile another cluster owns.  Its
         // accumulator goes to this CTA's partial slot; once every epilogue
         // warp's stores are ordered, one thread publishes the slot's flag.
@@ -992,7 +996,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       // earlier k-blocks; wait until each has published its partial (after the C/X loads
       // above are under way).
       int sk_first = cluster_id;
-      if (p.sk_units) {
+      if (kSK && p.sk_units) {
         sk_first = sk_unit_of((long long)wk.tile * p.k_blocks, p);
         bool got = true;
         for (int c = sk_first; got && c < cluster_id; ++c) {
@@ -1067,7 +1071,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         // Stream-K owner: add the earlier k-blocks' partial sums, in the
         // order of the clusters that hold them (fp32 accumulators only).
-        for (int c = sk_first; c < cluster_id; ++c) {
+        for (int c = sk_first; kSK && c < cluster_id; ++c) {
           const float4* const src = partial_rows(c) + (size_t)j * 8 * 128;
 #pragma unroll
           for (int pc = 0; pc < 8; ++pc) {
@@ -1198,7 +1202,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         __syncwarp();
         if constexpr (kRingStats) st_issue += clock64() - t_i;
       }
-      if (p.sk_units && sk_first < cluster_id && ok) {
+      if (kSK && p.sk_units && sk_first < cluster_id && ok) {
         // Every epilogue warp has read the partials: clear their flags for
         // the next launch (which reads nothing before this grid completes).
         __syncwarp();

@@ -10,11 +10,11 @@ namespace gb300 {
 
 const void* GB300_SHARED_NAME(GB300_AB, GB300_MC, GB300_NC)(int cta_group, int ka) {
   if (cta_group == 1 && ka == 1)
-    return (const void*)&persistent_gemm_kernel<1, GB300_AB, 1, GB300_MC, GB300_NC, 1>;
+    return (const void*)&persistent_gemm_kernel<1, GB300_AB, 1, GB300_MC, GB300_NC, 1, 0>;
   if (cta_group == 1 && ka == 2)
-    return (const void*)&persistent_gemm_kernel<1, GB300_AB, 2, GB300_MC, GB300_NC, 1>;
+    return (const void*)&persistent_gemm_kernel<1, GB300_AB, 2, GB300_MC, GB300_NC, 1, 0>;
   if (cta_group == 2 && ka == 2)
-    return (const void*)&persistent_gemm_kernel<2, GB300_AB, 2, GB300_MC, GB300_NC, 1>;
+    return (const void*)&persistent_gemm_kernel<2, GB300_AB, 2, GB300_MC, GB300_NC, 1, 0>;
   return nullptr;
 }
 

@@ -8,23 +8,27 @@ namespace gb300 {
 // 128-byte K atoms per ring stage (ka: 1 or 2), the cluster's CTA groups
 // along M (mc, sharing B) and along N (nc, sharing A), each 1 or 2, and the
 // epilogue warps per tensor-memory lane quarter (epw: 1, or 2 for clusters of
-// one CTA group).  The tile width is a launch parameter.
+// one CTA group) and stream-K items (sk: 0, or 1 for clusters of one CTA
+// group).  The tile width is a launch parameter.
 //
-// kern_plain.cu, compiled once per input width and epw, holds the clusters
+// kern_plain.cu, compiled once per input width, epw and sk, holds the clusters
 // of one CTA group; kern_shared.cu, compiled once per input width and
 // (mc, nc), holds the operand-sharing clusters, whose TMA loads multicast.
 // Only the single-GPU library links the latter (GB300_MULTICAST = 1).
-#define GB300_PLAIN_ENTRIES(X) X(2, 1) X(1, 1) X(4, 1) X(2, 2) X(1, 2) X(4, 2)
+#define GB300_PLAIN_ENTRIES(X)                                                          \
+  X(2, 1, 0) X(1, 1, 0) X(4, 1, 0) X(2, 2, 0) X(1, 2, 0) X(4, 2, 0) X(2, 1, 1) X(1, 1, 1) \
+  X(4, 1, 1) X(2, 2, 1) X(1, 2, 1) X(4, 2, 1)
 #define GB300_SHARED_ENTRIES(X) \
   X(2, 2, 1) X(2, 1, 2) X(2, 2, 2) X(1, 2, 1) X(1, 1, 2) X(1, 2, 2) X(4, 2, 1) X(4, 1, 2) X(4, 2, 2)
 
 // (two levels, so that macro arguments are expanded before they are pasted)
-#define GB300_PLAIN_NAME_(ab, epw) kernel_plain_ab##ab##_e##epw
-#define GB300_PLAIN_NAME(ab, epw) GB300_PLAIN_NAME_(ab, epw)
+#define GB300_PLAIN_NAME_(ab, epw, sk) kernel_plain_ab##ab##_e##epw##_s##sk
+#define GB300_PLAIN_NAME(ab, epw, sk) GB300_PLAIN_NAME_(ab, epw, sk)
 #define GB300_SHARED_NAME_(ab, mc, nc) kernel_shared_ab##ab##_m##mc##_n##nc
 #define GB300_SHARED_NAME(ab, mc, nc) GB300_SHARED_NAME_(ab, mc, nc)
 
-#define GB300_DECLARE_PLAIN(ab, epw) const void* GB300_PLAIN_NAME(ab, epw)(int cta_group, int ka);
+#define GB300_DECLARE_PLAIN(ab, epw, sk) \
+  const void* GB300_PLAIN_NAME(ab, epw, sk)(int cta_group, int ka);
 #define GB300_DECLARE_SHARED(ab, mc, nc) \
   const void* GB300_SHARED_NAME(ab, mc, nc)(int cta_group, int ka);
 GB300_PLAIN_ENTRIES(GB300_DECLARE_PLAIN)
@@ -45,15 +49,16 @@ constexpr int k_atoms(int cta_group, int tile_n) {
   return (cta_group == 1 && tile_n > 128) ? 1 : 2;
 }
 
-inline const void* kernel_for(int ab_bytes, int cta_group, int ka, int mc, int nc, int epw = 1) {
+inline const void* kernel_for(int ab_bytes, int cta_group, int ka, int mc, int nc, int epw = 1,
+                              int sk = 0) {
   if (mc == 1 && nc == 1) {
-#define GB300_PICK_PLAIN(ab, e) \
-  if (ab_bytes == ab && epw == e) return GB300_PLAIN_NAME(ab, e)(cta_group, ka);
+#define GB300_PICK_PLAIN(ab, e, k) \
+  if (ab_bytes == ab && epw == e && sk == k) return GB300_PLAIN_NAME(ab, e, k)(cta_group, ka);
     GB300_PLAIN_ENTRIES(GB300_PICK_PLAIN)
 #undef GB300_PICK_PLAIN
     return nullptr;
   }
-  if (epw != 1) return nullptr;
+  if (epw != 1 || sk != 0) return nullptr;
 #if GB300_MULTICAST
 #define GB300_PICK_SHARED(ab, m, n) \
   if (ab_bytes == ab && mc == m && nc == n) return GB300_SHARED_NAME(ab, m, n)(cta_group, ka);
