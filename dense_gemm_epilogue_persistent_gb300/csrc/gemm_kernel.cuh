@@ -594,8 +594,10 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     for (int s = 0; s < 4 * E; ++s) mbar_init(cfull0 + 8u * s, 1);
     mbar_init(never_bar, 1);
     for (int q = 0; q < kMaxEpiWarps * kMaxChunks; ++q) mbar_init(rfull0 + 8u * q, 1);
-    mbar_init(pdone, 4 * EPW);
-    mbar_init(pread, 4 * EPW);
+    if constexpr (kSK) {
+      mbar_init(pdone, 4 * EPW);
+      mbar_init(pread, 4 * EPW);
+    }
     *abort_ptr = 0u;
     fence_barrier_init();
     if (p.k_blocks > 0) {                    // A and B are encoded only when K > 0
@@ -768,7 +770,8 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
               ok = false;
               break;
             }
-            umma<CG, KIND>(d_tmem, ad, bd, idesc, (kb != wk.kb0 || k != 0) ? 1u : 0u);
+            const bool accumulate = kSK ? (kb != wk.kb0 || k != 0) : (kb | k) != 0;
+            umma<CG, KIND>(d_tmem, ad, bd, idesc, accumulate ? 1u : 0u);
           }
           if (kDebug && !ok) break;
           umma_commit<CG, MULTI>(empty0 + 8u * s, all_mask);   // slot drained: tell every loader
@@ -973,7 +976,7 @@ persistent_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       // none).
       // Only lane 0 keeps the cursor; it decides and tells the warp.
       int batch0 = nchunks;
-      if (loads && (it + num_clusters >= p.num_items || p.sk_units)) {   // (stream-K: owned items come last)
+      if (loads && (it + num_clusters >= p.num_items || (kSK && p.sk_units))) {   // (stream-K: owned items come last)
         const int nb = ld.it == it ? (nchunks - ld.j + EPW - 1) / EPW : 0;   // this warp's
         if (lead && nb > 0 && (uint32_t)nb * (4u * EPW) * sub <= ring_bytes) {
           batch0 = ld.j;
