@@ -209,7 +209,11 @@ typedef struct {
 /* Create a handle for CUDA device `device`.  Checks the device is compute
  * capability 10.3 (GEMM_ERR_UNSUPPORTED_ARCH otherwise), caches its SM count
  * and shared-memory limit, resolves cuTensorMapEncodeTiled through the runtime
- * and allocates a 4-byte device status word.  *out is NULL on failure. */
+ * and allocates a 4-byte device status word and the stream-K workspace (one
+ * 128 x 256 fp32 partial slot and one flag per SM: 20 MB on 152 SMs; if that
+ * allocation fails the handle works without stream-K).  No later call on the
+ * handle allocates device memory except gemm_run_host (its staging buffers).
+ * *out is NULL on failure. */
 gemm_status_t gemm_create(gemm_handle_t* out, int device);
 
 /* Release the handle, its status word and its host-call workspace.  NULL is
