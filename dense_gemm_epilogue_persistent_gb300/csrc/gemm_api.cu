@@ -355,11 +355,14 @@ double plan_cost(const TileCost& t, int epw) {
 // the 2048^3 bf16 GEMM with fp32 C/D ran 26.2-26.7 us with stream-K on all 152
 // SMs (128 x 256 tiles or 256 x 256 pairs) against 20.5-20.9 us without, in
 // alternating runs; each cluster issues 16 % fewer k-blocks, but its MMA
-// issuer's cycles per stage rose from ~785 to ~1020 (ring statistics) while
-// the partial sums were stored and read, and a copy that skipped the partial
-// stores still took 23.0-24.7 us.  A single wave of 152 tiles (2432 x 2048 x
-// 2048) runs in the same ~21 us as 128, so the 24 idle SMs are not what the
-// single wave loses.  Forced (stream_k = 2) it runs, with its parity tests.
+// issuer's cycles per stage rose from ~710 to ~1020 (ring statistics), and
+// copies that skipped the partial stores and reads (timing only) still took
+// 21.2 us at ~930 cycles per stage: without stream-K every CTA works on the
+// same k-block at the same time, so each A/B line is fetched for many CTAs at
+// once, and the staggered k offsets of stream-K lose that.  A single wave of
+// 152 tiles (2432 x 2048 x 2048) runs in the same ~21 us as 128, so the 24
+// idle SMs are not what the single wave loses.  Forced (stream_k = 2) it
+// runs, with its parity tests.
 bool stream_k_pays(int64_t tiles, int64_t k_blocks, int64_t units) {
   (void)tiles; (void)k_blocks; (void)units;
   return false;
