@@ -483,7 +483,9 @@ gemm_status_t plan(const gemm_problem_t* pp, int sm_count, int smem_optin,
   // Strips of 12 CTA-group tile rows: with the serpentine strip order and the
   // K direction alternating per wave, 8192^3 reads 1.206 GB from DRAM per
   // launch at 12 (1.235 GB at 8, 1.514 GB at 4, 1.307 GB at 16) and runs 0.5-0.8 %
-  // faster than at 8; other shapes measured the same at 8 and 12.  A cluster
+  // faster than at 8; other shapes measured the same at 8 and 12 (re-checked on
+  // the current kernel, 3 x 3000 launches each: 12 734.5-735.7 us, 8 736.4-737.8,
+  // 10 737-740, 14 738-740, 16 738-741, 6 744-745).  A cluster
   // tile stacks cluster_m group tiles, so the strip counts 12 / cluster_m of
   // them (B shared along M, 8192^3: 1.29 GB read at 6 against 1.58 GB at 12).
   int group_m = forced && forced->group_m ? forced->group_m : std::max(1, 12 / mc);
